@@ -1,0 +1,412 @@
+/*
+ * msda_oracle.c -- plain, slow, single-threaded fp64 CPU oracle for the
+ * multi-scale deformable attention (MSDeformAttn) core.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this file: only the tests, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header, table or constant
+ * with the CUDA library; it is written straight from the pages' definition.
+ *
+ * Citation key (the pages this follows):
+ *   [MSDA-tut]  "可变形注意力：多尺度稀疏采样与视觉检测实战解析" (bjdmk.com.cn)
+ *               -- §2.2 multi-scale formula, §2.3 bilinear interpolation,
+ *                  §3.1 interface, §3.2 the grid_sample module.
+ *   [DDETR-tut] "可变形 DETR：加速收敛的稀疏注意力检测器" (freeguideonline.com)
+ *               -- §3.2 single-scale formula, §3.3 multi-scale formula,
+ *                  §6 forward pseudocode (location = reference + offset / scale).
+ *   [DDETR-dep] "Deformable DETR的本质定位与设计动机" deployment notes
+ *               (un.csdn.net/8fh7s5u7wxgo) -- §2.2 worked example.
+ *
+ * Layouts (all row-major, contiguous):
+ *   value              [N][Len_in][n_heads][head_dim]         ([MSDA-tut] §3.2, value.view)
+ *   spatial_shapes     [n_levels][2] = (H_l, W_l)              ([MSDA-tut] §3.1)
+ *   level_start_index  [n_levels]                              ([MSDA-tut] §3.1)
+ *   sampling_locations [N][Len_q][n_heads][n_levels][n_points][2], (x, y) in [0,1]
+ *   attention_weights  [N][Len_q][n_heads][n_levels][n_points]
+ *   output             [N][Len_q][n_heads*head_dim]  (head m owns channels m*D..m*D+D-1)
+ *   reference_points   [N][Len_q][n_levels][2]
+ *   sampling_offsets   [N][Len_q][n_heads][n_levels][n_points][2], in pixels of level l
+ *   attention_logits   [N][Len_q][n_heads][n_levels*n_points]
+ *
+ * Readings taken where the pages are silent or disagree:
+ *   - normalised -> pixel: px = loc_x * W_l - 0.5, py = loc_y * H_l - 0.5
+ *     (grid_sample with align_corners=False, [MSDA-tut] §2.3 and §3.2).
+ *   - zero padding per corner: a corner outside [0,W)x[0,H) contributes 0, the
+ *     other corners keep their weights ([MSDA-tut] §2.3, padding_mode='zeros').
+ *   - the softmax runs over all n_levels*n_points logits of one (query, head)
+ *     ([MSDA-tut] §3.2 code: view(..., n_levels*n_points), softmax(dim=-1)).
+ *   - fused offsets are in pixels of their level: loc = ref + off / (W_l, H_l)
+ *     ([DDETR-tut] §6: reference_points + sampling_offsets / scale_factors).
+ *   - where floating point decides an integer (which pixel is the lower-left
+ *     corner), the decision is taken in the fp32 arithmetic the CUDA kernels
+ *     use, written out below in decide_floor_*; every weight, value and sum
+ *     after that decision is fp64.  Near an exact integer the two precisions
+ *     may pick neighbouring cells; bilinear interpolation is continuous there,
+ *     so only the (one-sided) location gradient depends on the choice.
+ *
+ * Return value of every entry point: 0 on success, -1 on a bad argument.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* Floor decisions in fp32 (the kernels' precision).                          */
+/* Compiled with -ffp-contract=off so that each float operation rounds once.  */
+/* ------------------------------------------------------------------------- */
+
+/* Unfused path: the corner is floor(RN(RN(loc * size) - 0.5)). */
+static int64_t decide_floor_unfused(double loc, int64_t size)
+{
+    float lf = (float)loc;
+    float sf = (float)size;
+    float p = lf * sf;
+    float ph = p - 0.5f;
+    return (int64_t)floorf(ph);
+}
+
+/* Fused path: the corner is floor(RN(RN(ref * size) + RN(off - 0.5))). */
+static int64_t decide_floor_fused(double ref, double off, int64_t size)
+{
+    float rf = (float)ref;
+    float of = (float)off;
+    float sf = (float)size;
+    float p = rf * sf;
+    float t = of - 0.5f;
+    float s = p + t;
+    return (int64_t)floorf(s);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Step a1: sampling location = reference point + offset / (W_l, H_l).        */
+/* [DDETR-tut] §6; [MSDA-tut] §3.2 (the scale and unscale pair).              */
+/* ------------------------------------------------------------------------- */
+int msda_oracle_locations(int64_t N, int64_t Len_q, int64_t n_heads, int64_t n_levels,
+                          int64_t n_points, const int64_t *spatial_shapes,
+                          const double *reference_points, const double *sampling_offsets,
+                          double *sampling_locations)
+{
+    if (N < 0 || Len_q < 0 || n_heads < 0 || n_levels < 0 || n_points < 0) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t q = 0; q < Len_q; ++q)
+            for (int64_t m = 0; m < n_heads; ++m)
+                for (int64_t l = 0; l < n_levels; ++l) {
+                    double H = (double)spatial_shapes[2 * l + 0];
+                    double W = (double)spatial_shapes[2 * l + 1];
+                    const double *ref = reference_points + ((n * Len_q + q) * n_levels + l) * 2;
+                    for (int64_t k = 0; k < n_points; ++k) {
+                        int64_t i = ((((n * Len_q + q) * n_heads + m) * n_levels + l) * n_points + k) * 2;
+                        sampling_locations[i + 0] = ref[0] + sampling_offsets[i + 0] / W;
+                        sampling_locations[i + 1] = ref[1] + sampling_offsets[i + 1] / H;
+                    }
+                }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Step a2: A = softmax over the n_levels*n_points logits of one (q, head),   */
+/* max-subtracted.  [MSDA-tut] §3.2: softmax(dim=-1) over levels*points.      */
+/* ------------------------------------------------------------------------- */
+int msda_oracle_softmax(int64_t rows, int64_t cols, const double *logits, double *weights)
+{
+    if (rows < 0 || cols <= 0) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *x = logits + r * cols;
+        double *y = weights + r * cols;
+        double mx = x[0];
+        for (int64_t j = 1; j < cols; ++j)
+            if (x[j] > mx) mx = x[j];
+        double sum = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            y[j] = exp(x[j] - mx);
+            sum += y[j];
+        }
+        for (int64_t j = 0; j < cols; ++j) y[j] /= sum;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Shared by forward and backward of both paths: one bilinear sample.         */
+/* [MSDA-tut] §2.3: the four integer neighbours of (x, y), weights            */
+/* (1-|dx|)(1-|dy|), a neighbour outside the map reads as zero.               */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    int64_t x0, y0;     /* lower corner (column, row) in pixels of the level */
+    double fx, fy;      /* px - x0, py - y0 */
+    int64_t row[4];     /* value row (index into Len_in) of corner c, -1 if outside */
+    double w[4];        /* bilinear weight of corner c (0 is kept for outside corners) */
+} corners_t;
+/* corner order c = 0:(x0,y0) 1:(x0+1,y0) 2:(x0,y0+1) 3:(x0+1,y0+1) */
+
+static void make_corners(int64_t x0, int64_t y0, double fx, double fy, int64_t H, int64_t W,
+                         int64_t start, corners_t *c)
+{
+    c->x0 = x0; c->y0 = y0; c->fx = fx; c->fy = fy;
+    for (int j = 0; j < 2; ++j)
+        for (int i = 0; i < 2; ++i) {
+            int ci = 2 * j + i;
+            int64_t xc = x0 + i, yc = y0 + j;
+            c->w[ci] = (i ? fx : 1.0 - fx) * (j ? fy : 1.0 - fy);
+            c->row[ci] = (xc >= 0 && xc < W && yc >= 0 && yc < H) ? start + yc * W + xc : -1;
+        }
+}
+
+static void corners_unfused(double lx, double ly, int64_t H, int64_t W, int64_t start, corners_t *c)
+{
+    int64_t x0 = decide_floor_unfused(lx, W);
+    int64_t y0 = decide_floor_unfused(ly, H);
+    double px = lx * (double)W - 0.5;   /* align_corners=False */
+    double py = ly * (double)H - 0.5;
+    make_corners(x0, y0, px - (double)x0, py - (double)y0, H, W, start, c);
+}
+
+static void corners_fused(double rx, double ry, double ox, double oy, int64_t H, int64_t W,
+                          int64_t start, corners_t *c)
+{
+    int64_t x0 = decide_floor_fused(rx, ox, W);
+    int64_t y0 = decide_floor_fused(ry, oy, H);
+    double lx = rx + ox / (double)W;    /* step a1 */
+    double ly = ry + oy / (double)H;
+    double px = lx * (double)W - 0.5;   /* step a3 */
+    double py = ly * (double)H - 0.5;
+    make_corners(x0, y0, px - (double)x0, py - (double)y0, H, W, start, c);
+}
+
+static int check_levels(int64_t Len_in, int64_t n_levels, const int64_t *shapes, const int64_t *starts)
+{
+    int64_t expect = 0;
+    for (int64_t l = 0; l < n_levels; ++l) {
+        if (shapes[2 * l] <= 0 || shapes[2 * l + 1] <= 0) return -1;
+        if (starts[l] != expect) return -1;
+        expect += shapes[2 * l] * shapes[2 * l + 1];
+    }
+    return expect == Len_in ? 0 : -1;
+}
+
+/* sample[d] = sum over in-map corners of w_c * value[n][row_c][m][d] */
+static void gather_sample(const double *value, int64_t Len_in, int64_t n_heads, int64_t D,
+                          int64_t n, int64_t m, const corners_t *c, double *sample)
+{
+    for (int64_t d = 0; d < D; ++d) sample[d] = 0.0;
+    for (int ci = 0; ci < 4; ++ci) {
+        if (c->row[ci] < 0) continue;
+        const double *v = value + ((n * Len_in + c->row[ci]) * n_heads + m) * D;
+        for (int64_t d = 0; d < D; ++d) sample[d] += c->w[ci] * v[d];
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Steps a3-a5: out[n][q][m*D+d] = sum_{l,k} A[n,q,m,l,k] * sample_{l,k}[d]  */
+/* [MSDA-tut] §2.2 (inner sum of the MSDeformAttn formula), §3.2 steps 4-5;   */
+/* [DDETR-tut] §3.3.  `fused` selects how the corner is located.              */
+/* ------------------------------------------------------------------------- */
+static int forward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, int64_t D,
+                        int64_t Len_q, int64_t n_levels, int64_t n_points,
+                        const double *value, const int64_t *shapes, const int64_t *starts,
+                        const double *loc_or_ref, const double *offsets, const double *attn,
+                        double *out)
+{
+    if (N < 0 || Len_in < 0 || n_heads <= 0 || D <= 0 || Len_q < 0 || n_levels <= 0 || n_points <= 0)
+        return -1;
+    if (check_levels(Len_in, n_levels, shapes, starts)) return -1;
+    double *sample = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!sample) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t q = 0; q < Len_q; ++q)
+            for (int64_t m = 0; m < n_heads; ++m) {
+                double *o = out + ((n * Len_q + q) * n_heads + m) * D;
+                for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+                for (int64_t l = 0; l < n_levels; ++l) {
+                    int64_t H = shapes[2 * l], W = shapes[2 * l + 1];
+                    for (int64_t k = 0; k < n_points; ++k) {
+                        int64_t s = (((n * Len_q + q) * n_heads + m) * n_levels + l) * n_points + k;
+                        corners_t c;
+                        if (fused) {
+                            const double *ref = loc_or_ref + ((n * Len_q + q) * n_levels + l) * 2;
+                            corners_fused(ref[0], ref[1], offsets[2 * s], offsets[2 * s + 1], H, W,
+                                          starts[l], &c);
+                        } else {
+                            corners_unfused(loc_or_ref[2 * s], loc_or_ref[2 * s + 1], H, W, starts[l], &c);
+                        }
+                        gather_sample(value, Len_in, n_heads, D, n, m, &c, sample);
+                        for (int64_t d = 0; d < D; ++d) o[d] += attn[s] * sample[d];
+                    }
+                }
+            }
+    free(sample);
+    return 0;
+}
+
+int msda_oracle_forward(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
+                        int64_t n_levels, int64_t n_points, const double *value,
+                        const int64_t *spatial_shapes, const int64_t *level_start_index,
+                        const double *sampling_locations, const double *attention_weights,
+                        double *output)
+{
+    return forward_impl(0, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+                        level_start_index, sampling_locations, NULL, attention_weights, output);
+}
+
+/* Steps a1-a5: softmax (a2) of the raw logits, then the sampling with the
+ * location taken from the reference point and the pixel offset (a1). */
+int msda_oracle_forward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
+                              int64_t n_levels, int64_t n_points, const double *value,
+                              const int64_t *spatial_shapes, const int64_t *level_start_index,
+                              const double *reference_points, const double *sampling_offsets,
+                              const double *attention_logits, double *output)
+{
+    int64_t rows = N * Len_q * n_heads, cols = n_levels * n_points;
+    if (rows < 0 || cols <= 0) return -1;
+    double *attn = (double *)malloc(sizeof(double) * (size_t)(rows * cols + 1));
+    if (!attn) return -1;
+    int rc = msda_oracle_softmax(rows, cols, attention_logits, attn);
+    if (!rc)
+        rc = forward_impl(1, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+                          level_start_index, reference_points, sampling_offsets, attn, output);
+    free(attn);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Steps a6-a8: the backward of a3-a5, derived from the bilinear formula of   */
+/* [MSDA-tut] §2.3 (continuous and differentiable, so the gradient reaches    */
+/* the offset branch).  For one sample s with corners c and weights w_c:      */
+/*   grad_attn[s]   = sum_d g[d] * sample_s[d]                                */
+/*   d sample/d px  = (1-fy)(v1-v0) + fy(v3-v2)      (corner order above)      */
+/*   d sample/d py  = (1-fx)(v2-v0) + fx(v3-v1)                                */
+/*   grad_loc_x     = A * sum_d g[d] d sample[d]/d px * W   (px = x*W - 0.5)   */
+/*   grad_value[row_c] += A * w_c * g                    (in-map corners only) */
+/* A corner outside the map has value 0 here as in the forward.  grad_value   */
+/* is overwritten (zeroed first).                                             */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    double *grad_value, *grad_loc, *grad_attn;
+} grads_t;
+
+static int backward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, int64_t D,
+                         int64_t Len_q, int64_t n_levels, int64_t n_points, const double *value,
+                         const int64_t *shapes, const int64_t *starts, const double *loc_or_ref,
+                         const double *offsets, const double *attn, const double *grad_out,
+                         grads_t *gr)
+{
+    if (N < 0 || Len_in < 0 || n_heads <= 0 || D <= 0 || Len_q < 0 || n_levels <= 0 || n_points <= 0)
+        return -1;
+    if (check_levels(Len_in, n_levels, shapes, starts)) return -1;
+    double *v = (double *)malloc(sizeof(double) * (size_t)(4 * D));
+    if (!v) return -1;
+    for (int64_t i = 0; i < N * Len_in * n_heads * D; ++i) gr->grad_value[i] = 0.0;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t q = 0; q < Len_q; ++q)
+            for (int64_t m = 0; m < n_heads; ++m) {
+                const double *g = grad_out + ((n * Len_q + q) * n_heads + m) * D;
+                for (int64_t l = 0; l < n_levels; ++l) {
+                    int64_t H = shapes[2 * l], W = shapes[2 * l + 1];
+                    for (int64_t k = 0; k < n_points; ++k) {
+                        int64_t s = (((n * Len_q + q) * n_heads + m) * n_levels + l) * n_points + k;
+                        corners_t c;
+                        if (fused) {
+                            const double *ref = loc_or_ref + ((n * Len_q + q) * n_levels + l) * 2;
+                            corners_fused(ref[0], ref[1], offsets[2 * s], offsets[2 * s + 1], H, W,
+                                          starts[l], &c);
+                        } else {
+                            corners_unfused(loc_or_ref[2 * s], loc_or_ref[2 * s + 1], H, W, starts[l], &c);
+                        }
+                        for (int ci = 0; ci < 4; ++ci)
+                            for (int64_t d = 0; d < D; ++d)
+                                v[ci * D + d] = c.row[ci] < 0 ? 0.0
+                                    : value[((n * Len_in + c.row[ci]) * n_heads + m) * D + d];
+                        double ga = 0.0, gx = 0.0, gy = 0.0;
+                        for (int64_t d = 0; d < D; ++d) {
+                            double smp = c.w[0] * v[d] + c.w[1] * v[D + d] + c.w[2] * v[2 * D + d]
+                                       + c.w[3] * v[3 * D + d];
+                            double dsx = (1.0 - c.fy) * (v[D + d] - v[d]) + c.fy * (v[3 * D + d] - v[2 * D + d]);
+                            double dsy = (1.0 - c.fx) * (v[2 * D + d] - v[d]) + c.fx * (v[3 * D + d] - v[D + d]);
+                            ga += g[d] * smp;
+                            gx += g[d] * dsx;
+                            gy += g[d] * dsy;
+                        }
+                        gr->grad_attn[s] = ga;
+                        gr->grad_loc[2 * s + 0] = attn[s] * gx * (double)W;
+                        gr->grad_loc[2 * s + 1] = attn[s] * gy * (double)H;
+                        for (int ci = 0; ci < 4; ++ci) {
+                            if (c.row[ci] < 0) continue;
+                            double *gv = gr->grad_value + ((n * Len_in + c.row[ci]) * n_heads + m) * D;
+                            for (int64_t d = 0; d < D; ++d) gv[d] += attn[s] * c.w[ci] * g[d];
+                        }
+                    }
+                }
+            }
+    free(v);
+    return 0;
+}
+
+int msda_oracle_backward(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
+                         int64_t n_levels, int64_t n_points, const double *value,
+                         const int64_t *spatial_shapes, const int64_t *level_start_index,
+                         const double *sampling_locations, const double *attention_weights,
+                         const double *grad_output, double *grad_value,
+                         double *grad_sampling_locations, double *grad_attention_weights)
+{
+    grads_t gr = {grad_value, grad_sampling_locations, grad_attention_weights};
+    return backward_impl(0, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+                         level_start_index, sampling_locations, NULL, attention_weights,
+                         grad_output, &gr);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Step a9: backward of the fused call, by the chain rule through a1 and a2.  */
+/*   loc = ref + off / W            => grad_off_x = grad_loc_x / W,            */
+/*                                     grad_ref_x[n,q,l] = sum_{m,k} grad_loc_x */
+/*   A = softmax(logit) over j      => grad_logit_j = A_j (gA_j - sum_i A_i gA_i) */
+/* ------------------------------------------------------------------------- */
+int msda_oracle_backward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
+                               int64_t n_levels, int64_t n_points, const double *value,
+                               const int64_t *spatial_shapes, const int64_t *level_start_index,
+                               const double *reference_points, const double *sampling_offsets,
+                               const double *attention_logits, const double *grad_output,
+                               double *grad_value, double *grad_reference_points,
+                               double *grad_sampling_offsets, double *grad_attention_logits)
+{
+    int64_t rows = N * Len_q * n_heads, cols = n_levels * n_points;
+    if (rows < 0 || cols <= 0) return -1;
+    size_t ns = (size_t)(rows * cols + 1);
+    double *attn = (double *)malloc(sizeof(double) * ns);
+    double *gloc = (double *)malloc(sizeof(double) * 2 * ns);
+    double *gattn = (double *)malloc(sizeof(double) * ns);
+    int rc = -1;
+    if (!attn || !gloc || !gattn) goto done;
+    rc = msda_oracle_softmax(rows, cols, attention_logits, attn);
+    if (rc) goto done;
+    grads_t gr = {grad_value, gloc, gattn};
+    rc = backward_impl(1, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+                       level_start_index, reference_points, sampling_offsets, attn, grad_output, &gr);
+    if (rc) goto done;
+    for (int64_t i = 0; i < N * Len_q * n_levels * 2; ++i) grad_reference_points[i] = 0.0;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t q = 0; q < Len_q; ++q)
+            for (int64_t m = 0; m < n_heads; ++m) {
+                int64_t r = (n * Len_q + q) * n_heads + m;
+                for (int64_t l = 0; l < n_levels; ++l) {
+                    double H = (double)spatial_shapes[2 * l], W = (double)spatial_shapes[2 * l + 1];
+                    double *gref = grad_reference_points + ((n * Len_q + q) * n_levels + l) * 2;
+                    for (int64_t k = 0; k < n_points; ++k) {
+                        int64_t s = r * cols + l * n_points + k;
+                        grad_sampling_offsets[2 * s + 0] = gloc[2 * s + 0] / W;
+                        grad_sampling_offsets[2 * s + 1] = gloc[2 * s + 1] / H;
+                        gref[0] += gloc[2 * s + 0];
+                        gref[1] += gloc[2 * s + 1];
+                    }
+                }
+                double dot = 0.0;
+                for (int64_t j = 0; j < cols; ++j) dot += attn[r * cols + j] * gattn[r * cols + j];
+                for (int64_t j = 0; j < cols; ++j)
+                    grad_attention_logits[r * cols + j] = attn[r * cols + j] * (gattn[r * cols + j] - dot);
+            }
+done:
+    free(attn);
+    free(gloc);
+    free(gattn);
+    return rc;
+}

@@ -1,0 +1,418 @@
+"""Pins of the fp64 oracle to facts other than itself.
+
+Each pin returns (error, tolerance).  They are used twice: on the built oracle
+(every pin must hold) and on deliberately broken copies of it
+(test_oracle_mutants.py: at least one pin must fail for every planted bug).
+
+What pins what:
+  worked_example      step a1 against the worked example printed in the
+                      Deformable DETR deployment notes, section 2.2, run both
+                      through the location step and through the fused forward.
+  softmax_closed      step a2: softmax(log[1,2,3,4]) = [.1,.2,.3,.4], overflow-safe
+                      at logits 1000/1001, zero logits give 1/(L*K).
+  constant_map        steps a3-a5: a constant map c returns
+                      c * sum_s A_s * s(px) * s(py), s(p) = max(0, min(1, p+1, size-p)).
+  pixel_centres       sampling at pixel centres is a pure gather.
+  linear_ramp         a map linear in (x, y) is reproduced exactly inside the map.
+  far_outside         samples far outside every level give exactly 0.
+  grid_sample         torch.nn.functional.grid_sample (bilinear, zeros,
+                      align_corners=False) in float64 on the CPU, one call per
+                      level as in the tutorial's module, agrees to 1e-12.
+  dense_tent          out = Wmat @ value with Wmat built from the tent form
+                      max(0,1-|px-x|) max(0,1-|py-y|) over every pixel.
+  backward_autograd   steps a6-a8 against torch autograd through grid_sample.
+  backward_fd         central finite differences of the oracle forward.
+  adjoint             <grad_value, dV> = <g, forward(dV)> (the forward is linear in value).
+  fused_*             a9 and the fused forward: finite differences through
+                      a1-a2, sum of logit gradients is 0, composition with a1/a2.
+"""
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _err(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.shape != b.shape:
+        return math.inf
+    if a.size == 0:
+        return 0.0
+    d = np.abs(a - b)
+    if not np.all(np.isfinite(d)):
+        return math.inf
+    return float(d.max())
+
+
+def _rel(a, b):
+    scale = max(float(np.abs(np.asarray(b)).max()), 1e-300) if np.asarray(b).size else 1.0
+    return _err(a, b) / scale
+
+
+def _tiny(seed=7, loc_lo=-0.1, loc_hi=1.1, levels=((8, 8), (4, 4)), N=1, M=2, D=8, Lq=20, K=2):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shapes = np.asarray(levels, dtype=np.int64)
+    starts = workloads.level_start_index(shapes)
+    S = int((shapes[:, 0] * shapes[:, 1]).sum())
+    L = len(levels)
+    value = rng.standard_normal((N, S, M, D))
+    loc = rng.uniform(loc_lo, loc_hi, size=(N, Lq, M, L, K, 2))
+    attn = oracle.softmax(rng.standard_normal((N, Lq, M, L * K))).reshape(N, Lq, M, L, K)
+    g = rng.standard_normal((N, Lq, M * D))
+    return dict(value=value, shapes=shapes, starts=starts, loc=loc, attn=attn, g=g,
+                N=N, S=S, M=M, D=D, Lq=Lq, L=L, K=K)
+
+
+def _px(loc, size):
+    return loc * size - 0.5
+
+
+# --------------------------------------------------------------------------- a1
+def read_worked_example():
+    rows = []
+    with open(os.path.join(GOLDEN, "worked_example_locations.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append([float(t) for t in line.split()])
+    return np.asarray(rows)
+
+
+def pin_worked_example():
+    rows = read_worked_example()
+    worst = 0.0
+    for (H, W) in [(100, 167), (13, 21), (1, 1), (64, 64)]:
+        shapes = np.asarray([[H, W]], dtype=np.int64)
+        ref = np.zeros((1, 1, 1, 2))
+        ref[0, 0, 0] = rows[0, 0:2]
+        off = np.zeros((1, 1, 1, 1, 4, 2))
+        off[0, 0, 0, 0, :, 0] = rows[:, 2] * W
+        off[0, 0, 0, 0, :, 1] = rows[:, 3] * H
+        loc = oracle.locations(shapes, ref, off)
+        worst = max(worst, _err(loc[0, 0, 0, 0], rows[:, 4:6]))
+    # the same points seen through the fused forward: a ramp map whose two
+    # channels are the pixel column and row, one sample at a time (A = 1)
+    H, W = 100, 167
+    shapes = np.asarray([[H, W]], dtype=np.int64)
+    ys, xs = np.meshgrid(np.arange(H), np.arange(W), indexing="ij")
+    value = np.stack([xs.ravel(), ys.ravel()], axis=-1).astype(np.float64)[None, :, None, :]
+    for r in rows:
+        ref = np.asarray(r[0:2]).reshape(1, 1, 1, 2)
+        off = np.asarray([r[2] * W, r[3] * H]).reshape(1, 1, 1, 1, 1, 2)
+        out = oracle.forward_fused(value, shapes, np.zeros(1, np.int64), ref, off, np.zeros((1, 1, 1, 1)))
+        got = np.asarray([(out[0, 0, 0] + 0.5) / W, (out[0, 0, 1] + 0.5) / H])
+        worst = max(worst, _err(got, r[4:6]))
+    return worst, 1e-12
+
+
+# --------------------------------------------------------------------------- a2
+def pin_softmax_closed():
+    worst = _err(oracle.softmax(np.log([[1.0, 2.0, 3.0, 4.0]])), [[0.1, 0.2, 0.3, 0.4]])
+    e = math.e
+    worst = max(worst, _err(oracle.softmax(np.asarray([[1000.0, 1001.0]])), [[1 / (1 + e), e / (1 + e)]]))
+    worst = max(worst, _err(oracle.softmax(np.zeros((3, 16))), np.full((3, 16), 1 / 16)))
+    x = np.random.Generator(np.random.PCG64(3)).standard_normal((5, 12))
+    worst = max(worst, _err(oracle.softmax(x + 37.25), oracle.softmax(x)))
+    return worst, 1e-14
+
+
+# --------------------------------------------------------------------------- a3-a5
+def _coverage(p, size):
+    return np.maximum(0.0, np.minimum(np.minimum(1.0, p + 1.0), size - p))
+
+
+def pin_constant_map():
+    t = _tiny(seed=11, loc_lo=-0.6, loc_hi=1.6, levels=((8, 8), (4, 4), (1, 5), (3, 1)), Lq=40, K=3)
+    c = 1.7
+    value = np.full_like(t["value"], c)
+    out = oracle.forward(value, t["shapes"], t["starts"], t["loc"], t["attn"])
+    expect = np.zeros((t["N"], t["Lq"], t["M"]))
+    for l, (H, W) in enumerate(t["shapes"]):
+        sx = _coverage(_px(t["loc"][..., l, :, 0], W), W)
+        sy = _coverage(_px(t["loc"][..., l, :, 1], H), H)
+        expect += c * (t["attn"][..., l, :] * sx * sy).sum(-1)
+    expect = np.repeat(expect[..., None], t["D"], axis=-1).reshape(t["N"], t["Lq"], -1)
+    return _err(out, expect), 1e-12
+
+
+def pin_pixel_centres():
+    t = _tiny(seed=12, levels=((8, 8), (4, 4), (2, 7)), Lq=30, K=3)
+    rng = np.random.Generator(np.random.PCG64(5))
+    loc = np.zeros_like(t["loc"])
+    expect = np.zeros((t["N"], t["Lq"], t["M"], t["D"]))
+    for l, (H, W) in enumerate(t["shapes"]):
+        i = rng.integers(0, W, size=loc.shape[:3] + (t["K"],))
+        j = rng.integers(0, H, size=loc.shape[:3] + (t["K"],))
+        loc[..., l, :, 0] = (i + 0.5) / W
+        loc[..., l, :, 1] = (j + 0.5) / H
+        for n in range(t["N"]):
+            for q in range(t["Lq"]):
+                for m in range(t["M"]):
+                    for k in range(t["K"]):
+                        row = t["starts"][l] + j[n, q, m, k] * W + i[n, q, m, k]
+                        expect[n, q, m] += t["attn"][n, q, m, l, k] * t["value"][n, row, m]
+    out = oracle.forward(t["value"], t["shapes"], t["starts"], loc, t["attn"])
+    return _err(out, expect.reshape(out.shape)), 1e-12
+
+
+def pin_linear_ramp():
+    t = _tiny(seed=13, levels=((8, 8), (4, 6), (5, 2)), Lq=30, K=3, M=3, D=4)
+    rng = np.random.Generator(np.random.PCG64(6))
+    L, M, D = t["L"], t["M"], t["D"]
+    alpha, beta, gamma = (rng.standard_normal((L, M, D)) for _ in range(3))
+    value = np.zeros_like(t["value"])
+    loc = np.zeros_like(t["loc"])
+    expect = np.zeros((t["N"], t["Lq"], M, D))
+    for l, (H, W) in enumerate(t["shapes"]):
+        ys, xs = np.meshgrid(np.arange(H), np.arange(W), indexing="ij")
+        lvl = (alpha[l][None] * xs.ravel()[:, None, None] + beta[l][None] * ys.ravel()[:, None, None]
+               + gamma[l][None])
+        value[:, t["starts"][l]:t["starts"][l] + H * W] = lvl[None]
+        # keep all four corners inside: px in [0, W-1], py in [0, H-1]
+        loc[..., l, :, 0] = (rng.uniform(0, W - 1, size=loc.shape[:3] + (t["K"],)) + 0.5) / W
+        loc[..., l, :, 1] = (rng.uniform(0, H - 1, size=loc.shape[:3] + (t["K"],)) + 0.5) / H
+        px = _px(loc[..., l, :, 0], W)
+        py = _px(loc[..., l, :, 1], H)
+        A = t["attn"][..., l, :]
+        expect += np.einsum("nqmk,md->nqmd", A * px, alpha[l]) + np.einsum("nqmk,md->nqmd", A * py, beta[l]) \
+            + np.einsum("nqmk,md->nqmd", A, gamma[l])
+    out = oracle.forward(value, t["shapes"], t["starts"], loc, t["attn"])
+    return _err(out, expect.reshape(out.shape)), 1e-11
+
+
+def pin_far_outside():
+    t = _tiny(seed=14)
+    loc = t["loc"].copy()
+    far = np.asarray([[-5.0, 0.5], [2.0, 0.5], [0.5, -3.0], [0.5, 7.0], [-1.0, -1.0], [9.0, 9.0]])
+    idx = np.arange(loc[..., 0].size) % len(far)
+    loc.reshape(-1, 2)[:] = far[idx]
+    out = oracle.forward(t["value"], t["shapes"], t["starts"], loc, t["attn"])
+    return float(np.abs(out).max()), 0.0
+
+
+def _grid_sample_forward(value, shapes, starts, loc, attn):
+    """The tutorial module's per-level grid_sample path, in float64 torch."""
+    N, S, M, D = value.shape
+    _, Lq, _, L, K, _ = loc.shape
+    out = 0
+    for l in range(L):
+        H, W = int(shapes[l, 0]), int(shapes[l, 1])
+        s0 = int(starts[l])
+        v_l = value[:, s0:s0 + H * W].reshape(N, H, W, M, D).permute(0, 3, 4, 1, 2).reshape(N * M, D, H, W)
+        grid = (2.0 * loc[:, :, :, l] - 1.0).permute(0, 2, 1, 3, 4).reshape(N * M, Lq, K, 2)
+        smp = F.grid_sample(v_l, grid, mode="bilinear", padding_mode="zeros", align_corners=False)
+        a = attn[:, :, :, l].permute(0, 2, 1, 3).reshape(N * M, 1, Lq, K)
+        out = out + (smp * a).sum(-1)                       # (N*M, D, Lq)
+    return out.reshape(N, M, D, Lq).permute(0, 3, 1, 2).reshape(N, Lq, M * D)
+
+
+def pin_grid_sample():
+    worst = 0.0
+    for seed, lv in [(15, ((8, 8), (4, 4))), (16, ((5, 9), (3, 2), (1, 1)))]:
+        t = _tiny(seed=seed, levels=lv, loc_lo=-0.3, loc_hi=1.3, Lq=25, K=3, M=3, D=5)
+        out = oracle.forward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"])
+        ref = _grid_sample_forward(torch.from_numpy(t["value"]), t["shapes"], t["starts"],
+                                   torch.from_numpy(t["loc"]), torch.from_numpy(t["attn"])).numpy()
+        worst = max(worst, _err(out, ref))
+    return worst, 1e-12
+
+
+def pin_dense_tent():
+    t = _tiny(seed=17, levels=((6, 7), (3, 4)), loc_lo=-0.2, loc_hi=1.2, Lq=15, K=3, M=2, D=3)
+    out = oracle.forward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"])
+    N, Lq, M = t["N"], t["Lq"], t["M"]
+    expect = np.zeros((N, Lq, M, t["D"]))
+    for n in range(N):
+        for m in range(M):
+            Wmat = np.zeros((Lq, t["S"]))
+            for l, (H, W) in enumerate(t["shapes"]):
+                ys, xs = np.meshgrid(np.arange(H), np.arange(W), indexing="ij")
+                cols = t["starts"][l] + ys.ravel() * W + xs.ravel()
+                for q in range(Lq):
+                    for k in range(t["K"]):
+                        px = _px(t["loc"][n, q, m, l, k, 0], W)
+                        py = _px(t["loc"][n, q, m, l, k, 1], H)
+                        tent = np.maximum(0, 1 - np.abs(px - xs.ravel())) * np.maximum(0, 1 - np.abs(py - ys.ravel()))
+                        Wmat[q, cols] += t["attn"][n, q, m, l, k] * tent
+            expect[n, :, m] = Wmat @ t["value"][n, :, m]
+    return _err(out, expect.reshape(out.shape)), 1e-12
+
+
+# --------------------------------------------------------------------------- a6-a8
+def pin_backward_autograd():
+    t = _tiny(seed=18, levels=((8, 8), (4, 4), (3, 5)), loc_lo=-0.2, loc_hi=1.2, Lq=20, K=2, M=2, D=4)
+    v = torch.from_numpy(t["value"]).requires_grad_(True)
+    loc = torch.from_numpy(t["loc"]).requires_grad_(True)
+    a = torch.from_numpy(t["attn"]).requires_grad_(True)
+    out = _grid_sample_forward(v, t["shapes"], t["starts"], loc, a)
+    out.backward(torch.from_numpy(t["g"]))
+    gv, gl, ga = oracle.backward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"], t["g"])
+    # grid_sample's grid lives in [-1,1]: d grid / d loc = 2 is inside autograd already
+    worst = max(_rel(gv, v.grad.numpy()), _rel(gl, loc.grad.numpy()), _rel(ga, a.grad.numpy()))
+    return worst, 1e-12
+
+
+def _near_kink(loc, shapes, margin):
+    """Mask of samples whose pixel coordinate is within `margin` of an integer."""
+    bad = np.zeros(loc.shape[:-1], dtype=bool)
+    for l, (H, W) in enumerate(shapes):
+        for c, size in ((0, W), (1, H)):
+            p = _px(loc[..., l, :, c], size)
+            bad[..., l, :] |= np.abs(p - np.round(p)) < margin
+    return bad
+
+
+def pin_backward_fd():
+    t = _tiny(seed=19, levels=((8, 8), (4, 4)), loc_lo=-0.15, loc_hi=1.15, Lq=6, K=2, M=2, D=3)
+    gv, gl, ga = oracle.backward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"], t["g"])
+
+    def J(value=None, loc=None, attn=None):
+        out = oracle.forward(t["value"] if value is None else value, t["shapes"], t["starts"],
+                             t["loc"] if loc is None else loc, t["attn"] if attn is None else attn)
+        return float((out * t["g"]).sum())
+
+    h = 1e-6
+    worst = 0.0
+    kink = _near_kink(t["loc"], t["shapes"], 1e-3)
+    for idx in np.ndindex(t["loc"].shape):
+        if kink[idx[:-1]]:
+            continue
+        p, m = t["loc"].copy(), t["loc"].copy()
+        p[idx] += h
+        m[idx] -= h
+        fd = (J(loc=p) - J(loc=m)) / (2 * h)
+        worst = max(worst, abs(fd - gl[idx]) / (1 + abs(gl[idx])))
+    for idx in list(np.ndindex(t["attn"].shape))[:24]:
+        p, m = t["attn"].copy(), t["attn"].copy()
+        p[idx] += h
+        m[idx] -= h
+        worst = max(worst, abs((J(attn=p) - J(attn=m)) / (2 * h) - ga[idx]) / (1 + abs(ga[idx])))
+    rng = np.random.Generator(np.random.PCG64(20))
+    for _ in range(40):
+        idx = tuple(int(rng.integers(0, s)) for s in t["value"].shape)
+        p, m = t["value"].copy(), t["value"].copy()
+        p[idx] += h
+        m[idx] -= h
+        worst = max(worst, abs((J(value=p) - J(value=m)) / (2 * h) - gv[idx]) / (1 + abs(gv[idx])))
+    return worst, 1e-6
+
+
+def pin_adjoint():
+    t = _tiny(seed=21, levels=((8, 8), (4, 4), (2, 3)), Lq=30, K=3, M=2, D=4)
+    gv, _, _ = oracle.backward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"], t["g"])
+    dV = np.random.Generator(np.random.PCG64(22)).standard_normal(t["value"].shape)
+    lhs = float((gv * dV).sum())
+    rhs = float((t["g"] * oracle.forward(dV, t["shapes"], t["starts"], t["loc"], t["attn"])).sum())
+    return abs(lhs - rhs) / max(1.0, abs(rhs)), 1e-12
+
+
+# --------------------------------------------------------------------------- fused
+def _fused_inputs(seed, levels=((8, 8), (4, 4), (3, 5)), N=1, Lq=8, M=2, K=2, D=3):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shapes = np.asarray(levels, dtype=np.int64)
+    starts = workloads.level_start_index(shapes)
+    S = int((shapes[:, 0] * shapes[:, 1]).sum())
+    L = len(levels)
+    ref = rng.uniform(0.1, 0.9, size=(N, Lq, L, 2))
+    scale = np.asarray([[w, h] for (h, w) in levels], dtype=np.float64)
+    off = rng.standard_normal((N, Lq, M, L, K, 2)) * 0.2 * scale[None, None, None, :, None, :]
+    logits = rng.standard_normal((N, Lq, M, L * K))
+    value = rng.standard_normal((N, S, M, D))
+    g = rng.standard_normal((N, Lq, M * D))
+    return dict(shapes=shapes, starts=starts, ref=ref, off=off, logits=logits, value=value, g=g)
+
+
+def pin_fused_composition():
+    f = _fused_inputs(23, Lq=12, M=3, K=3, D=4)
+    out = oracle.forward_fused(f["value"], f["shapes"], f["starts"], f["ref"], f["off"], f["logits"])
+    loc = oracle.locations(f["shapes"], f["ref"], f["off"])
+    attn = oracle.softmax(f["logits"]).reshape(f["off"].shape[:-1])
+    ref_out = _grid_sample_forward(torch.from_numpy(f["value"]), f["shapes"], f["starts"],
+                                   torch.from_numpy(loc), torch.from_numpy(attn)).numpy()
+    worst = _err(out, ref_out)
+    # zero logits: uniform weights 1/(L*K) (zero-initialised weight branch)
+    out0 = oracle.forward_fused(f["value"], f["shapes"], f["starts"], f["ref"], f["off"],
+                                np.zeros_like(f["logits"]))
+    uni = np.full(attn.shape, 1.0 / f["logits"].shape[-1])
+    worst = max(worst, _err(out0, oracle.forward(f["value"], f["shapes"], f["starts"], loc, uni)))
+    return worst, 1e-12
+
+
+def pin_fused_backward():
+    f = _fused_inputs(24)
+    gv, gr, go, gl = oracle.backward_fused(f["value"], f["shapes"], f["starts"], f["ref"], f["off"],
+                                           f["logits"], f["g"])
+
+    def J(ref=None, off=None, logits=None):
+        out = oracle.forward_fused(f["value"], f["shapes"], f["starts"], f["ref"] if ref is None else ref,
+                                   f["off"] if off is None else off, f["logits"] if logits is None else logits)
+        return float((out * f["g"]).sum())
+
+    h = 1e-6
+    worst = 0.0
+    loc = oracle.locations(f["shapes"], f["ref"], f["off"])
+    kink = _near_kink(loc, f["shapes"], 1e-3)
+    for idx in np.ndindex(f["off"].shape):
+        if kink[idx[:-1]]:
+            continue
+        p, m = f["off"].copy(), f["off"].copy()
+        p[idx] += h
+        m[idx] -= h
+        worst = max(worst, abs((J(off=p) - J(off=m)) / (2 * h) - go[idx]) / (1 + abs(go[idx])))
+    for idx in np.ndindex(f["ref"].shape):
+        if kink[idx[0], idx[1], :, idx[2]].any():
+            continue
+        p, m = f["ref"].copy(), f["ref"].copy()
+        p[idx] += h
+        m[idx] -= h
+        worst = max(worst, abs((J(ref=p) - J(ref=m)) / (2 * h) - gr[idx]) / (1 + abs(gr[idx])))
+    for idx in np.ndindex(f["logits"].shape):
+        p, m = f["logits"].copy(), f["logits"].copy()
+        p[idx] += h
+        m[idx] -= h
+        worst = max(worst, abs((J(logits=p) - J(logits=m)) / (2 * h) - gl[idx]) / (1 + abs(gl[idx])))
+    # softmax invariant: the logit gradients of one (query, head) sum to zero
+    worst = max(worst, float(np.abs(gl.sum(-1)).max()))
+    # grad_value does not depend on how the location was formed
+    attn = oracle.softmax(f["logits"]).reshape(f["off"].shape[:-1])
+    gv2, _, _ = oracle.backward(f["value"], f["shapes"], f["starts"], loc, attn, f["g"])
+    worst = max(worst, _err(gv, gv2))
+    return worst, 1e-6
+
+
+ALL_PINS = {
+    "worked_example": pin_worked_example,
+    "softmax_closed": pin_softmax_closed,
+    "constant_map": pin_constant_map,
+    "pixel_centres": pin_pixel_centres,
+    "linear_ramp": pin_linear_ramp,
+    "far_outside": pin_far_outside,
+    "grid_sample": pin_grid_sample,
+    "dense_tent": pin_dense_tent,
+    "backward_autograd": pin_backward_autograd,
+    "backward_fd": pin_backward_fd,
+    "adjoint": pin_adjoint,
+    "fused_composition": pin_fused_composition,
+    "fused_backward": pin_fused_backward,
+}
+
+
+def run_all():
+    """{name: (passed, error, tol)}; an exception counts as a failed pin."""
+    res = {}
+    for name, fn in ALL_PINS.items():
+        try:
+            err, tol = fn()
+            res[name] = (bool(err <= tol), err, tol)
+        except Exception as exc:  # a broken oracle may reject its own arguments
+            res[name] = (False, repr(exc), None)
+    return res
