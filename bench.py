@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Throughput of the MSDeformAttn core on B300: sampled points/s of one
+forward + backward step, achieved HBM bandwidth against the measured peak,
+the same step end to end from host memory, and the fp64 CPU oracle beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is msda_forward followed by msda_backward (atomic mode) on the
+Deformable DETR encoder workload (N=2, M=8, D=32, four levels 100x167, 50x84,
+25x42, 13x21, Len_q = Len_in = 22223, K=4, fp32), seeded synthetic inputs.
+L2 is flushed (a 256 MB write) before every step; per-step CUDA events on the
+launching stream exclude the flush.  For N > 1 (torchrun) every rank runs its
+own batch (weak scaling, no collective on the data path); the time is the
+maximum over ranks and the value counts the points of all ranks.
+
+Prints one JSON line on rank 0.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MSDeformAttn sampled-points/s fwd & fwd+bwd; achieved HBM GB/s vs B300 peak"
+UNIT = "sampled-points/s"
+WORKLOAD = "encoder_train"
+FLUSH_BYTES = 256 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic.json")
+CSRC = os.path.join(ROOT, "scale_deformable_attention_06_b300", "csrc")
+
+
+# ----------------------------------------------------------------------------- host logic
+def dist_env():
+    """(rank, local_rank, world_size) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def rank_seed(base_seed, rank):
+    """Each rank draws its own batch (weak scaling: independent problems)."""
+    return base_seed + 7919 * rank
+
+
+def max_over_ranks(x, dist=None):
+    """Maximum of a float over all ranks (the slowest rank sets the time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(points_per_rank, world, seconds_max):
+    """Whole-job throughput: points of all ranks over the slowest rank's time."""
+    return points_per_rank * world / seconds_max if seconds_max > 0 else 0.0
+
+
+def algorithmic_bytes(w):
+    """Compulsory HBM bytes of each call on workload w: every tensor the call
+    reads or writes, counted once (value re-reads and the grad_value memset
+    are not counted)."""
+    vb = 2 if w.dtype == "bf16" else 4
+    n_val = w.N * w.Len_in * w.M * w.D
+    n_out = w.N * w.Lq * w.M * w.D
+    n_smp = w.N * w.Lq * w.M * w.L * w.K
+    fwd = n_val * vb + n_smp * 2 * 4 + n_smp * 4 + n_out * vb
+    bwd = n_val * vb + n_smp * 2 * 4 + n_smp * 4 + n_out * vb + n_val * 4 + n_smp * 2 * 4 + n_smp * 4
+    fused = n_val * vb + w.N * w.Lq * w.L * 2 * 4 + n_smp * 2 * 4 + n_smp * 4 + n_out * vb
+    return {"fwd": fwd, "bwd": bwd, "fused_fwd": fused}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernels changed since it was captured."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("kernels", {}).get(kernel, {}).get("dram_bytes_per_launch")
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except (OSError, ValueError, KeyError):
+        return 6400.0, "fallback 6.4 TB/s"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons around a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, period_ms=100):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(1.0)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import scale_deformable_attention_06_b300 as msda
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    raw = workloads.draw(w, seed=rank_seed(w.seed, rank))
+
+    # input preparation (outside every timed region): the unfused inputs are
+    # the location step and the softmax of the raw draws, in float64 on the host
+    sh = torch.from_numpy(raw["spatial_shapes"])
+    wh = sh[:, [1, 0]].to(torch.float64)
+    ref = torch.from_numpy(raw["reference_points"]).double()
+    off = torch.from_numpy(raw["sampling_offsets"]).double()
+    loc_h = (ref[:, :, None, :, None, :] + off / wh[None, None, None, :, None, :]).float().contiguous()
+    attn_h = torch.softmax(torch.from_numpy(raw["attention_logits"]).double(), -1).float() \
+        .reshape(loc_h.shape[:-1]).contiguous()
+    vdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    value_h = torch.from_numpy(raw["value"]).to(vdt).contiguous()
+    gout_h = torch.from_numpy(raw["grad_output"]).to(vdt).contiguous()
+    starts = raw["level_start_index"]
+
+    value, loc, attn, gout = (t.to(dev) for t in (value_h, loc_h, attn_h, gout_h))
+    ref_d = torch.from_numpy(raw["reference_points"]).to(dev)
+    off_d = torch.from_numpy(raw["sampling_offsets"]).to(dev)
+    logit_d = torch.from_numpy(raw["attention_logits"]).to(dev)
+    out = torch.empty((w.N, w.Lq, w.M * w.D), dtype=vdt, device=dev)
+    gv = torch.empty(value.shape, dtype=torch.float32, device=dev)
+    gl = torch.empty_like(loc)
+    ga = torch.empty_like(attn)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        msda.msda_forward(value, sh, starts, loc, attn, output=out)
+
+    def bwd(flags=0):
+        msda.msda_backward(value, sh, starts, loc, attn, gout, grad_value=gv, grad_sampling_locations=gl,
+                           grad_attention_weights=ga, flags=flags)
+
+    def fused():
+        msda.msda_forward_fused(value, sh, starts, ref_d, off_d, logit_d, output=out)
+
+    def step():
+        fwd()
+        bwd()
+
+    def timed(fn, iters, pre=None):
+        """Sum of per-call device times (ms) with an L2 flush before each call."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for e0, e1 in evs:
+            flush.fill_(1.0)
+            if pre is not None:
+                pre()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+        fused()
+    torch.cuda.synchronize(dev)
+
+    # ---- the timed step: K steps between a barrier + synchronize on each side
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    step_ms = timed(step, args.steps)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    total_s = max_over_ranks(sum(step_ms) / 1e3, dist if world > 1 else None)
+
+    pts = w.samples
+    value_pts = aggregate(pts, world, total_s / args.steps)
+    ab = algorithmic_bytes(w)
+
+    # ---- per-kernel times (same protocol) for the roofline and the parts
+    reps = max(10, min(args.steps, 200))
+    fwd_ms = statistics.mean(timed(fwd, reps))
+    fused_ms = statistics.mean(timed(fused, reps))
+    bwd_ms = statistics.mean(timed(lambda: bwd(msda.MSDA_ACCUMULATE_GRAD_VALUE), reps, pre=lambda: gv.zero_()))
+    det_ms = statistics.mean(timed(lambda: bwd(msda.MSDA_DETERMINISTIC), max(5, reps // 4)))
+    peak, peak_src = measured_peak()
+    kern = {"fwd": ("msda_forward_kernel", fwd_ms), "bwd": ("msda_backward_kernel", bwd_ms)}
+    dom = max(kern, key=lambda k: kern[k][1])
+    name, ms = kern[dom]
+    achieved = ab[dom] / (ms / 1e3) / 1e9
+    traffic = profiled_traffic(name)
+
+    # ---- end to end from pinned host memory through the same calls
+    h_in = [t.pin_memory() for t in (value_h, loc_h, attn_h, gout_h)]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, gv, gl, ga)]
+
+    def e2e_step():
+        for h, d in zip(h_in, (value, loc, attn, gout)):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(h_out, (out, gv, gl, ga)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_iters = max(3, min(args.steps, 20))
+    e2e_ms = timed(e2e_step, e2e_iters)
+    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3 / e2e_iters, dist if world > 1 else None)
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, raw, loc_h.numpy(), attn_h.numpy(), value_h.float().numpy(), gout_h.float().numpy())
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": value_pts, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16-storage/f32",
+        "data": "synthetic (seeded PCG64 draws with the encoder workload's shapes and distributions)",
+        "config": {"workload": "Deformable DETR encoder fwd+bwd: N=2, M=8, D=32, L=4 levels 100x167, 50x84, "
+                               "25x42, 13x21 (Len_in=22223), Len_q=Len_in, K=4, fp32"
+                               if args.workload == WORKLOAD else args.workload,
+                   "step": "msda_forward + msda_backward (atomic grad_value)", "per_rank_batch": w.N,
+                   "sampled_points_per_step_per_rank": pts,
+                   "l2": "flushed before every step (256 MB write); per-step events exclude the flush",
+                   "parallelism": f"dp{world} (independent batches per rank)"},
+        "fwd": {"ms": fwd_ms, "points_per_s": pts / (fwd_ms / 1e3), "gbs": ab["fwd"] / (fwd_ms / 1e3) / 1e9,
+                "frac_of_peak": ab["fwd"] / (fwd_ms / 1e3) / 1e9 / peak, "algorithmic_bytes": ab["fwd"]},
+        "bwd": {"ms": bwd_ms, "points_per_s": pts / (bwd_ms / 1e3), "gbs": ab["bwd"] / (bwd_ms / 1e3) / 1e9,
+                "frac_of_peak": ab["bwd"] / (bwd_ms / 1e3) / 1e9 / peak, "algorithmic_bytes": ab["bwd"],
+                "deterministic_ms": det_ms},
+        "fused_fwd": {"ms": fused_ms, "points_per_s": pts / (fused_ms / 1e3),
+                      "gbs": ab["fused_fwd"] / (fused_ms / 1e3) / 1e9},
+        "fwd_bwd_gbs": (ab["fwd"] + ab["bwd"]) / (total_s / args.steps) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ab[dom], "launch_ms": ms},
+        "e2e": {"value": aggregate(pts, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "library": msda.LIBRARY,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- oracle timings
+def _oracle_sample(w, raw, loc, attn, value, gout, q0, q1):
+    """float64 inputs of queries [q0, q1) (all batches); the oracle's own input format."""
+    return dict(value=np.ascontiguousarray(value, dtype=np.float64), sh=raw["spatial_shapes"],
+                st=raw["level_start_index"], loc=np.ascontiguousarray(loc[:, q0:q1], dtype=np.float64),
+                attn=np.ascontiguousarray(attn[:, q0:q1], dtype=np.float64),
+                g=np.ascontiguousarray(gout[:, q0:q1], dtype=np.float64))
+
+
+def _oracle_step(s):
+    import oracle
+    oracle.forward(s["value"], s["sh"], s["st"], s["loc"], s["attn"])
+    oracle.backward(s["value"], s["sh"], s["st"], s["loc"], s["attn"], s["g"])
+
+
+def cpu_baseline(w, raw, loc, attn, value, gout, budget_s=12.0):
+    """The fp64 oracle, as it stands, single-threaded on this host: forward +
+    backward on the whole workload, repeated until about `budget_s` seconds."""
+    s = _oracle_sample(w, raw, loc, attn, value, gout, 0, w.Lq)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(s)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 10:
+            break
+    return {"value": w.samples * reps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"whole {w.name} workload (all {w.N * w.Lq} queries), forward + backward, {reps} repetitions, "
+                      f"{el:.1f} s", "host_cores_available": os.cpu_count()}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    raw = workloads.draw(w)
+    sh = raw["spatial_shapes"]
+    wh = np.asarray(sh[:, [1, 0]], dtype=np.float64)
+    loc = (raw["reference_points"].astype(np.float64)[:, :, None, :, None, :]
+           + raw["sampling_offsets"].astype(np.float64) / wh[None, None, None, :, None, :]).astype(np.float32)
+    x = raw["attention_logits"].astype(np.float64)
+    e = np.exp(x - x.max(-1, keepdims=True))
+    attn = (e / e.sum(-1, keepdims=True)).astype(np.float32).reshape(loc.shape[:-1])
+    # one step = forward + backward of a bounded query sample (all batches)
+    q_per_step = max(1, w.Lq // 16)
+    starts = [(i * q_per_step) % max(1, w.Lq - q_per_step) for i in range(args.warmup + args.steps)]
+    samples = [_oracle_sample(w, raw, loc, attn, raw["value"], raw["grad_output"], q, q + q_per_step) for q in starts]
+    for s in samples[:args.warmup]:
+        _oracle_step(s)
+    t0 = time.perf_counter()
+    for s in samples[args.warmup:]:
+        _oracle_step(s)
+    el = time.perf_counter() - t0
+    pts = w.N * q_per_step * w.M * w.L * w.K * args.steps
+    v = pts / el
+    sample = f"{q_per_step} of {w.Lq} queries (x{w.N} batches) per step, forward + backward"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "Deformable DETR encoder fwd+bwd (oracle on a query sample per step)",
+                       "step": "oracle forward + backward"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * msda.h -- C ABI of libmsda, the multi-scale deformable attention
+ * (MSDeformAttn) core for NVIDIA B300 (sm_103a).
+ *
+ * What the library computes.  For every batch element n, query q and head m,
+ * the core samples a head_dim-channel vector from each of n_levels flattened
+ * feature levels at n_points locations each, bilinearly, weights every sample
+ * by its attention weight and sums them:
+ *
+ *   out[n][q][m*D + d] = sum_{l,k} A[n,q,m,l,k] * bilinear_l(value[n,:,m,d], loc[n,q,m,l,k])
+ *
+ * This is the inner sum of the MSDeformAttn formula, "可变形注意力：多尺度稀疏
+ * 采样与视觉检测实战解析" §2.2 (and "可变形 DETR：加速收敛的稀疏注意力检测器"
+ * §3.3); the value, offset, weight and output projections around it are not
+ * part of this library.  Bilinear sampling follows that tutorial's §2.3 and the
+ * grid_sample module of its §3.2: the pixel coordinate of a normalised
+ * location is px = loc_x * W_l - 0.5, py = loc_y * H_l - 0.5 (align_corners
+ * = False), the four integer neighbours are weighted (1-|dx|)(1-|dy|), and a
+ * neighbour outside [0,W_l) x [0,H_l) contributes zero while the others keep
+ * their weights (padding_mode = 'zeros').
+ *
+ * Conventions shared by every call:
+ *   - All tensors are dense, row-major, and live in device memory owned by
+ *     the caller, except spatial_shapes and level_start_index, which are
+ *     HOST arrays (read during the call, not retained).  The library never
+ *     allocates memory; temporary memory comes from the caller (workspace).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and enqueues work on the current CUDA device.
+ *     A call returns after launching, not after the kernels finish.
+ *   - Arguments are checked on the host before any launch.  A failed check
+ *     returns MSDA_ERR_INVALID_ARG or MSDA_ERR_UNSUPPORTED and launches
+ *     nothing; msda_last_error() then describes the failure (thread-local).
+ *   - A launch failure returns MSDA_ERR_CUDA (cudaGetLastError after launch).
+ *   - Calls with N == 0 or Len_q == 0 launch no sampling work; they still
+ *     zero grad_value where the call says it does.
+ *   - Inputs are assumed finite.  A non-finite value may reach samples whose
+ *     corners fall outside the map (their loads are kept, with weight 0).
+ *
+ * Layouts (D = head_dim, M = n_heads, L = n_levels, K = n_points):
+ *   value               [N][Len_in][M][D]            dtype (f32 or bf16)
+ *   spatial_shapes      [L][2] = (H_l, W_l)           int64, host
+ *   level_start_index   [L]                           int64, host;
+ *                       level_start_index[0] = 0, [l+1] = [l] + H_l*W_l,
+ *                       Len_in = sum_l H_l*W_l
+ *   sampling_locations  [N][Len_q][M][L][K][2]        f32, (x, y), normalised
+ *   attention_weights   [N][Len_q][M][L][K]           f32
+ *   output              [N][Len_q][M*D]               dtype
+ *   reference_points    [N][Len_q][L][2]              f32, (x, y), normalised
+ *   sampling_offsets    [N][Len_q][M][L][K][2]        f32, in pixels of level l
+ *   attention_logits    [N][Len_q][M][L*K]            f32
+ *   grad_output         [N][Len_q][M*D]               dtype
+ *   grad_value          [N][Len_in][M][D]             f32 (for both dtypes)
+ *   grad_sampling_locations [N][Len_q][M][L][K][2]    f32
+ *   grad_attention_weights  [N][Len_q][M][L][K]       f32
+ *
+ * Supported: head_dim in {8, 16, 32, 64}; 1 <= n_levels <= 16;
+ * 1 <= n_levels * n_points <= 256; N*Len_q*M < 2^31; (Len_in + 2*max W_l + 4)
+ * * M * D < 2^31.  value/output/grad_output/grad_value must be 16-byte
+ * aligned, sampling_locations/reference_points/sampling_offsets 8-byte
+ * aligned, the other f32 tensors 4-byte aligned.
+ */
+#ifndef MSDA_H_
+#define MSDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MSDA_API __attribute__((visibility("default")))
+#else
+#define MSDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum msda_status {
+    MSDA_OK = 0,
+    MSDA_ERR_INVALID_ARG = 1,   /* a null pointer, a bad size, inconsistent levels */
+    MSDA_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle */
+    MSDA_ERR_CUDA = 3,          /* the CUDA runtime reported an error */
+    MSDA_ERR_WORKSPACE = 4      /* workspace missing, too small or misaligned */
+} msda_status;
+
+/* Storage type of value, output and grad_output.  Arithmetic is fp32. */
+typedef enum msda_dtype {
+    MSDA_F32 = 0,
+    MSDA_BF16 = 1               /* bf16 storage, fp32 accumulation, RNE rounding of output */
+} msda_dtype;
+
+/* Sizes of one call (names follow the tutorial module's interface, §3.1). */
+typedef struct msda_problem {
+    int32_t N;          /* batch size */
+    int32_t Len_in;     /* flattened value length, sum of H_l*W_l */
+    int32_t n_heads;    /* M */
+    int32_t head_dim;   /* D, channels per head */
+    int32_t Len_q;      /* number of queries */
+    int32_t n_levels;   /* L */
+    int32_t n_points;   /* K, samples per level per head */
+    int32_t dtype;      /* msda_dtype */
+} msda_problem;
+
+/* msda_backward flags */
+#define MSDA_DETERMINISTIC          1u  /* bitwise reproducible grad_value (fixed-point sums) */
+#define MSDA_ACCUMULATE_GRAD_VALUE  2u  /* add into grad_value instead of overwriting it */
+
+/*
+ * msda_forward -- steps a3-a5: bilinear multi-level sampling, weighted sum.
+ * "可变形注意力：多尺度稀疏采样与视觉检测实战解析" §2.2 (formula), §2.3
+ * (bilinear, zero padding), §3.2 steps 4-5 (per-level sampling, weighted sum).
+ *
+ *   value               in   [N][Len_in][M][D], dtype
+ *   spatial_shapes      in   host [L][2] (H, W)
+ *   level_start_index   in   host [L]
+ *   sampling_locations  in   [N][Len_q][M][L][K][2] f32
+ *   attention_weights   in   [N][Len_q][M][L][K] f32 (used as given; no softmax)
+ *   output              out  [N][Len_q][M*D], dtype; fully overwritten
+ */
+MSDA_API msda_status msda_forward(const msda_problem *problem, const void *value,
+                         const int64_t *spatial_shapes, const int64_t *level_start_index,
+                         const float *sampling_locations, const float *attention_weights,
+                         void *output, void *stream);
+
+/*
+ * msda_forward_fused -- steps a1-a5 in one launch: the sampling location
+ * loc = ref + off / (W_l, H_l) ("可变形 DETR：加速收敛的稀疏注意力检测器" §6,
+ * reference_points + sampling_offsets / scale_factors), the softmax of the
+ * raw logits over all L*K samples of one (query, head) (the tutorial module
+ * of "可变形注意力…" §3.2: softmax over n_levels*n_points), then the sampling
+ * of msda_forward.  Locations and weights stay in registers.
+ *
+ *   reference_points    in   [N][Len_q][L][2] f32, normalised (x, y)
+ *   sampling_offsets    in   [N][Len_q][M][L][K][2] f32, pixels of level l
+ *   attention_logits    in   [N][Len_q][M][L*K] f32
+ *   output              out  [N][Len_q][M*D], dtype; fully overwritten
+ */
+MSDA_API msda_status msda_forward_fused(const msda_problem *problem, const void *value,
+                               const int64_t *spatial_shapes, const int64_t *level_start_index,
+                               const float *reference_points, const float *sampling_offsets,
+                               const float *attention_logits, void *output, void *stream);
+
+/*
+ * Bytes of device workspace msda_backward needs for `flags` (0 unless
+ * MSDA_DETERMINISTIC is set).  Host-only, launches nothing.
+ */
+MSDA_API size_t msda_backward_workspace_size(const msda_problem *problem, unsigned flags);
+
+/*
+ * msda_backward -- steps a6-a8, the gradient of msda_forward, derived from
+ * the bilinear form of "可变形注意力…" §2.3 (continuous, so the gradient
+ * reaches the offset branch).  With g = grad_output[n][q][m*D..]:
+ *   grad_attention_weights[s]  = <g, sample_s>
+ *   grad_sampling_locations[s] = A_s * <g, d sample_s / d(px, py)> * (W_l, H_l)
+ *   grad_value[n][corner][m]  += A_s * w_corner * g      (corners inside the map)
+ * At an integer pixel coordinate the location gradient is the one-sided
+ * derivative of the cell that floor() selects.
+ *
+ *   grad_output            in   [N][Len_q][M*D], dtype
+ *   grad_value             out  [N][Len_in][M][D] f32; zeroed first unless
+ *                               MSDA_ACCUMULATE_GRAD_VALUE
+ *   grad_sampling_locations out [N][Len_q][M][L][K][2] f32, overwritten
+ *   grad_attention_weights out  [N][Len_q][M][L][K] f32, overwritten
+ *   flags                  in   MSDA_DETERMINISTIC | MSDA_ACCUMULATE_GRAD_VALUE
+ *   workspace              in   device memory of at least
+ *                               msda_backward_workspace_size() bytes, 256-byte
+ *                               aligned (may be NULL when that size is 0);
+ *                               its contents on entry do not matter.
+ * Default mode sums grad_value with fp32 atomics, so its low bits vary from
+ * run to run.  MSDA_DETERMINISTIC sums in 64-bit fixed point, scaled from a
+ * bound on the total so that no sum can overflow, then converts to fp32: the
+ * result is bitwise identical from run to run.  grad_sampling_locations and
+ * grad_attention_weights are bitwise reproducible in both modes.
+ */
+MSDA_API msda_status msda_backward(const msda_problem *problem, const void *value,
+                          const int64_t *spatial_shapes, const int64_t *level_start_index,
+                          const float *sampling_locations, const float *attention_weights,
+                          const void *grad_output, float *grad_value,
+                          float *grad_sampling_locations, float *grad_attention_weights,
+                          unsigned flags, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Name of a status code (static string). */
+MSDA_API const char *msda_status_string(msda_status status);
+
+/* Description of the last failure on the calling thread ("" if none). */
+MSDA_API const char *msda_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+MSDA_API int msda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSDA_H_ */

@@ -1,0 +1,206 @@
+"""ctypes binding of libmsda (include/msda.h): argument marshalling only.
+
+Every function here checks shapes and dtypes of torch tensors, passes their
+device pointers and the current CUDA stream to the C ABI, and raises
+MSDAError when the library returns a non-OK status.  No step of the method
+runs in Python; there is no CPU fallback.  If libmsda.so has not been built,
+importing the package raises ImportError.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libmsda.so")
+
+MSDA_OK = 0
+MSDA_F32 = 0
+MSDA_BF16 = 1
+MSDA_DETERMINISTIC = 1
+MSDA_ACCUMULATE_GRAD_VALUE = 2
+
+EXPORTED = ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_workspace_size",
+            "msda_status_string", "msda_last_error", "msda_version")
+
+
+class MSDAError(RuntimeError):
+    def __init__(self, status, name, detail):
+        super().__init__(f"{name}: {detail}")
+        self.status = status
+        self.name = name
+
+
+class msda_problem(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int32), ("Len_in", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("Len_q", ctypes.c_int32), ("n_levels", ctypes.c_int32),
+                ("n_points", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIBRARY):
+        raise ImportError(f"{LIBRARY} is missing: build it with `python -m scale_deformable_attention_06_b300.build`")
+    lib = ctypes.CDLL(LIBRARY)
+    vp, i64p, fp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p
+    pp = ctypes.POINTER(msda_problem)
+    lib.msda_forward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, vp]
+    lib.msda_forward_fused.argtypes = [pp, vp, i64p, i64p, fp, fp, fp, vp, vp]
+    lib.msda_backward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, fp, fp, fp, ctypes.c_uint, vp, ctypes.c_size_t, vp]
+    lib.msda_backward_workspace_size.argtypes = [pp, ctypes.c_uint]
+    lib.msda_backward_workspace_size.restype = ctypes.c_size_t
+    for f in ("msda_forward", "msda_forward_fused", "msda_backward"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.msda_status_string.argtypes = [ctypes.c_int]
+    lib.msda_status_string.restype = ctypes.c_char_p
+    lib.msda_last_error.argtypes = []
+    lib.msda_last_error.restype = ctypes.c_char_p
+    lib.msda_version.restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    """The loaded ctypes library (for tests that call the C ABI directly)."""
+    return _lib
+
+
+def _check(status):
+    if status != MSDA_OK:
+        raise MSDAError(status, _lib.msda_status_string(status).decode(), _lib.msda_last_error().decode())
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return MSDA_F32
+    if t.dtype == torch.bfloat16:
+        return MSDA_BF16
+    raise TypeError(f"value dtype {t.dtype} is not float32 or bfloat16")
+
+
+def _dev(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class _HostLevels:
+    """spatial_shapes [L,2] and level_start_index [L] as host int64 arrays."""
+
+    def __init__(self, spatial_shapes, level_start_index):
+        sh = torch.as_tensor(spatial_shapes).detach().to("cpu", torch.int64).contiguous().reshape(-1, 2)
+        st = torch.as_tensor(level_start_index).detach().to("cpu", torch.int64).contiguous().reshape(-1)
+        self.sh, self.st = sh, st          # keep alive for the call
+        self.L = sh.shape[0]
+        self.shp = ctypes.cast(sh.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+        self.stp = ctypes.cast(st.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+
+
+def _stream(stream, device):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def problem(value, Len_q, n_levels, n_points):
+    N, S, M, D = value.shape
+    return msda_problem(N, S, M, D, Len_q, n_levels, n_points, _dtype_code(value))
+
+
+def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
+                 output=None, stream=None):
+    """out[N, Len_q, M*D] from value [N,Len_in,M,D] (f32|bf16), sampling_locations
+    [N,Len_q,M,L,K,2] f32 and attention_weights [N,Len_q,M,L,K] f32."""
+    lv = _HostLevels(spatial_shapes, level_start_index)
+    N, S, M, D = value.shape
+    if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != 2:
+        raise ValueError("sampling_locations must be [N, Len_q, M, L, K, 2]")
+    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
+    if tuple(sampling_locations.shape[:5]) != (N, Lq, M, L, K) or tuple(attention_weights.shape) != (N, Lq, M, L, K):
+        raise ValueError("sampling_locations / attention_weights shapes disagree with value")
+    if L != lv.L:
+        raise ValueError("n_levels of sampling_locations and spatial_shapes disagree")
+    if output is None:
+        output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
+    elif tuple(output.shape) != (N, Lq, M * D) or output.dtype != value.dtype:
+        raise ValueError("output must be [N, Len_q, M*D] with the dtype of value")
+    prob = problem(value, Lq, L, K)
+    _check(_lib.msda_forward(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
+                             _dev(sampling_locations, "sampling_locations", torch.float32),
+                             _dev(attention_weights, "attention_weights", torch.float32),
+                             _dev(output, "output"), _stream(stream, value.device)))
+    return output
+
+
+def msda_forward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
+                       attention_logits, output=None, stream=None):
+    """out[N, Len_q, M*D] from reference_points [N,Len_q,L,2], sampling_offsets
+    [N,Len_q,M,L,K,2] (pixels of each level) and attention_logits [N,Len_q,M,L*K]."""
+    lv = _HostLevels(spatial_shapes, level_start_index)
+    N, S, M, D = value.shape
+    if sampling_offsets.dim() != 6 or sampling_offsets.shape[-1] != 2:
+        raise ValueError("sampling_offsets must be [N, Len_q, M, L, K, 2]")
+    Lq, L, K = sampling_offsets.shape[1], sampling_offsets.shape[3], sampling_offsets.shape[4]
+    if tuple(reference_points.shape) != (N, Lq, L, 2):
+        raise ValueError("reference_points must be [N, Len_q, L, 2]")
+    if attention_logits.numel() != N * Lq * M * L * K:
+        raise ValueError("attention_logits must hold N*Len_q*M*L*K values")
+    if L != lv.L:
+        raise ValueError("n_levels of sampling_offsets and spatial_shapes disagree")
+    if output is None:
+        output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
+    prob = problem(value, Lq, L, K)
+    _check(_lib.msda_forward_fused(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
+                                   _dev(reference_points, "reference_points", torch.float32),
+                                   _dev(sampling_offsets, "sampling_offsets", torch.float32),
+                                   _dev(attention_logits, "attention_logits", torch.float32),
+                                   _dev(output, "output"), _stream(stream, value.device)))
+    return output
+
+
+def msda_backward_workspace_size(value, Len_q, n_levels, n_points, flags=0):
+    prob = problem(value, Len_q, n_levels, n_points)
+    return int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
+
+
+def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, grad_output,
+                  grad_value=None, grad_sampling_locations=None, grad_attention_weights=None, flags=0,
+                  workspace=None, stream=None):
+    """Returns (grad_value f32 [N,Len_in,M,D], grad_sampling_locations, grad_attention_weights)."""
+    lv = _HostLevels(spatial_shapes, level_start_index)
+    N, S, M, D = value.shape
+    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
+    if tuple(attention_weights.shape) != (N, Lq, M, L, K) or tuple(grad_output.shape) != (N, Lq, M * D):
+        raise ValueError("attention_weights / grad_output shapes disagree with value")
+    if grad_output.dtype != value.dtype:
+        raise TypeError("grad_output must have the dtype of value")
+    dev = value.device
+    if grad_value is None:
+        grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)
+    if grad_sampling_locations is None:
+        grad_sampling_locations = torch.empty_like(sampling_locations)
+    if grad_attention_weights is None:
+        grad_attention_weights = torch.empty_like(attention_weights)
+    prob = problem(value, Lq, L, K)
+    need = int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.msda_backward(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
+                              _dev(sampling_locations, "sampling_locations", torch.float32),
+                              _dev(attention_weights, "attention_weights", torch.float32),
+                              _dev(grad_output, "grad_output"), _dev(grad_value, "grad_value", torch.float32),
+                              _dev(grad_sampling_locations, "grad_sampling_locations", torch.float32),
+                              _dev(grad_attention_weights, "grad_attention_weights", torch.float32),
+                              flags, ws_ptr, ws_bytes, _stream(stream, dev)))
+    return grad_value, grad_sampling_locations, grad_attention_weights

@@ -1,0 +1,195 @@
+// msda_api.cu -- the C ABI of libmsda (declared in include/msda.h): host-side
+// argument checks, the per-level table, and dispatch to the kernel launchers.
+// Nothing here allocates device memory.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/msda.h"
+#include "msda_launch.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+msda_status fail(msda_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks the sizes and the levels and fills the launch geometry.
+msda_status make_geometry(const msda_problem *p, const int64_t *shapes, const int64_t *starts,
+                          msda::LaunchGeometry &g) {
+    if (!p) return fail(MSDA_ERR_INVALID_ARG, "problem is NULL");
+    if (p->N < 0 || p->Len_q < 0 || p->Len_in < 0)
+        return fail(MSDA_ERR_INVALID_ARG, "negative size (N=%d Len_q=%d Len_in=%d)", p->N, p->Len_q, p->Len_in);
+    if (p->n_heads < 1 || p->n_points < 1 || p->n_levels < 1)
+        return fail(MSDA_ERR_INVALID_ARG, "n_heads, n_levels and n_points must be >= 1");
+    if (p->dtype != MSDA_F32 && p->dtype != MSDA_BF16)
+        return fail(MSDA_ERR_UNSUPPORTED, "dtype %d is not MSDA_F32 or MSDA_BF16", p->dtype);
+    if (p->head_dim != 8 && p->head_dim != 16 && p->head_dim != 32 && p->head_dim != 64)
+        return fail(MSDA_ERR_UNSUPPORTED, "head_dim %d not in {8, 16, 32, 64}", p->head_dim);
+    if (p->n_levels > msda::kMaxLevels)
+        return fail(MSDA_ERR_UNSUPPORTED, "n_levels %d above %d", p->n_levels, msda::kMaxLevels);
+    if ((int64_t)p->n_levels * p->n_points > msda::kMaxSamples)
+        return fail(MSDA_ERR_UNSUPPORTED, "n_levels * n_points = %lld above %d",
+                    (long long)p->n_levels * p->n_points, msda::kMaxSamples);
+    if (!shapes || !starts) return fail(MSDA_ERR_INVALID_ARG, "spatial_shapes / level_start_index is NULL");
+    int64_t expect = 0, maxW = 0;
+    for (int l = 0; l < p->n_levels; ++l) {
+        const int64_t H = shapes[2 * l], W = shapes[2 * l + 1];
+        if (H < 1 || W < 1) return fail(MSDA_ERR_INVALID_ARG, "level %d has shape (%lld, %lld)", l, (long long)H, (long long)W);
+        if (H > (1 << 24) || W > (1 << 24))
+            return fail(MSDA_ERR_UNSUPPORTED, "level %d side above 2^24 (float pixel coordinates)", l);
+        if (starts[l] != expect)
+            return fail(MSDA_ERR_INVALID_ARG, "level_start_index[%d] = %lld, expected %lld", l, (long long)starts[l],
+                        (long long)expect);
+        expect += H * W;
+        if (W > maxW) maxW = W;
+    }
+    if (expect != p->Len_in)
+        return fail(MSDA_ERR_INVALID_ARG, "sum of H*W over levels is %lld but Len_in is %d", (long long)expect, p->Len_in);
+    const int64_t pix = (int64_t)p->n_heads * p->head_dim;
+    if ((p->Len_in + 2 * maxW + 4) * pix >= (int64_t(1) << 31))
+        return fail(MSDA_ERR_UNSUPPORTED, "(Len_in + 2 W + 4) * n_heads * head_dim exceeds 2^31");
+    const int64_t rows = (int64_t)p->N * p->Len_q * p->n_heads;
+    if (rows >= (int64_t(1) << 31)) return fail(MSDA_ERR_UNSUPPORTED, "N * Len_q * n_heads exceeds 2^31");
+
+    std::memset(&g, 0, sizeof(g));
+    g.d.N = p->N;
+    g.d.Len_in = p->Len_in;
+    g.d.M = p->n_heads;
+    g.d.Len_q = p->Len_q;
+    g.d.L = p->n_levels;
+    g.d.K = p->n_points;
+    g.d.P = p->n_levels * p->n_points;
+    g.d.rows = (int)rows;
+    g.d.qm = p->Len_q * p->n_heads;
+    g.d.pix = (int)pix;
+    for (int l = 0; l < p->n_levels; ++l) {
+        g.lv.H[l] = (int)shapes[2 * l];
+        g.lv.W[l] = (int)shapes[2 * l + 1];
+        g.lv.start[l] = (int)starts[l];
+        g.lv.Hf[l] = (float)shapes[2 * l];
+        g.lv.Wf[l] = (float)shapes[2 * l + 1];
+    }
+    for (int s = 0; s < g.d.P; ++s) g.level_of[s] = (unsigned char)(s / p->n_points);
+    return MSDA_OK;
+}
+
+msda_status cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return MSDA_OK;
+    return fail(MSDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+msda_status msda_forward(const msda_problem *problem, const void *value, const int64_t *spatial_shapes,
+                         const int64_t *level_start_index, const float *sampling_locations,
+                         const float *attention_weights, void *output, void *stream) {
+    g_last_error[0] = 0;
+    msda::LaunchGeometry g;
+    msda_status st = make_geometry(problem, spatial_shapes, level_start_index, g);
+    if (st != MSDA_OK) return st;
+    if (g.d.rows == 0) return MSDA_OK;
+    if (!value || !sampling_locations || !attention_weights || !output)
+        return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!aligned(value, 16) || !aligned(output, 16) || !aligned(sampling_locations, 8) || !aligned(attention_weights, 4))
+        return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor (value/output 16 B, locations 8 B, weights 4 B)");
+    return cuda_status(msda::launch_forward(g, problem->dtype, problem->head_dim, value, sampling_locations,
+                                            attention_weights, output, static_cast<cudaStream_t>(stream)),
+                       "msda_forward launch");
+}
+
+msda_status msda_forward_fused(const msda_problem *problem, const void *value, const int64_t *spatial_shapes,
+                               const int64_t *level_start_index, const float *reference_points,
+                               const float *sampling_offsets, const float *attention_logits, void *output,
+                               void *stream) {
+    g_last_error[0] = 0;
+    msda::LaunchGeometry g;
+    msda_status st = make_geometry(problem, spatial_shapes, level_start_index, g);
+    if (st != MSDA_OK) return st;
+    if (g.d.rows == 0) return MSDA_OK;
+    if (!value || !reference_points || !sampling_offsets || !attention_logits || !output)
+        return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!aligned(value, 16) || !aligned(output, 16) || !aligned(reference_points, 8) || !aligned(sampling_offsets, 8) ||
+        !aligned(attention_logits, 4))
+        return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor (value/output 16 B, points/offsets 8 B, logits 4 B)");
+    return cuda_status(msda::launch_forward_fused(g, problem->dtype, problem->head_dim, value, reference_points,
+                                                  sampling_offsets, attention_logits, output,
+                                                  static_cast<cudaStream_t>(stream)),
+                       "msda_forward_fused launch");
+}
+
+size_t msda_backward_workspace_size(const msda_problem *problem, unsigned flags) {
+    if (!problem || problem->N < 0 || problem->Len_in < 0 || problem->n_heads < 1 || problem->head_dim < 1) return 0;
+    msda::LaunchGeometry g;
+    std::memset(&g, 0, sizeof(g));
+    g.d.N = problem->N;
+    g.d.Len_in = problem->Len_in;
+    g.d.M = problem->n_heads;
+    return msda::backward_workspace_bytes(g, problem->head_dim, (flags & MSDA_DETERMINISTIC) != 0);
+}
+
+msda_status msda_backward(const msda_problem *problem, const void *value, const int64_t *spatial_shapes,
+                          const int64_t *level_start_index, const float *sampling_locations,
+                          const float *attention_weights, const void *grad_output, float *grad_value,
+                          float *grad_sampling_locations, float *grad_attention_weights, unsigned flags,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    g_last_error[0] = 0;
+    msda::LaunchGeometry g;
+    msda_status st = make_geometry(problem, spatial_shapes, level_start_index, g);
+    if (st != MSDA_OK) return st;
+    if (flags & ~(MSDA_DETERMINISTIC | MSDA_ACCUMULATE_GRAD_VALUE))
+        return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const bool det = (flags & MSDA_DETERMINISTIC) != 0, acc = (flags & MSDA_ACCUMULATE_GRAD_VALUE) != 0;
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * problem->head_dim;
+    if (nval > 0 && !grad_value) return fail(MSDA_ERR_INVALID_ARG, "grad_value is NULL");
+    if (grad_value && !aligned(grad_value, 16)) return fail(MSDA_ERR_INVALID_ARG, "grad_value not 16-byte aligned");
+    if (g.d.rows > 0) {
+        if (!value || !sampling_locations || !attention_weights || !grad_output || !grad_sampling_locations ||
+            !grad_attention_weights)
+            return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+        if (!aligned(value, 16) || !aligned(grad_output, 16) || !aligned(sampling_locations, 8) ||
+            !aligned(grad_sampling_locations, 8) || !aligned(attention_weights, 4) || !aligned(grad_attention_weights, 4))
+            return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor");
+    }
+    const size_t need = msda::backward_workspace_bytes(g, problem->head_dim, det);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need)
+            return fail(MSDA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
+        if (!aligned(workspace, 256)) return fail(MSDA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    }
+    if (nval == 0 && g.d.rows == 0) return MSDA_OK;
+    if (g.d.rows == 0 && acc) return MSDA_OK;
+    return cuda_status(msda::launch_backward(g, problem->dtype, problem->head_dim, value, sampling_locations,
+                                             attention_weights, grad_output, grad_value, grad_sampling_locations,
+                                             grad_attention_weights, det, acc, workspace,
+                                             static_cast<cudaStream_t>(stream)),
+                       "msda_backward launch");
+}
+
+const char *msda_status_string(msda_status s) {
+    switch (s) {
+        case MSDA_OK: return "MSDA_OK";
+        case MSDA_ERR_INVALID_ARG: return "MSDA_ERR_INVALID_ARG";
+        case MSDA_ERR_UNSUPPORTED: return "MSDA_ERR_UNSUPPORTED";
+        case MSDA_ERR_CUDA: return "MSDA_ERR_CUDA";
+        case MSDA_ERR_WORKSPACE: return "MSDA_ERR_WORKSPACE";
+    }
+    return "MSDA_ERR_UNKNOWN";
+}
+
+const char *msda_last_error(void) { return g_last_error; }
+
+int msda_version(void) { return 100; }
+
+}  // extern "C"

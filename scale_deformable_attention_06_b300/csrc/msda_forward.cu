@@ -1,0 +1,199 @@
+// msda_forward.cu -- forward kernels of the MSDeformAttn core.
+//
+//   out[n][q][m*D+d] = sum_{l,k} A[n,q,m,l,k] * bilinear_l(value[n,:,m,d], loc[n,q,m,l,k])
+//
+// ("可变形注意力：多尺度稀疏采样与视觉检测实战解析" §2.2 formula, §2.3 bilinear
+// sampling, §3.2 steps 4-5; "可变形 DETR：加速收敛的稀疏注意力检测器" §3.3.)
+// The fused variant also forms loc = ref + off / (W_l, H_l) ("可变形 DETR…" §6)
+// and A = softmax over the L*K logits of the row (the tutorial module, §3.2).
+//
+// Work decomposition.  A "row" is one (n, q, m).  A warp owns HW = 32 / R
+// consecutive rows, R lanes per row, each lane holding 16 bytes of the row's
+// D channels (4 fp32 or 8 bf16).  Per chunk of samples:
+//   phase 1: each lane computes the corner records (four element offsets and
+//            four weights, attention weight folded in) of one or two samples,
+//            coalesced over the warp's rows, into warp-private shared memory;
+//   phase 2: each lane walks the chunk's samples of its own row and issues four
+//            independent 16-byte gathers per sample, accumulating in fp32.
+// Every corner fetch is a full 16-byte vector per lane and R lanes cover one
+// contiguous D-channel row segment, so a warp-wide gather touches HW value
+// rows, each fully used.
+#include "msda_device.cuh"
+#include "msda_launch.h"
+
+namespace msda {
+
+struct FwdArgs {
+    const void *value;
+    const float *loc;      // unfused
+    const float *attn;     // unfused
+    const float *ref;      // fused
+    const float *off;      // fused
+    const float *logits;   // fused
+    void *out;
+    Dims d;
+    LevelTable lv;
+    unsigned char level_of[kMaxSamples];   // level of sample s = l*K + k
+};
+
+template <typename T, int D, bool FUSED>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+msda_forward_kernel(const __grid_constant__ FwdArgs a) {
+    using Lay = Layout<T, D>;
+    constexpr int V = Lay::V, R = Lay::R, HW = Lay::HW;
+    constexpr int JC = kRecordsPerWarp / HW;     // samples of each row per chunk
+
+    __shared__ int4 s_off[kWarpsPerBlock][kRecordsPerWarp];
+    __shared__ float4 s_w[kWarpsPerBlock][kRecordsPerWarp];
+    __shared__ float2 s_stat[kWarpsPerBlock][HW];   // fused: (row max, 1 / row sum)
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * kWarpsPerBlock + warp) * HW;
+    const Dims &dm = a.d;
+    if (row0 >= dm.rows) return;
+    const int P = dm.P;
+
+    if constexpr (FUSED) {
+        // softmax statistics of each row: max and 1/sum of exp(logit - max)
+        for (int h = 0; h < HW; ++h) {
+            const int row = row0 + h;
+            if (row >= dm.rows) break;                  // warp-uniform
+            const float *lg = a.logits + (size_t)row * P;
+            float mx = -INFINITY;
+            for (int s = lane; s < P; s += 32) mx = fmaxf(mx, __ldg(lg + s));
+            mx = warp_max(mx);
+            float sum = 0.f;
+            for (int s = lane; s < P; s += 32) sum += expf(__ldg(lg + s) - mx);
+            sum = warp_sum(sum);
+            if (lane == 0) s_stat[warp][h] = make_float2(mx, 1.f / sum);
+        }
+        __syncwarp();
+    }
+
+    // phase-2 lane role
+    const int h = lane / R, ch = lane % R;
+    const int row = row0 + h;
+    const bool row_ok = row < dm.rows;
+    const int rowc = row_ok ? row : dm.rows - 1;
+    const int n = rowc / dm.qm;
+    const int m = rowc % dm.M;
+    const T *vbase = static_cast<const T *>(a.value) + ((size_t)n * dm.Len_in * dm.M + m) * D + ch * V;
+    const uint64_t pol = l2_keep_policy();
+
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+
+    for (int s0 = 0; s0 < P; s0 += JC) {
+        const int J = min(JC, P - s0);
+        // ---- phase 1: corner records, record i = j * HW + hh
+        for (int i = lane; i < HW * J; i += 32) {
+            const int hh = i % HW, j = i / HW;
+            const int r = row0 + hh, s = s0 + j;
+            int4 off = make_int4(0, 0, 0, 0);
+            float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < dm.rows) {
+                const int l = a.level_of[s];
+                const float Wf = a.lv.Wf[l], Hf = a.lv.Hf[l];
+                float x0, fx, y0, fy, A;
+                const size_t si = (size_t)r * P + s;
+                if constexpr (FUSED) {
+                    const int nq = r / dm.M;            // (n, q) of this row
+                    const float2 rf = __ldg(reinterpret_cast<const float2 *>(a.ref) + (size_t)nq * dm.L + l);
+                    const float2 of = load_stream2(a.off + 2 * si);
+                    pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
+                    pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
+                    const float2 st = s_stat[warp][hh];
+                    A = expf(load_stream1(a.logits + si) - st.x) * st.y;
+                } else {
+                    const float2 lc = load_stream2(a.loc + 2 * si);
+                    pixel_coord(lc.x, Wf, x0, fx);
+                    pixel_coord(lc.y, Hf, y0, fy);
+                    A = load_stream1(a.attn + si);
+                }
+                Corners c = make_corners(x0, fx, y0, fy, a.lv.W[l], a.lv.H[l], Wf, Hf, a.lv.start[l], dm.pix);
+                off = c.off;
+                w = make_float4(c.w.x * A, c.w.y * A, c.w.z * A, c.w.w * A);
+            }
+            s_off[warp][i] = off;
+            s_w[warp][i] = w;
+        }
+        __syncwarp();
+        // ---- phase 2: gathers of this lane's row
+#pragma unroll 2
+        for (int j = 0; j < J; ++j) {
+            const int4 o = s_off[warp][j * HW + h];
+            const float4 w = s_w[warp][j * HW + h];
+            const Vec<T> v0 = load_value(vbase + o.x, pol);
+            const Vec<T> v1 = load_value(vbase + o.y, pol);
+            const Vec<T> v2 = load_value(vbase + o.z, pol);
+            const Vec<T> v3 = load_value(vbase + o.w, pol);
+            fma_row<T, V>(acc, w.x, v0);
+            fma_row<T, V>(acc, w.y, v1);
+            fma_row<T, V>(acc, w.z, v2);
+            fma_row<T, V>(acc, w.w, v3);
+        }
+        __syncwarp();
+    }
+    if (row_ok) store_row<T, V>(static_cast<T *>(a.out) + (size_t)row * D + ch * V, acc);
+}
+
+template <typename T, int D, bool FUSED>
+static cudaError_t launch_fwd(const FwdArgs &args, cudaStream_t stream) {
+    constexpr int HW = Layout<T, D>::HW;
+    const long long warps = ((long long)args.d.rows + HW - 1) / HW;
+    const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    msda_forward_kernel<T, D, FUSED><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    return cudaGetLastError();
+}
+
+template <bool FUSED>
+static cudaError_t dispatch_fwd(const FwdArgs &args, int dtype, int D, cudaStream_t stream) {
+    if (dtype == 0) {
+        switch (D) {
+            case 8: return launch_fwd<float, 8, FUSED>(args, stream);
+            case 16: return launch_fwd<float, 16, FUSED>(args, stream);
+            case 32: return launch_fwd<float, 32, FUSED>(args, stream);
+            case 64: return launch_fwd<float, 64, FUSED>(args, stream);
+        }
+    } else {
+        switch (D) {
+            case 8: return launch_fwd<__nv_bfloat16, 8, FUSED>(args, stream);
+            case 16: return launch_fwd<__nv_bfloat16, 16, FUSED>(args, stream);
+            case 32: return launch_fwd<__nv_bfloat16, 32, FUSED>(args, stream);
+            case 64: return launch_fwd<__nv_bfloat16, 64, FUSED>(args, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+static void fill_common(FwdArgs &fa, const LaunchGeometry &g) {
+    fa.d = g.d;
+    fa.lv = g.lv;
+    for (int s = 0; s < kMaxSamples; ++s) fa.level_of[s] = g.level_of[s];
+}
+
+cudaError_t launch_forward(const LaunchGeometry &g, int dtype, int D, const void *value, const float *loc,
+                           const float *attn, void *out, cudaStream_t stream) {
+    FwdArgs fa{};
+    fill_common(fa, g);
+    fa.value = value;
+    fa.loc = loc;
+    fa.attn = attn;
+    fa.out = out;
+    return dispatch_fwd<false>(fa, dtype, D, stream);
+}
+
+cudaError_t launch_forward_fused(const LaunchGeometry &g, int dtype, int D, const void *value, const float *ref,
+                                 const float *off, const float *logits, void *out, cudaStream_t stream) {
+    FwdArgs fa{};
+    fill_common(fa, g);
+    fa.value = value;
+    fa.ref = ref;
+    fa.off = off;
+    fa.logits = logits;
+    fa.out = out;
+    return dispatch_fwd<true>(fa, dtype, D, stream);
+}
+
+}  // namespace msda

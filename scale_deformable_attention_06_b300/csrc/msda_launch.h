@@ -1,0 +1,34 @@
+// msda_launch.h -- internal interface between the C-ABI layer (msda_api.cu)
+// and the kernel launchers.  Not installed, not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "msda_device.cuh"
+
+namespace msda {
+
+// Everything the kernels need to know about the sizes and the levels; filled
+// and checked on the host by msda_api.cu.
+struct LaunchGeometry {
+    Dims d;
+    LevelTable lv;
+    unsigned char level_of[kMaxSamples];
+};
+
+cudaError_t launch_forward(const LaunchGeometry &g, int dtype, int D, const void *value, const float *loc,
+                           const float *attn, void *out, cudaStream_t stream);
+
+cudaError_t launch_forward_fused(const LaunchGeometry &g, int dtype, int D, const void *value, const float *ref,
+                                 const float *off, const float *logits, void *out, cudaStream_t stream);
+
+// Bytes of workspace for the deterministic backward: fixed-point accumulators
+// plus a 256-byte header.
+size_t backward_workspace_bytes(const LaunchGeometry &g, int D, bool deterministic);
+
+cudaError_t launch_backward(const LaunchGeometry &g, int dtype, int D, const void *value, const float *loc,
+                            const float *attn, const void *grad_out, float *grad_value, float *grad_loc,
+                            float *grad_attn, bool deterministic, bool accumulate, void *workspace,
+                            cudaStream_t stream);
+
+}  // namespace msda

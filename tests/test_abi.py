@@ -1,0 +1,138 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports
+every symbol include/msda.h declares, and rejects bad arguments on the host
+before any launch (no compute call is made here)."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msda.h")
+
+
+@pytest.fixture(scope="module")
+def msda():
+    from scale_deformable_attention_06_b300 import build
+    build.build()
+    import scale_deformable_attention_06_b300 as m
+    return m
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MSDA_API\s+[\w\s\*]+?\b(msda_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    syms = declared_symbols()
+    for name in ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_workspace_size"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(msda):
+    out = subprocess.run(["nm", "-D", "--defined-only", msda.LIBRARY], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(msda_\w+)", out))
+    missing = [s for s in declared_symbols() if s not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    # and nothing else leaks out under the msda_ prefix
+    assert exported == set(declared_symbols())
+    for s in declared_symbols():
+        assert hasattr(msda.lib(), s)
+
+
+def test_library_targets_sm_103a(msda):
+    out = subprocess.run(["cuobjdump", "--list-elf", msda.LIBRARY], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def _problem(msda, **kw):
+    base = dict(N=1, Len_in=80, n_heads=2, head_dim=8, Len_q=80, n_levels=2, n_points=2, dtype=0)
+    base.update(kw)
+    return msda.msda_problem(**base)
+
+
+def _levels(shapes, starts):
+    sh = (ctypes.c_int64 * len(shapes))(*shapes)
+    st = (ctypes.c_int64 * len(starts))(*starts)
+    return sh, st
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails its checks first
+
+
+@pytest.mark.parametrize("kw,shapes,starts,expect", [
+    (dict(head_dim=12), [8, 8, 4, 4], [0, 64], 2),
+    (dict(head_dim=4), [8, 8, 4, 4], [0, 64], 2),
+    (dict(dtype=7), [8, 8, 4, 4], [0, 64], 2),
+    (dict(n_levels=17), [1, 1] * 17, list(range(17)), 2),
+    (dict(n_points=200), [8, 8, 4, 4], [0, 64], 2),
+    (dict(), [8, 8, 4, 4], [0, 63], 1),
+    (dict(), [8, 8, 4, 4], [1, 64], 1),
+    (dict(Len_in=81), [8, 8, 4, 4], [0, 64], 1),
+    (dict(), [8, 0, 4, 4], [0, 0], 1),
+    (dict(N=-1), [8, 8, 4, 4], [0, 64], 1),
+    (dict(n_heads=0), [8, 8, 4, 4], [0, 64], 1),
+])
+def test_host_checks_reject_before_launch(msda, kw, shapes, starts, expect):
+    p = _problem(msda, **kw)
+    sh, st = _levels(shapes, starts)
+    rc = msda.lib().msda_forward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, None)
+    assert rc == expect, msda.lib().msda_last_error()
+    assert msda.lib().msda_last_error().decode()
+    rc = msda.lib().msda_forward_fused(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, None)
+    assert rc == expect
+    rc = msda.lib().msda_backward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None, 0, None)
+    assert rc == expect
+
+
+def test_null_and_misaligned_pointers(msda):
+    p = _problem(msda)
+    sh, st = _levels([8, 8, 4, 4], [0, 64])
+    lib = msda.lib()
+    assert lib.msda_forward(ctypes.byref(p), None, sh, st, FAKE, FAKE, FAKE, None) == 1
+    assert lib.msda_forward(ctypes.byref(p), ctypes.c_void_p(0x10004), sh, st, FAKE, FAKE, FAKE, None) == 1
+    assert lib.msda_forward(None, FAKE, sh, st, FAKE, FAKE, FAKE, None) == 1
+    assert lib.msda_forward(ctypes.byref(p), FAKE, None, st, FAKE, FAKE, FAKE, None) == 1
+    # unknown backward flag
+    assert lib.msda_backward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, None, 0, None) == 1
+    # deterministic mode without a workspace
+    assert lib.msda_backward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, None, 0, None) == 4
+
+
+def test_workspace_size(msda):
+    p = _problem(msda)
+    lib = msda.lib()
+    assert lib.msda_backward_workspace_size(ctypes.byref(p), 0) == 0
+    assert lib.msda_backward_workspace_size(ctypes.byref(p), 1) == 256 + 1 * 80 * 2 * 8 * 8
+    assert lib.msda_version() > 0
+    assert lib.msda_status_string(3) == b"MSDA_ERR_CUDA"
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No silent fallback: without libmsda.so the package does not import."""
+    code = ("import sys, os; sys.path.insert(0, %r); import scale_deformable_attention_06_b300._capi as c" % ROOT)
+    env = dict(os.environ)
+    pkg = os.path.join(ROOT, "scale_deformable_attention_06_b300")
+    # run against a copy of the package without the .so
+    dst = tmp_path / "scale_deformable_attention_06_b300"
+    dst.mkdir()
+    for f in ("__init__.py", "_capi.py"):
+        (dst / f).write_text(open(os.path.join(pkg, f)).read())
+    code = "import sys; sys.path.insert(0, %r); import scale_deformable_attention_06_b300" % str(tmp_path)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    assert r.returncode != 0 and "ImportError" in r.stderr
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "scale_deformable_attention_06_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f"{f} mentions the oracle"
+                assert "_work/" not in text and "/_work" not in text, f"{f} refers to working files"

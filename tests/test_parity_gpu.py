@@ -1,0 +1,227 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Every case runs the same seeded inputs through libmsda on the GPU and through
+the oracle on the CPU and compares element by element:
+  forward fp32   max-abs <= 1e-5 and normwise rel <= 1e-5
+  backward fp32  normwise rel <= 1e-4 per tensor (atomic order is free)
+  bf16 storage   normwise rel <= 2e-2 for bf16 outputs; fp32 gradients of a
+                 bf16 problem are held to the fp32 bar (same rounded inputs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def msda():
+    import scale_deformable_attention_06_b300 as m
+    assert torch.cuda.is_available(), "these tests need a CUDA device"
+    return m
+
+
+def _run_forward(msda, w, p):
+    dt = H.storage_dtype(w)
+    out = msda.msda_forward(H.dev(p["value"], dt), p["spatial_shapes"], p["level_start_index"],
+                            H.dev(p["sampling_locations"]), H.dev(p["attention_weights"]))
+    return out.float().cpu().numpy()
+
+
+def _run_fused(msda, w, p):
+    dt = H.storage_dtype(w)
+    out = msda.msda_forward_fused(H.dev(p["value"], dt), p["spatial_shapes"], p["level_start_index"],
+                                  H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]),
+                                  H.dev(p["attention_logits"]))
+    return out.float().cpu().numpy()
+
+
+def _run_backward(msda, w, p, flags=0):
+    dt = H.storage_dtype(w)
+    gv, gl, ga = msda.msda_backward(H.dev(p["value"], dt), p["spatial_shapes"], p["level_start_index"],
+                                    H.dev(p["sampling_locations"]), H.dev(p["attention_weights"]),
+                                    H.dev(p["grad_output"], dt), flags=flags)
+    return gv.cpu().numpy(), gl.cpu().numpy(), ga.cpu().numpy()
+
+
+def _oracle_forward(p):
+    return oracle.forward(p["value"], p["spatial_shapes"], p["level_start_index"], p["sampling_locations"],
+                          p["attention_weights"])
+
+
+def _oracle_backward(p):
+    return oracle.backward(p["value"], p["spatial_shapes"], p["level_start_index"], p["sampling_locations"],
+                           p["attention_weights"], p["grad_output"])
+
+
+def _check_backward(w, got, ref):
+    dtype = "f32"   # gradients are fp32 outputs of identical (rounded) inputs
+    for name, g, r in zip(("grad_value", "grad_sampling_locations", "grad_attention_weights"), got, ref):
+        H.assert_bwd(g, r, dtype, f"{w.name} {name}")
+
+
+# ----------------------------------------------------------------- workloads
+def test_tiny_forward_backward(msda):
+    w = workloads.WORKLOADS["tiny"]
+    p = H.prepared(w)
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), w.dtype)
+    ref = _oracle_backward(p)
+    _check_backward(w, _run_backward(msda, w, p), ref)
+    _check_backward(w, _run_backward(msda, w, p, msda.MSDA_DETERMINISTIC), ref)
+
+
+def test_encoder_forward_fp32(msda):
+    w = workloads.WORKLOADS["encoder"]
+    p = H.prepared(w)
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), w.dtype, "encoder output")
+
+
+def test_encoder_forward_fused_fp32(msda):
+    w = workloads.WORKLOADS["encoder"]
+    p = H.prepared(w)
+    ref = oracle.forward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
+                               p["sampling_offsets"], p["attention_logits"])
+    H.assert_fwd(_run_fused(msda, w, p), ref, w.dtype, "encoder fused output")
+
+
+def test_decoder_fused_bf16(msda):
+    w = workloads.WORKLOADS["decoder"]
+    p = H.prepared(w)
+    ref = oracle.forward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
+                               p["sampling_offsets"], p["attention_logits"])
+    H.assert_fwd(_run_fused(msda, w, p), ref, w.dtype, "decoder fused output")
+    # the unfused call on the locations the oracle forms agrees as well
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), w.dtype, "decoder output")
+
+
+def test_encoder_train_backward(msda):
+    w = workloads.WORKLOADS["encoder_train"]
+    p = H.prepared(w)
+    ref = _oracle_backward(p)
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), w.dtype)
+    _check_backward(w, _run_backward(msda, w, p), ref)
+    det = [_run_backward(msda, w, p, msda.MSDA_DETERMINISTIC) for _ in range(3)]
+    _check_backward(w, det[0], ref)
+    for other in det[1:]:
+        for a, b in zip(det[0], other):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), "deterministic mode is not bitwise stable"
+
+
+def test_large_bf16_forward_backward(msda):
+    w = workloads.WORKLOADS["large"]
+    p = H.prepared(w)
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), w.dtype, "large output")
+    _check_backward(w, _run_backward(msda, w, p), _oracle_backward(p))
+
+
+# ----------------------------------------------------------------- shapes and edges
+RAGGED_LEVELS = [(7, 5), (3, 9), (1, 1), (2, 1)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("D", [8, 16, 32, 64])
+def test_ragged_all_head_dims(msda, dtype, D):
+    """Len_q not a multiple of the rows a warp owns, odd level sizes
+    including 1x1, 2x1, samples partly outside the maps."""
+    w = workloads.custom(N=2, M=3, D=D, levels=RAGGED_LEVELS, K=3, Len_q=37, dtype=dtype, refs="uniform",
+                         ref_range=(-0.05, 1.05), offset_sigma=0.2, seed=99 + D)
+    p = H.prepared(w)
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), dtype, f"D={D} {dtype} output")
+    ref = oracle.forward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
+                               p["sampling_offsets"], p["attention_logits"])
+    H.assert_fwd(_run_fused(msda, w, p), ref, dtype, f"D={D} {dtype} fused output")
+    ref_b = _oracle_backward(p)
+    _check_backward(w, _run_backward(msda, w, p), ref_b)
+    _check_backward(w, _run_backward(msda, w, p, msda.MSDA_DETERMINISTIC), ref_b)
+
+
+@pytest.mark.parametrize("L,K", [(1, 1), (1, 4), (16, 16), (5, 7)])
+def test_levels_and_points(msda, L, K):
+    """Single-scale (L=1), the largest L*K (256), and a ragged L*K."""
+    levels = [(3 + (l % 4), 2 + (l * 3) % 7) for l in range(L)]
+    w = workloads.custom(N=1, M=2, D=32, levels=levels, K=K, Len_q=21, refs="uniform", ref_range=(0.0, 1.0),
+                         offset_sigma=0.3, seed=7 + L * 31 + K)
+    p = H.prepared(w)
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), "f32")
+    _check_backward(w, _run_backward(msda, w, p), _oracle_backward(p))
+    ref = oracle.forward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
+                               p["sampling_offsets"], p["attention_logits"])
+    H.assert_fwd(_run_fused(msda, w, p), ref, "f32")
+
+
+def test_all_outside_and_integer_coordinates(msda):
+    w = workloads.custom(N=1, M=2, D=16, levels=[(6, 5), (3, 4)], K=4, Len_q=30, refs="none", seed=5)
+    p = H.prepared(w)
+    loc = p["sampling_locations"].copy()
+    rng = np.random.Generator(np.random.PCG64(8))
+    # first third: far outside; second third: exact pixel corners (integer px);
+    # last third: exactly on the outer border lines px = -1 and px = W
+    n = loc.shape[1] // 3
+    loc[:, :n] = rng.choice([-3.0, 4.0], size=loc[:, :n].shape)
+    for l, (Hl, Wl) in enumerate(w.levels):
+        ix = rng.integers(-1, Wl + 1, size=loc[:, n:2 * n, :, l, :, 0].shape)
+        iy = rng.integers(-1, Hl + 1, size=loc[:, n:2 * n, :, l, :, 1].shape)
+        loc[:, n:2 * n, :, l, :, 0] = (ix + 0.5) / Wl
+        loc[:, n:2 * n, :, l, :, 1] = (iy + 0.5) / Hl
+        loc[:, 2 * n:, :, l, :, 0] = rng.choice([-0.5 / Wl, (Wl + 0.5) / Wl], size=loc[:, 2 * n:, :, l, :, 0].shape)
+    p["sampling_locations"] = loc.astype(np.float32)
+    got = _run_forward(msda, w, p)
+    H.assert_fwd(got, _oracle_forward(p), "f32")
+    assert np.all(got[:, :n] == 0.0)
+    _check_backward(w, _run_backward(msda, w, p), _oracle_backward(p))
+
+
+def test_empty_problems(msda):
+    w = workloads.custom(N=2, M=2, D=8, levels=[(4, 4)], K=2, Len_q=5, refs="none", seed=3)
+    p = H.prepared(w)
+    dev = "cuda"
+    value = H.dev(p["value"])
+    # Len_q = 0: nothing to sample; backward still zeroes grad_value
+    loc0 = torch.zeros((2, 0, 2, 1, 2, 2), device=dev)
+    a0 = torch.zeros((2, 0, 2, 1, 2), device=dev)
+    out = msda.msda_forward(value, p["spatial_shapes"], p["level_start_index"], loc0, a0)
+    assert out.shape == (2, 0, 16)
+    gv = torch.full_like(value, 7.0)
+    msda.msda_backward(value, p["spatial_shapes"], p["level_start_index"], loc0, a0, torch.zeros((2, 0, 16), device=dev),
+                       grad_value=gv)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(gv).item() == 0
+    # N = 0
+    v0 = torch.zeros((0, 16, 2, 8), device=dev)
+    out = msda.msda_forward(v0, p["spatial_shapes"], p["level_start_index"], torch.zeros((0, 5, 2, 1, 2, 2), device=dev),
+                            torch.zeros((0, 5, 2, 1, 2), device=dev))
+    assert out.shape == (0, 5, 16)
+
+
+def test_accumulate_grad_value(msda):
+    w = workloads.WORKLOADS["tiny"]
+    p = H.prepared(w)
+    gv0 = np.random.Generator(np.random.PCG64(4)).standard_normal(p["value"].shape).astype(np.float32)
+    ref_gv, _, _ = _oracle_backward(p)
+    for flags in (msda.MSDA_ACCUMULATE_GRAD_VALUE, msda.MSDA_ACCUMULATE_GRAD_VALUE | msda.MSDA_DETERMINISTIC):
+        gv = H.dev(gv0)
+        msda.msda_backward(H.dev(p["value"]), p["spatial_shapes"], p["level_start_index"], H.dev(p["sampling_locations"]),
+                           H.dev(p["attention_weights"]), H.dev(p["grad_output"]), grad_value=gv, flags=flags)
+        H.assert_bwd(gv.cpu().numpy(), gv0 + ref_gv, "f32", "accumulated grad_value")
+
+
+def test_invalid_arguments_return_errors(msda):
+    w = workloads.WORKLOADS["tiny"]
+    p = H.prepared(w)
+    value = H.dev(p["value"])
+    loc, attn = H.dev(p["sampling_locations"]), H.dev(p["attention_weights"])
+    bad_starts = p["level_start_index"].copy()
+    bad_starts[1] += 1
+    with pytest.raises(msda.MSDAError) as e:
+        msda.msda_forward(value, p["spatial_shapes"], bad_starts, loc, attn)
+    assert e.value.name == "MSDA_ERR_INVALID_ARG"
+    with pytest.raises(msda.MSDAError) as e:
+        msda.msda_forward(value[..., :4].contiguous(), p["spatial_shapes"], p["level_start_index"],
+                          loc, attn, output=torch.empty((1, 80, 8), device="cuda"))
+    assert e.value.name == "MSDA_ERR_UNSUPPORTED"
+    with pytest.raises(ValueError):
+        msda.msda_forward(value.cpu(), p["spatial_shapes"], p["level_start_index"], loc, attn)
