@@ -239,6 +239,14 @@ def run_ours(args):
     pts = w.samples
     value_pts = aggregate(pts, world, total_s / args.steps)
     ab = algorithmic_bytes(w)
+    if args.only_step:          # profiling runs: the timed step alone
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value_pts, "unit": UNIT, "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
+                              "only_step": True}))
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # ---- per-kernel times (same protocol) for the roofline and the parts
     reps = max(10, min(args.steps, 200))
@@ -352,15 +360,11 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
+    import oracle
     w = workloads.WORKLOADS[args.workload]
     raw = workloads.draw(w)
-    sh = raw["spatial_shapes"]
-    wh = np.asarray(sh[:, [1, 0]], dtype=np.float64)
-    loc = (raw["reference_points"].astype(np.float64)[:, :, None, :, None, :]
-           + raw["sampling_offsets"].astype(np.float64) / wh[None, None, None, :, None, :]).astype(np.float32)
-    x = raw["attention_logits"].astype(np.float64)
-    e = np.exp(x - x.max(-1, keepdims=True))
-    attn = (e / e.sum(-1, keepdims=True)).astype(np.float32).reshape(loc.shape[:-1])
+    loc = oracle.locations(raw["spatial_shapes"], raw["reference_points"], raw["sampling_offsets"]).astype(np.float32)
+    attn = oracle.softmax(raw["attention_logits"]).astype(np.float32).reshape(loc.shape[:-1])
     # one step = forward + backward of a bounded query sample (all batches)
     q_per_step = max(1, w.Lq // 16)
     starts = [(i * q_per_step) % max(1, w.Lq - q_per_step) for i in range(args.warmup + args.steps)]
@@ -392,6 +396,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-step", action="store_true", help="time the step only (for profiler runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -39,7 +39,7 @@ class msda_problem(ctypes.Structure):
 
 def _load():
     if not os.path.exists(LIBRARY):
-        raise ImportError(f"{LIBRARY} is missing: build it with `python -m scale_deformable_attention_06_b300.build`")
+        raise ImportError(f"{LIBRARY} is missing: build it with `python scale_deformable_attention_06_b300/build.py` (or __graft_entry__.build())")
     lib = ctypes.CDLL(LIBRARY)
     vp, i64p, fp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p
     pp = ctypes.POINTER(msda_problem)

@@ -1,6 +1,6 @@
 """Build libmsda.so (the CUDA kernels and the C ABI) in-tree, for sm_103a.
 
-    python -m scale_deformable_attention_06_b300.build [--force] [--verbose]
+    python scale_deformable_attention_06_b300/build.py [--force] [--verbose]
 
 The library links the shared CUDA runtime (libcudart.so.13), so it shares the
 runtime state (current device, streams) of the process that loads it.

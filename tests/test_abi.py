@@ -15,8 +15,8 @@ HEADER = os.path.join(ROOT, "include", "msda.h")
 
 @pytest.fixture(scope="module")
 def msda():
-    from scale_deformable_attention_06_b300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import scale_deformable_attention_06_b300 as m
     return m
 
