@@ -179,6 +179,41 @@ MSDA_API msda_status msda_backward(const msda_problem *problem, const void *valu
                           float *grad_sampling_locations, float *grad_attention_weights,
                           unsigned flags, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * msda_backward_noalloc -- msda_backward in MSDA_DETERMINISTIC mode without a
+ * caller workspace.  The pages have no counterpart of this entry point; it
+ * exists for callers that cannot allocate device memory: a plugin that a host
+ * application hands only its input and output buffers (and that may not call
+ * cudaMalloc or the host's allocator), or a loop that must not allocate after
+ * start-up because cudaMalloc/cudaFree can synchronize the device.
+ *
+ * The scratch lives in the library: one 64 MiB device array (fixed-point
+ * accumulators plus a 256-byte header), which every GPU that loads the
+ * library holds until the process exits.  Problems with
+ * N * Len_in * n_heads * head_dim above 8,388,576 elements do not fit and are
+ * rejected with MSDA_ERR_UNSUPPORTED before anything is launched; use
+ * msda_backward with a workspace for them.
+ *
+ * Same arguments, results and checks as msda_backward with
+ * flags = MSDA_DETERMINISTIC, except that there is no workspace and `flags`
+ * accepts only MSDA_ACCUMULATE_GRAD_VALUE.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree.
+ *
+ * The first call on a device looks up the device address of the scratch
+ * array (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call clears the part of the scratch it
+ * uses before summing into it.  All calls on one device share the one
+ * array, so calls whose kernels overlap on the GPU (on different streams, or
+ * from different threads) race on it and give wrong results: order them on
+ * one stream or synchronize between them.
+ */
+MSDA_API msda_status msda_backward_noalloc(const msda_problem *problem, const void *value,
+                                           const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                           const float *sampling_locations, const float *attention_weights,
+                                           const void *grad_output, float *grad_value,
+                                           float *grad_sampling_locations, float *grad_attention_weights,
+                                           unsigned flags, void *stream);
+
 /* Name of a status code (static string). */
 MSDA_API const char *msda_status_string(msda_status status);
 

@@ -21,7 +21,7 @@ MSDA_DETERMINISTIC = 1
 MSDA_ACCUMULATE_GRAD_VALUE = 2
 
 EXPORTED = ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_workspace_size",
-            "msda_status_string", "msda_last_error", "msda_version")
+            "msda_backward_noalloc", "msda_status_string", "msda_last_error", "msda_version")
 
 
 class MSDAError(RuntimeError):
@@ -46,6 +46,8 @@ def _load():
     lib.msda_forward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, vp]
     lib.msda_forward_fused.argtypes = [pp, vp, i64p, i64p, fp, fp, fp, vp, vp]
     lib.msda_backward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, fp, fp, fp, ctypes.c_uint, vp, ctypes.c_size_t, vp]
+    lib.msda_backward_noalloc.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, fp, fp, fp, ctypes.c_uint, vp]
+    lib.msda_backward_noalloc.restype = ctypes.c_int
     lib.msda_backward_workspace_size.argtypes = [pp, ctypes.c_uint]
     lib.msda_backward_workspace_size.restype = ctypes.c_size_t
     for f in ("msda_forward", "msda_forward_fused", "msda_backward"):
@@ -203,4 +205,24 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, 
                               _dev(grad_sampling_locations, "grad_sampling_locations", torch.float32),
                               _dev(grad_attention_weights, "grad_attention_weights", torch.float32),
                               flags, ws_ptr, ws_bytes, _stream(stream, dev)))
+    return grad_value, grad_sampling_locations, grad_attention_weights
+
+
+def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
+                          grad_output, grad_value, grad_sampling_locations, grad_attention_weights, flags=0,
+                          stream=None):
+    """Deterministic backward with the library's built-in scratch (no workspace,
+    no allocation anywhere, the outputs included: the caller passes them).
+    For callers that may not allocate device memory; see include/msda.h for
+    the size limit and for why overlapping calls race."""
+    lv = _HostLevels(spatial_shapes, level_start_index)
+    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
+    prob = problem(value, Lq, L, K)
+    _check(_lib.msda_backward_noalloc(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
+                                      _dev(sampling_locations, "sampling_locations", torch.float32),
+                                      _dev(attention_weights, "attention_weights", torch.float32),
+                                      _dev(grad_output, "grad_output"), _dev(grad_value, "grad_value", torch.float32),
+                                      _dev(grad_sampling_locations, "grad_sampling_locations", torch.float32),
+                                      _dev(grad_attention_weights, "grad_attention_weights", torch.float32),
+                                      flags, _stream(stream, value.device)))
     return grad_value, grad_sampling_locations, grad_attention_weights

@@ -90,6 +90,36 @@ msda_status cuda_status(cudaError_t e, const char *what) {
 
 }  // namespace
 
+// Helpers of msda_backward_noalloc (msda_noalloc.cu): the same host checks as
+// msda_backward, reached from the other translation unit.
+namespace msda {
+
+msda_status noalloc_fail(msda_status s, const char *msg) { return fail(s, "%s", msg); }
+
+msda_status noalloc_check_and_geometry(const msda_problem *problem, const int64_t *spatial_shapes,
+                                       const int64_t *level_start_index, LaunchGeometry &g) {
+    g_last_error[0] = 0;
+    return make_geometry(problem, spatial_shapes, level_start_index, g);
+}
+
+msda_status noalloc_check_pointers(const msda_problem *problem, const LaunchGeometry &g, const void *value,
+                                   const float *loc, const float *attn, const void *grad_out, const float *grad_value,
+                                   const float *grad_loc, const float *grad_attn) {
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * problem->head_dim;
+    if (nval > 0 && !grad_value) return fail(MSDA_ERR_INVALID_ARG, "grad_value is NULL");
+    if (grad_value && !aligned(grad_value, 16)) return fail(MSDA_ERR_INVALID_ARG, "grad_value not 16-byte aligned");
+    if (g.d.rows > 0) {
+        if (!value || !loc || !attn || !grad_out || !grad_loc || !grad_attn)
+            return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+        if (!aligned(value, 16) || !aligned(grad_out, 16) || !aligned(loc, 8) || !aligned(grad_loc, 8) ||
+            !aligned(attn, 4) || !aligned(grad_attn, 4))
+            return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor");
+    }
+    return MSDA_OK;
+}
+
+}  // namespace msda
+
 extern "C" {
 
 msda_status msda_forward(const msda_problem *problem, const void *value, const int64_t *spatial_shapes,
