@@ -55,6 +55,8 @@ msda_status make_geometry(const msda_problem *p, const int64_t *shapes, const in
     }
     if (expect != p->Len_in)
         return fail(MSDA_ERR_INVALID_ARG, "sum of H*W over levels is %lld but Len_in is %d", (long long)expect, p->Len_in);
+    if (p->Len_in >= (int64_t(1) << 28))
+        return fail(MSDA_ERR_UNSUPPORTED, "Len_in %d is not below 2^28 (pixel index of a corner record)", p->Len_in);
     const int64_t pix = (int64_t)p->n_heads * p->head_dim;
     if ((p->Len_in + 2 * maxW + 4) * pix >= (int64_t(1) << 31))
         return fail(MSDA_ERR_UNSUPPORTED, "(Len_in + 2 W + 4) * n_heads * head_dim exceeds 2^31");

@@ -9,19 +9,31 @@
 // derived from the bilinear form of "可变形注意力：多尺度稀疏采样与视觉检测实战
 // 解析" §2.3 (continuous, so the gradient reaches the offset branch).
 //
-// Work decomposition follows the forward (msda_forward.cu): a warp owns HW
-// rows with R lanes per row; phase 1 stages corner records in shared memory,
-// phase 2 gathers the four corner vectors of each sample, forms the per-corner
-// dot products <g, v_c> over the lane's channels, reduces them over the R
-// lanes of the row with shuffles, and scatters A * w_c * g into grad_value with
-// one vector reduction (red.global.add.v4.f32) per corner and 4 channels;
-// phase 3 writes the chunk's grad_attention_weights / grad_sampling_locations
-// coalesced.
+// Work decomposition.  A warp owns HW consecutive queries of one (n, head m)
+// ("head-major"), every lane 4 channels of one of them (R = D / 4 lanes per
+// query, HW = 32 / R).  Per chunk of up to RC samples:
+//   phase 1: one 16-byte corner record per (query, sample) into warp-private
+//            shared memory (pack_record), reads contiguous along the samples;
+//   phase 2: per sample, four gathers of the lane's channels; the lane forms
+//            its partial <g, v_c> and from them its partial grad_attn, d/dpx,
+//            d/dpy (all linear in the dot products), which a reduce-scatter
+//            over the R lanes sums with 2 + log2(R/4) shuffles instead of
+//            3 * log2(R); then the grad_value contributions A * w_c * g;
+//   phase 3: the chunk's per-sample gradients, written contiguously.
+// grad_value contributions go out as one vector reduction (red.global.add.v4
+// .f32) per corner and lane, or, on densely sampled levels of a D = 32
+// problem, through a per-warp merge table: the HW queries of a warp are
+// neighbours, so on a coarse level their corners often coincide; the table
+// sums, per distinct corner pixel, one coefficient per query, and one
+// reduction per distinct pixel carries sum_h alpha_h * g_h.  Either way every
+// contribution is added exactly once.
 //
 // Deterministic mode replaces the fp32 reductions by 64-bit integer ones in
 // fixed point (integer addition is associative, so the order in which the
 // atomics land does not matter), with a scale chosen from a bound on the total
-// |contribution| so that no sum can overflow, then converts to fp32.
+// |contribution| so that no sum can overflow, then converts to fp32.  The
+// merge table's fp32 coefficient sums are formed in a fixed order (program
+// order of the samples), so they too are the same from run to run.
 #include "msda_device.cuh"
 #include "msda_launch.h"
 
@@ -40,10 +52,12 @@ struct BwdArgs {
     Dims d;
     LevelTable lv;
     unsigned char level_of[kMaxSamples];
+    int qblocks;                   // ceil(Len_q / HW) query blocks per (n, head)
+    unsigned merge_mask;           // bit l: merge grad_value contributions on level l
 };
 
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+__device__ __forceinline__ void red_add_v4(float *p, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
 }
 
@@ -62,137 +76,245 @@ __device__ __forceinline__ int fixed_shift(unsigned bits, int rows) {
     return shift < -60 ? -60 : (shift > 100 ? 100 : shift);
 }
 
-template <typename T, int D, bool DET>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-msda_backward_kernel(const __grid_constant__ BwdArgs a) {
-    using Lay = Layout<T, D>;
-    constexpr int V = Lay::V, R = Lay::R, HW = Lay::HW;
-    constexpr int JC = kRecordsPerWarp / HW;
+// grad_value[dst .. dst + 4) += v (fp32 reduction, or fixed point)
+template <bool DET>
+__device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, float4 v, float scale) {
+    if constexpr (DET) {
+        unsigned long long *p = a.fixed + dst;
+        red_add_u64(p + 0, __float2ll_rn(v.x * scale));
+        red_add_u64(p + 1, __float2ll_rn(v.y * scale));
+        red_add_u64(p + 2, __float2ll_rn(v.z * scale));
+        red_add_u64(p + 3, __float2ll_rn(v.w * scale));
+    } else {
+        red_add_v4(a.grad_value + dst, v);
+    }
+}
 
-    __shared__ int4 s_off[kWarpsPerBlock][kRecordsPerWarp];
-    __shared__ float4 s_w[kWarpsPerBlock][kRecordsPerWarp];    // bilinear * mask
-    __shared__ float4 s_aux[kWarpsPerBlock][kRecordsPerWarp];  // fx, fy, A, mask bits
-    __shared__ float4 s_res[kWarpsPerBlock][kRecordsPerWarp];  // gA, A*d/dpx, A*d/dpy
+// Sums three per-lane partials over the R lanes of a query (lanes h*R .. h*R+R-1
+// of the warp).  Afterwards the lane holds in out[0] the total of value
+// `first` (0: x0, 1: x1, 2: x2, 3: nothing) and, for R == 2, in out[1] the total
+// of value first + 1.  All 32 lanes must call it.
+template <int R>
+__device__ __forceinline__ void reduce_scatter3(float x0, float x1, float x2, int ch, float (&out)[2], int &first) {
+    const bool hb = (ch & (R / 2)) != 0;
+    const float s0 = __shfl_xor_sync(0xffffffffu, hb ? x0 : x2, R / 2);
+    const float s1 = __shfl_xor_sync(0xffffffffu, hb ? x1 : 0.f, R / 2);
+    const float y0 = (hb ? x2 : x0) + s0, y1 = (hb ? 0.f : x1) + s1;
+    if constexpr (R == 2) {
+        out[0] = y0;
+        out[1] = y1;
+        first = hb ? 2 : 0;
+    } else {
+        const bool lb = (ch & (R / 4)) != 0;
+        float z = (lb ? y1 : y0) + __shfl_xor_sync(0xffffffffu, lb ? y0 : y1, R / 4);
+#pragma unroll
+        for (int o = R / 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        out[0] = z;
+        out[1] = 0.f;
+        first = (hb ? 2 : 0) + (lb ? 1 : 0);
+    }
+}
+
+constexpr unsigned kEmptyKey = 0xffffffffu;
+constexpr int kMergeSlots = 128;       // per warp; a merge chunk has at most 64 entries
+constexpr int kMergeSamples = 4;       // samples per merge chunk (4 queries x 4 x 4 corners = 64 entries)
+
+template <int HW, int RC, bool MERGE>
+struct BwdWarpSmem {
+    uint4 rec[HW][RC + 1];             // corner records (padded rows)
+    float4 res[HW][RC + 1];            // per sample: grad_attn, A*d/dpx, A*d/dpy
+};
+
+template <int HW, int RC>
+struct BwdWarpSmem<HW, RC, true> {
+    uint4 rec[HW][RC + 1];
+    float4 res[HW][RC + 1];
+    unsigned key[kMergeSlots];         // corner pixel of the slot, kEmptyKey if free
+    float4 alpha[kMergeSlots];         // per query of the warp: summed A * w_c (HW == 4)
+    unsigned short list[kMergeSlots];  // occupied slots in order of first use
+    int count;
+};
+
+template <typename T, int D, bool DET, bool MERGE>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
+msda_backward_kernel(const __grid_constant__ BwdArgs a) {
+    constexpr int R = D / 4, HW = 32 / R;
+    constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
+    static_assert(!MERGE || HW == 4, "the merge table holds four queries per slot");
+    using WS = BwdWarpSmem<HW, RC, MERGE>;
+    __shared__ WS smem[kWarpsPerBlock];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = (blockIdx.x * kWarpsPerBlock + warp) * HW;
+    WS &sm = smem[warp];
     const Dims &dm = a.d;
-    if (row0 >= dm.rows) return;
+    const int task = blockIdx.x * kWarpsPerBlock + warp;
+    if (task >= dm.N * a.qblocks * dm.M) return;       // warp-uniform
+    const int m = task % dm.M, t2 = task / dm.M;
+    const int qb = t2 % a.qblocks, n = t2 / a.qblocks;
     const int P = dm.P;
-
     const int h = lane / R, ch = lane % R;
-    const int row = row0 + h;
-    const bool row_ok = row < dm.rows;
-    const int rowc = row_ok ? row : dm.rows - 1;
-    const int n = rowc / dm.qm;
-    const int m = rowc % dm.M;
-    const size_t vrow = ((size_t)n * dm.Len_in * dm.M + m) * D + ch * V;
-    const T *vbase = static_cast<const T *>(a.value) + vrow;
+    const int q = qb * HW + h;
+    const bool row_ok = q < dm.Len_q;
+    const int row = (n * dm.Len_q + (row_ok ? q : qb * HW)) * dm.M + m;
+    const size_t vhead = ((size_t)n * dm.Len_in * dm.M + m) * D + ch * 4;   // (n, pixel 0, m, lane channels)
+    const T *vbase = static_cast<const T *>(a.value) + vhead;
     const uint64_t pol = l2_keep_policy();
 
-    float g[V];
-    load_row_f32<T, V>(static_cast<const T *>(a.grad_out) + (size_t)rowc * D + ch * V, g);
-    if (!row_ok) {
-#pragma unroll
-        for (int i = 0; i < V; ++i) g[i] = 0.f;
-    }
+    float4 g = load4_stream<T>(static_cast<const T *>(a.grad_out) + (size_t)row * D + ch * 4);
+    if (!row_ok) g = make_float4(0.f, 0.f, 0.f, 0.f);
     float scale = 1.f;
     if constexpr (DET) scale = ldexpf(1.f, fixed_shift(*a.bound_bits, dm.rows));
 
-    for (int s0 = 0; s0 < P; s0 += JC) {
-        const int J = min(JC, P - s0);
-        // ---- phase 1: corner records
-        for (int i = lane; i < HW * J; i += 32) {
-            const int hh = i % HW, j = i / HW;
-            const int r = row0 + hh, s = s0 + j;
-            int4 off = make_int4(0, 0, 0, 0);
-            float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 aux = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < dm.rows) {
-                const int l = a.level_of[s];
+    float4 gall[MERGE ? HW : 1];       // merge flush: this lane's channels of every query of the warp
+    if constexpr (MERGE) {
+#pragma unroll
+        for (int hh = 0; hh < HW; ++hh) {
+            gall[hh].x = __shfl_sync(0xffffffffu, g.x, hh * R + ch);
+            gall[hh].y = __shfl_sync(0xffffffffu, g.y, hh * R + ch);
+            gall[hh].z = __shfl_sync(0xffffffffu, g.z, hh * R + ch);
+            gall[hh].w = __shfl_sync(0xffffffffu, g.w, hh * R + ch);
+        }
+        for (int i = lane; i < kMergeSlots; i += 32) {
+            sm.key[i] = kEmptyKey;
+            sm.alpha[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (lane == 0) sm.count = 0;
+        __syncwarp();
+    }
+
+    for (int r0 = 0; r0 < P; r0 += RC) {
+        const int RJ = min(RC, P - r0);
+        // ---- phase 1: corner records of samples r0 .. r0 + RJ
+        for (int i = lane; i < HW * RC; i += 32) {
+            const int j = i % RC, hh = i / RC;
+            if (j >= RJ) continue;
+            const int qq = qb * HW + hh;
+            uint4 rc = make_uint4(0u, 0u, 0u, 0u);
+            if (qq < dm.Len_q) {
+                const int l = a.level_of[r0 + j];
                 const float Wf = a.lv.Wf[l], Hf = a.lv.Hf[l];
-                const size_t si = (size_t)r * P + s;
+                const size_t si = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + r0 + j;
                 const float2 lc = load_stream2(a.loc + 2 * si);
                 float x0, fx, y0, fy;
                 pixel_coord(lc.x, Wf, x0, fx);
                 pixel_coord(lc.y, Hf, y0, fy);
-                const float A = load_stream1(a.attn + si);
-                Corners c = make_corners(x0, fx, y0, fy, a.lv.W[l], a.lv.H[l], Wf, Hf, a.lv.start[l], dm.pix);
-                off = c.off;
-                w = c.w;
-                aux = make_float4(fx, fy, A, __uint_as_float(c.mask));
+                rc = pack_record(x0, fx, y0, fy, load_stream1(a.attn + si), a.lv.W[l], a.lv.H[l], Wf, Hf,
+                                 a.lv.start[l]);
             }
-            s_off[warp][i] = off;
-            s_w[warp][i] = w;
-            s_aux[warp][i] = aux;
+            sm.rec[hh][j] = rc;
         }
         __syncwarp();
-        // ---- phase 2: gather, dot products, scatter into grad_value
-        for (int j = 0; j < J; ++j) {
-            const int rec = j * HW + h;
-            const int4 o = s_off[warp][rec];
-            const float4 w = s_w[warp][rec];
-            const float4 ax = s_aux[warp][rec];
-            const unsigned mask = __float_as_uint(ax.w);
-            const Vec<T> v0 = load_value(vbase + o.x, pol);
-            const Vec<T> v1 = load_value(vbase + o.y, pol);
-            const Vec<T> v2 = load_value(vbase + o.z, pol);
-            const Vec<T> v3 = load_value(vbase + o.w, pol);
-            float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+        // ---- phase 2, one level (or merge chunk) at a time
+        for (int s0 = r0; s0 < r0 + RJ;) {
+            const int l = a.level_of[s0];
+            const bool merge = MERGE && ((a.merge_mask >> l) & 1u);
+            int J = r0 + RJ - s0;
+            if (merge && J > kMergeSamples) J = kMergeSamples;
+            for (int jj = 1; jj < J; ++jj)
+                if (a.level_of[s0 + jj] != l) { J = jj; break; }
+            const int W = a.lv.W[l];
+            // one sample at a time: unrolling raises the register count past the
+            // 64 that four resident blocks allow, and measured slower
+#pragma unroll 1
+            for (int j = s0 - r0; j < s0 - r0 + J; ++j) {
+                const Unpacked u = unpack_record(sm.rec[h][j], W);
+                float4 v[4];
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                t0 = __fmaf_rn(g[i], v0.get(i), t0);
-                t1 = __fmaf_rn(g[i], v1.get(i), t1);
-                t2 = __fmaf_rn(g[i], v2.get(i), t2);
-                t3 = __fmaf_rn(g[i], v3.get(i), t3);
-            }
+                for (int c = 0; c < 4; ++c) v[c] = load4_value(vbase + (size_t)u.pix[c] * dm.pix, pol);
+                // partial <g, v_c> over this lane's channels
+                float t[4];
 #pragma unroll
-            for (int o2 = R / 2; o2 > 0; o2 >>= 1) {
-                t0 += __shfl_xor_sync(0xffffffffu, t0, o2);
-                t1 += __shfl_xor_sync(0xffffffffu, t1, o2);
-                t2 += __shfl_xor_sync(0xffffffffu, t2, o2);
-                t3 += __shfl_xor_sync(0xffffffffu, t3, o2);
-            }
-            // corners outside the map read as zero in the gradient formulas
-            t0 = (mask & 1u) ? t0 : 0.f;
-            t1 = (mask & 2u) ? t1 : 0.f;
-            t2 = (mask & 4u) ? t2 : 0.f;
-            t3 = (mask & 8u) ? t3 : 0.f;
-            const float fx = ax.x, fy = ax.y, A = ax.z;
-            if (ch == 0) {
-                const float ga = w.x * t0 + w.y * t1 + w.z * t2 + w.w * t3;
-                const float dx = (1.f - fy) * (t1 - t0) + fy * (t3 - t2);
-                const float dy = (1.f - fx) * (t2 - t0) + fx * (t3 - t1);
-                s_res[warp][rec] = make_float4(ga, A * dx, A * dy, 0.f);
-            }
-            if (row_ok) {
-                const float cw[4] = {A * w.x, A * w.y, A * w.z, A * w.w};
-                const int co[4] = {o.x, o.y, o.z, o.w};
+                for (int c = 0; c < 4; ++c)
+                    t[c] = __fmaf_rn(g.w, v[c].w, __fmaf_rn(g.z, v[c].z, __fmaf_rn(g.y, v[c].y, g.x * v[c].x)));
+                // partial grad_attn, d/dpx, d/dpy; corners outside the map read as zero
+                const float gy0 = 1.f - u.fy, gx0 = 1.f - u.fx;
+                const float pga = u.w[0] * t[0] + u.w[1] * t[1] + u.w[2] * t[2] + u.w[3] * t[3];
+                const float pdx = (u.in[1] ? gy0 * t[1] : 0.f) - (u.in[0] ? gy0 * t[0] : 0.f) +
+                                  (u.in[3] ? u.fy * t[3] : 0.f) - (u.in[2] ? u.fy * t[2] : 0.f);
+                const float pdy = (u.in[2] ? gx0 * t[2] : 0.f) - (u.in[0] ? gx0 * t[0] : 0.f) +
+                                  (u.in[3] ? u.fx * t[3] : 0.f) - (u.in[1] ? u.fx * t[1] : 0.f);
+                float tot[2];
+                int first;
+                reduce_scatter3<R>(pga, pdx, pdy, ch, tot, first);
+                if (R <= 4 || (ch & (R / 4 - 1)) == 0) {
+                    float *rs = reinterpret_cast<float *>(&sm.res[h][j]);
+                    if (first < 3) rs[first] = first == 0 ? tot[0] : u.A * tot[0];
+                    if (R == 2 && first == 0) rs[1] = u.A * tot[1];
+                }
+                if (row_ok) {
+                    if (!merge) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (!(mask & (1u << c))) continue;
-                    if constexpr (DET) {
-                        unsigned long long *dst = a.fixed + vrow + co[c];
-#pragma unroll
-                        for (int i = 0; i < V; ++i) red_add_u64(dst + i, __float2ll_rn(cw[c] * g[i] * scale));
-                    } else {
-                        float *dst = a.grad_value + vrow + co[c];
-#pragma unroll
-                        for (int i = 0; i < V; i += 4)
-                            red_add_v4(dst + i, cw[c] * g[i], cw[c] * g[i + 1], cw[c] * g[i + 2], cw[c] * g[i + 3]);
+                        for (int c = 0; c < 4; ++c) {
+                            if (!u.in[c]) continue;
+                            const float cw = u.A * u.w[c];
+                            scatter4<DET>(a, vhead + (size_t)u.pix[c] * dm.pix,
+                                          make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w), scale);
+                        }
+                    } else if constexpr (MERGE) {
+                        // lanes ch < 4 insert corner c = ch of their query; the valid
+                        // corners of one sample are distinct pixels, so no two lanes of
+                        // one step touch the same (slot, query) coefficient
+                        if (ch < 4) {
+                            const int c = ch;
+                            const bool inside = c == 0 ? u.in[0] : c == 1 ? u.in[1] : c == 2 ? u.in[2] : u.in[3];
+                            if (inside) {
+                                const unsigned key = c == 0 ? u.pix[0] : c == 1 ? u.pix[1] : c == 2 ? u.pix[2] : u.pix[3];
+                                const float coef = u.A * (c == 0 ? u.w[0] : c == 1 ? u.w[1] : c == 2 ? u.w[2] : u.w[3]);
+                                // at most 64 keys per chunk in 128 slots: a free or matching
+                                // slot is always found
+                                unsigned slot = key & (kMergeSlots - 1);
+                                for (int probe = 0; probe < kMergeSlots; ++probe) {
+                                    const unsigned old = atomicCAS(&sm.key[slot], kEmptyKey, key);
+                                    if (old == kEmptyKey) sm.list[atomicAdd(&sm.count, 1)] = (unsigned short)slot;
+                                    if (old == kEmptyKey || old == key) {
+                                        reinterpret_cast<float *>(&sm.alpha[slot])[h] += coef;
+                                        break;
+                                    }
+                                    slot = (slot + 1) & (kMergeSlots - 1);
+                                }
+                            }
+                        }
                     }
                 }
+                __syncwarp();
             }
+            if constexpr (MERGE) {
+                if (merge) {
+                    // one reduction per distinct corner pixel and lane: sum_h alpha_h * g_h
+                    const int U = sm.count;
+                    for (int u0 = 0; u0 < U; u0 += HW) {
+                        const int ui = u0 + h;
+                        if (ui < U) {
+                            const int slot = sm.list[ui];
+                            const float4 al = sm.alpha[slot];
+                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                            acc = ffma4(al.x, gall[0], acc);
+                            acc = ffma4(al.y, gall[1], acc);
+                            acc = ffma4(al.z, gall[2], acc);
+                            acc = ffma4(al.w, gall[3], acc);
+                            scatter4<DET>(a, vhead + (size_t)sm.key[slot] * dm.pix, acc, scale);
+                        }
+                    }
+                    __syncwarp();
+                    for (int ui = lane; ui < U; ui += 32) {
+                        const int slot = sm.list[ui];
+                        sm.key[slot] = kEmptyKey;
+                        sm.alpha[slot] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    if (lane == 0) sm.count = 0;
+                    __syncwarp();
+                }
+            }
+            s0 += J;
         }
-        __syncwarp();
-        // ---- phase 3: per-sample gradients, coalesced
-        for (int i = lane; i < HW * J; i += 32) {
-            const int hh = i % HW, j = i / HW;
-            const int r = row0 + hh, s = s0 + j;
-            if (r < dm.rows) {
-                const int l = a.level_of[s];
-                const float4 res = s_res[warp][i];
-                const size_t si = (size_t)r * P + s;
+        // ---- phase 3: per-sample gradients of the chunk
+        for (int i = lane; i < HW * RC; i += 32) {
+            const int j = i % RC, hh = i / RC;
+            const int qq = qb * HW + hh;
+            if (j < RJ && qq < dm.Len_q) {
+                const int l = a.level_of[r0 + j];
+                const size_t si = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + r0 + j;
+                const float4 res = sm.res[hh][j];
                 __stcs(a.grad_attn + si, res.x);
                 __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si, make_float2(res.y * a.lv.Wf[l], res.z * a.lv.Hf[l]));
             }
@@ -252,11 +374,22 @@ size_t backward_workspace_bytes(const LaunchGeometry &g, int D, bool determinist
     return 256 + n * sizeof(unsigned long long);
 }
 
+// Levels whose samples are dense enough that neighbouring queries' corners
+// often coincide: Len_q * n_points samples on H*W pixels, at least 32 per pixel.
+static unsigned merge_levels(const LaunchGeometry &g) {
+    unsigned mask = 0;
+    for (int l = 0; l < g.d.L; ++l) {
+        const double pixels = (double)g.lv.H[l] * (double)g.lv.W[l];
+        if ((double)g.d.Len_q * g.d.K >= 32.0 * pixels) mask |= 1u << l;
+    }
+    return mask;
+}
+
 template <typename T, int D>
 static cudaError_t launch_bwd_t(const LaunchGeometry &g, const void *value, const float *loc, const float *attn,
                                 const void *grad_out, float *grad_value, float *grad_loc, float *grad_attn,
                                 bool det, bool accumulate, void *workspace, cudaStream_t stream) {
-    constexpr int HW = Layout<T, D>::HW;
+    constexpr int HW = 32 / (D / 4);
     const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
     BwdArgs a{};
     a.value = value;
@@ -269,6 +402,8 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const void *value, cons
     a.d = g.d;
     a.lv = g.lv;
     for (int s = 0; s < kMaxSamples; ++s) a.level_of[s] = g.level_of[s];
+    a.qblocks = (g.d.Len_q + HW - 1) / HW;
+    a.merge_mask = HW == 4 ? merge_levels(g) : 0u;
     if (det) {
         unsigned *hdr = static_cast<unsigned *>(workspace);
         unsigned long long *fixed = reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + 256);
@@ -284,12 +419,18 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const void *value, cons
         zero_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(reinterpret_cast<float4 *>(grad_value), nval / 4);
     }
     if (g.d.rows > 0) {
-        const long long warps = ((long long)g.d.rows + HW - 1) / HW;
-        const unsigned blocks = (unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
-        if (det)
-            msda_backward_kernel<T, D, true><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
-        else
-            msda_backward_kernel<T, D, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+        const long long tasks = (long long)g.d.N * a.qblocks * g.d.M;
+        const unsigned blocks = (unsigned)((tasks + kWarpsPerBlock - 1) / kWarpsPerBlock);
+        const bool merge = a.merge_mask != 0;
+        if constexpr (HW == 4) {
+            if (det && merge) msda_backward_kernel<T, D, true, true><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+            else if (det) msda_backward_kernel<T, D, true, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+            else if (merge) msda_backward_kernel<T, D, false, true><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+            else msda_backward_kernel<T, D, false, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+        } else {
+            if (det) msda_backward_kernel<T, D, true, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+            else msda_backward_kernel<T, D, false, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+        }
     }
     if (det && nval > 0)
         fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(a.fixed, a.bound_bits, g.d.rows, grad_value,

@@ -193,6 +193,90 @@ __device__ __forceinline__ Corners make_corners(float x0f, float fx, float y0f, 
     return c;
 }
 
+// ---- 16-byte corner records -------------------------------------------------
+// One sample's four corners in 16 bytes, written once per sample and read by
+// every lane of its row:
+//   .x  value row (pixel index, < 2^28) of corner 00 clamped into the map, with
+//       four validity bits above it: bit 28 column x0 inside, 29 column x0+1,
+//       30 row y0, 31 row y0+1;
+//   .y  fx,  .z  fy  (fractions of the pixel coordinate);
+//   .w  the sample's attention weight.
+// A corner is inside the map when its column and its row are.  Corners 10/01/11
+// step from the clamped corner 00 by one column / one row only when both
+// columns / both rows are inside; otherwise the step is 0, which keeps every
+// address inside the map and, since then one of the two neighbours has weight
+// 0, leaves the inside neighbour at its true address.
+constexpr uint32_t kPixMask = 0x0fffffffu;
+
+__device__ __forceinline__ uint4 pack_record(float x0f, float fx, float y0f, float fy, float A, int W, int H,
+                                             float Wf, float Hf, int start) {
+    // clamp far-away samples so the integer arithmetic cannot overflow
+    const int x0 = (int)fminf(fmaxf(x0f, -2.f), Wf + 1.f);
+    const int y0 = (int)fminf(fmaxf(y0f, -2.f), Hf + 1.f);
+    const uint32_t fl = ((unsigned)x0 < (unsigned)W ? 1u : 0u) | ((unsigned)(x0 + 1) < (unsigned)W ? 2u : 0u) |
+                        ((unsigned)y0 < (unsigned)H ? 4u : 0u) | ((unsigned)(y0 + 1) < (unsigned)H ? 8u : 0u);
+    const int cx = min(max(x0, 0), W - 1), cy = min(max(y0, 0), H - 1);
+    const uint32_t p = (uint32_t)(start + cy * W + cx);
+    return make_uint4(p | (fl << 28), __float_as_uint(fx), __float_as_uint(fy), __float_as_uint(A));
+}
+
+struct Unpacked {
+    uint32_t pix[4];    // value row of corners 00, 10, 01, 11 (always inside the map)
+    float w[4];         // bilinear weights, 0 for corners outside the map
+    bool in[4];         // corner inside the map
+    float fx, fy, A;
+};
+
+// W: width of the sample's level (pixels per row of the map)
+__device__ __forceinline__ Unpacked unpack_record(uint4 rc, int W) {
+    Unpacked u;
+    const uint32_t fl = rc.x >> 28;
+    const uint32_t p = rc.x & kPixMask;
+    const uint32_t dx = ((fl & 3u) == 3u) ? 1u : 0u;
+    const uint32_t dy = ((fl & 12u) == 12u) ? (uint32_t)W : 0u;
+    u.pix[0] = p; u.pix[1] = p + dx; u.pix[2] = p + dy; u.pix[3] = p + dy + dx;
+    u.fx = __uint_as_float(rc.y); u.fy = __uint_as_float(rc.z); u.A = __uint_as_float(rc.w);
+    const float wx0 = (fl & 1u) ? 1.f - u.fx : 0.f, wx1 = (fl & 2u) ? u.fx : 0.f;
+    const float wy0 = (fl & 4u) ? 1.f - u.fy : 0.f, wy1 = (fl & 8u) ? u.fy : 0.f;
+    u.w[0] = wx0 * wy0; u.w[1] = wx1 * wy0; u.w[2] = wx0 * wy1; u.w[3] = wx1 * wy1;
+    u.in[0] = (fl & 5u) == 5u; u.in[1] = (fl & 6u) == 6u; u.in[2] = (fl & 9u) == 9u; u.in[3] = (fl & 10u) == 10u;
+    return u;
+}
+
+// ---- 4-channel lane vectors (any storage type) ------------------------------
+template <typename T>
+__device__ __forceinline__ float4 load4_value(const T *p, uint64_t pol) {
+    uint32_t a, b, c, d;
+    if constexpr (sizeof(T) == 4) {
+        asm("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+            : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "l"(p), "l"(pol));
+        return make_float4(__uint_as_float(a), __uint_as_float(b), __uint_as_float(c), __uint_as_float(d));
+    } else {
+        asm("ld.global.nc.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;" : "=r"(a), "=r"(b) : "l"(p), "l"(pol));
+        return make_float4(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u), __uint_as_float(b << 16),
+                           __uint_as_float(b & 0xffff0000u));
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float4 load4_stream(const T *p) {
+    if constexpr (sizeof(T) == 4) {
+        return __ldcs(reinterpret_cast<const float4 *>(p));
+    } else {
+        const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(p));
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                           __uint_as_float(u.y & 0xffff0000u));
+    }
+}
+
+// y + a * x, two packed fp32 FMAs
+__device__ __forceinline__ float4 ffma4(float a, float4 x, float4 y) {
+    const float2 aa = make_float2(a, a);
+    const float2 lo = __ffma2_rn(aa, make_float2(x.x, x.y), make_float2(y.x, y.y));
+    const float2 hi = __ffma2_rn(aa, make_float2(x.z, x.w), make_float2(y.z, y.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
 // acc[0..V) += w * v
 template <typename T, int V>
 __device__ __forceinline__ void fma_row(float (&acc)[V], float w, const Vec<T> &v) {

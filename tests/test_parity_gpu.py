@@ -139,6 +139,24 @@ def test_ragged_all_head_dims(msda, dtype, D):
     _check_backward(w, _run_backward(msda, w, p, msda.MSDA_DETERMINISTIC), ref_b)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_dense_levels_merge_path(msda, dtype):
+    """Many queries on small maps: every level carries at least 32 samples per
+    pixel, so the backward sums coinciding corners of neighbouring queries
+    before reducing into grad_value.  Ragged Len_q (not a multiple of the four
+    queries a warp owns), samples partly outside the maps, both modes."""
+    w = workloads.custom(N=2, M=3, D=32, levels=[(5, 7), (2, 3), (1, 2)], K=4, Len_q=301, dtype=dtype,
+                         refs="uniform", ref_range=(-0.05, 1.05), offset_sigma=0.2, seed=1301)
+    p = H.prepared(w)
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), dtype, f"dense {dtype} output")
+    ref_b = _oracle_backward(p)
+    _check_backward(w, _run_backward(msda, w, p), ref_b)
+    det = [_run_backward(msda, w, p, msda.MSDA_DETERMINISTIC) for _ in range(2)]
+    _check_backward(w, det[0], ref_b)
+    for a, b in zip(det[0], det[1]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), "deterministic mode is not bitwise stable"
+
+
 @pytest.mark.parametrize("L,K", [(1, 1), (1, 4), (16, 16), (5, 7)])
 def test_levels_and_points(msda, L, K):
     """Single-scale (L=1), the largest L*K (256), and a ragged L*K."""
