@@ -77,8 +77,13 @@ def algorithmic_bytes(w):
     n_smp = w.N * w.Lq * w.M * w.L * w.K
     fwd = n_val * vb + n_smp * 2 * 4 + n_smp * 4 + n_out * vb
     bwd = n_val * vb + n_smp * 2 * 4 + n_smp * 4 + n_out * vb + n_val * 4 + n_smp * 2 * 4 + n_smp * 4
-    fused = n_val * vb + w.N * w.Lq * w.L * 2 * 4 + n_smp * 2 * 4 + n_smp * 4 + n_out * vb
-    return {"fwd": fwd, "bwd": bwd, "fused_fwd": fused}
+    n_ref = w.N * w.Lq * w.L * 2
+    fused = n_val * vb + n_ref * 4 + n_smp * 2 * 4 + n_smp * 4 + n_out * vb
+    # fused backward: value, ref, offsets, logits, grad_output in; grad_value,
+    # grad_ref, grad_offsets, grad_logits out
+    fused_bwd = (n_val * vb + n_ref * 4 + n_smp * 3 * 4 + n_out * vb
+                 + n_val * 4 + n_ref * 4 + n_smp * 3 * 4)
+    return {"fwd": fwd, "bwd": bwd, "fused_fwd": fused, "fused_bwd": fused_bwd}
 
 
 def kernel_source_hash():
@@ -200,6 +205,15 @@ def run_ours(args):
     def fused():
         msda.msda_forward_fused(value, sh, starts, ref_d, off_d, logit_d, output=out)
 
+    gref = torch.empty_like(ref_d)
+    goff = torch.empty_like(off_d)
+    glog = torch.empty_like(logit_d)
+
+    def fused_bwd(flags=0):
+        msda.msda_backward_fused(value, sh, starts, ref_d, off_d, logit_d, gout, grad_value=gv,
+                                 grad_reference_points=gref, grad_sampling_offsets=goff, grad_attention_logits=glog,
+                                 flags=flags)
+
     def step():
         fwd()
         bwd()
@@ -254,6 +268,8 @@ def run_ours(args):
     fused_ms = statistics.mean(timed(fused, reps))
     bwd_ms = statistics.mean(timed(lambda: bwd(msda.MSDA_ACCUMULATE_GRAD_VALUE), reps, pre=lambda: gv.zero_()))
     det_ms = statistics.mean(timed(lambda: bwd(msda.MSDA_DETERMINISTIC), max(5, reps // 4)))
+    fused_bwd_ms = statistics.mean(timed(lambda: fused_bwd(msda.MSDA_ACCUMULATE_GRAD_VALUE), reps,
+                                         pre=lambda: gv.zero_()))
     peak, peak_src = measured_peak()
     kern = {"fwd": ("msda_forward_kernel", fwd_ms), "bwd": ("msda_backward_kernel", bwd_ms)}
     dom = max(kern, key=lambda k: kern[k][1])
@@ -309,6 +325,8 @@ def run_ours(args):
                 "deterministic_ms": det_ms},
         "fused_fwd": {"ms": fused_ms, "points_per_s": pts / (fused_ms / 1e3),
                       "gbs": ab["fused_fwd"] / (fused_ms / 1e3) / 1e9},
+        "fused_bwd": {"ms": fused_bwd_ms, "points_per_s": pts / (fused_bwd_ms / 1e3),
+                      "gbs": ab["fused_bwd"] / (fused_bwd_ms / 1e3) / 1e9},
         "fwd_bwd_gbs": (ab["fwd"] + ab["bwd"]) / (total_s / args.steps) / 1e9,
         "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,

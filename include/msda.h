@@ -141,7 +141,7 @@ MSDA_API msda_status msda_forward_fused(const msda_problem *problem, const void 
                                const float *attention_logits, void *output, void *stream);
 
 /*
- * Bytes of device workspace msda_backward needs for `flags` (0 unless
+ * Bytes of device workspace msda_backward and msda_backward_fused need for `flags` (0 unless
  * MSDA_DETERMINISTIC is set).  Host-only, launches nothing.
  */
 MSDA_API size_t msda_backward_workspace_size(const msda_problem *problem, unsigned flags);
@@ -178,6 +178,40 @@ MSDA_API msda_status msda_backward(const msda_problem *problem, const void *valu
                           const void *grad_output, float *grad_value,
                           float *grad_sampling_locations, float *grad_attention_weights,
                           unsigned flags, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * msda_backward_fused -- the gradient of msda_forward_fused: through the
+ * sampling of msda_backward, then the location step loc = ref + off / (W_l, H_l)
+ * ("可变形 DETR：加速收敛的稀疏注意力检测器" §6) and the softmax over the L*K
+ * logits of one (query, head) ("可变形注意力…" §3.2 module):
+ *   grad_sampling_offsets[s] = A_s * d/d(px, py)          (pixels of level l)
+ *   grad_reference_points[n][q][l] = sum over heads m and points k of the
+ *                              location gradient A_s * (W_l, H_l) * d/d(px, py)
+ *   grad_attention_logits[s] = A_s * (g_s - sum_t A_t g_t),  g_s = <grad_output, sample_s>
+ *   grad_value              as msda_backward, with A = softmax(logits)
+ * The location and the softmax are recomputed from the raw inputs with the
+ * arithmetic of msda_forward_fused, so the samples are the ones that call took.
+ *
+ *   reference_points       in   [N][Len_q][L][2] f32
+ *   sampling_offsets       in   [N][Len_q][M][L][K][2] f32, pixels of level l
+ *   attention_logits       in   [N][Len_q][M][L*K] f32
+ *   grad_output            in   [N][Len_q][M*D], dtype
+ *   grad_value             out  [N][Len_in][M][D] f32; zeroed first unless
+ *                               MSDA_ACCUMULATE_GRAD_VALUE
+ *   grad_reference_points  out  [N][Len_q][L][2] f32, overwritten
+ *   grad_sampling_offsets  out  [N][Len_q][M][L][K][2] f32, overwritten
+ *   grad_attention_logits  out  [N][Len_q][M][L*K] f32, overwritten
+ *   flags, workspace       as msda_backward (same workspace size)
+ * Every output except grad_value is bitwise reproducible in both modes;
+ * grad_value is under MSDA_DETERMINISTIC.
+ */
+MSDA_API msda_status msda_backward_fused(const msda_problem *problem, const void *value,
+                                         const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                         const float *reference_points, const float *sampling_offsets,
+                                         const float *attention_logits, const void *grad_output, float *grad_value,
+                                         float *grad_reference_points, float *grad_sampling_offsets,
+                                         float *grad_attention_logits, unsigned flags, void *workspace,
+                                         size_t workspace_bytes, void *stream);
 
 /*
  * msda_backward_noalloc -- msda_backward in MSDA_DETERMINISTIC mode without a

@@ -2,13 +2,14 @@
 
 The computation runs in libmsda.so (hand-written CUDA for sm_103a, C ABI in
 include/msda.h); this package is its Python binding.  See _capi for the call
-signatures: msda_forward, msda_forward_fused, msda_backward.
+signatures: msda_forward, msda_forward_fused, msda_backward,
+msda_backward_fused.
 """
 from ._capi import (EXPORTED, LIBRARY, MSDA_ACCUMULATE_GRAD_VALUE, MSDA_BF16, MSDA_DETERMINISTIC, MSDA_F32,
-                    MSDAError, lib, msda_backward, msda_backward_noalloc, msda_backward_workspace_size, msda_forward, msda_forward_fused,
-                    msda_problem)
+                    MSDAError, lib, msda_backward, msda_backward_fused, msda_backward_noalloc,
+                    msda_backward_workspace_size, msda_forward, msda_forward_fused, msda_problem)
 
-__all__ = ["msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_workspace_size",
-           "msda_backward_noalloc", "MSDAError",
+__all__ = ["msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_fused",
+           "msda_backward_workspace_size", "msda_backward_noalloc", "MSDAError",
            "MSDA_DETERMINISTIC", "MSDA_ACCUMULATE_GRAD_VALUE", "MSDA_F32", "MSDA_BF16", "LIBRARY", "EXPORTED",
            "lib", "msda_problem"]

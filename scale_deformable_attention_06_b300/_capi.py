@@ -20,8 +20,9 @@ MSDA_BF16 = 1
 MSDA_DETERMINISTIC = 1
 MSDA_ACCUMULATE_GRAD_VALUE = 2
 
-EXPORTED = ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_workspace_size",
-            "msda_backward_noalloc", "msda_status_string", "msda_last_error", "msda_version")
+EXPORTED = ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_fused",
+            "msda_backward_workspace_size", "msda_backward_noalloc", "msda_status_string", "msda_last_error",
+            "msda_version")
 
 
 class MSDAError(RuntimeError):
@@ -46,11 +47,13 @@ def _load():
     lib.msda_forward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, vp]
     lib.msda_forward_fused.argtypes = [pp, vp, i64p, i64p, fp, fp, fp, vp, vp]
     lib.msda_backward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, fp, fp, fp, ctypes.c_uint, vp, ctypes.c_size_t, vp]
+    lib.msda_backward_fused.argtypes = [pp, vp, i64p, i64p, fp, fp, fp, vp, fp, fp, fp, fp, ctypes.c_uint, vp,
+                                        ctypes.c_size_t, vp]
     lib.msda_backward_noalloc.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, fp, fp, fp, ctypes.c_uint, vp]
     lib.msda_backward_noalloc.restype = ctypes.c_int
     lib.msda_backward_workspace_size.argtypes = [pp, ctypes.c_uint]
     lib.msda_backward_workspace_size.restype = ctypes.c_size_t
-    for f in ("msda_forward", "msda_forward_fused", "msda_backward"):
+    for f in ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_fused"):
         getattr(lib, f).restype = ctypes.c_int
     lib.msda_status_string.argtypes = [ctypes.c_int]
     lib.msda_status_string.restype = ctypes.c_char_p
@@ -206,6 +209,53 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, 
                               _dev(grad_attention_weights, "grad_attention_weights", torch.float32),
                               flags, ws_ptr, ws_bytes, _stream(stream, dev)))
     return grad_value, grad_sampling_locations, grad_attention_weights
+
+
+def msda_backward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
+                        attention_logits, grad_output, grad_value=None, grad_reference_points=None,
+                        grad_sampling_offsets=None, grad_attention_logits=None, flags=0, workspace=None,
+                        stream=None):
+    """Gradient of msda_forward_fused.  Returns (grad_value f32 [N,Len_in,M,D],
+    grad_reference_points [N,Len_q,L,2], grad_sampling_offsets [N,Len_q,M,L,K,2],
+    grad_attention_logits shaped like attention_logits)."""
+    lv = _HostLevels(spatial_shapes, level_start_index)
+    N, S, M, D = value.shape
+    if sampling_offsets.dim() != 6 or sampling_offsets.shape[-1] != 2:
+        raise ValueError("sampling_offsets must be [N, Len_q, M, L, K, 2]")
+    Lq, L, K = sampling_offsets.shape[1], sampling_offsets.shape[3], sampling_offsets.shape[4]
+    if tuple(reference_points.shape) != (N, Lq, L, 2):
+        raise ValueError("reference_points must be [N, Len_q, L, 2]")
+    if attention_logits.numel() != N * Lq * M * L * K or tuple(grad_output.shape) != (N, Lq, M * D):
+        raise ValueError("attention_logits / grad_output shapes disagree with value")
+    if grad_output.dtype != value.dtype:
+        raise TypeError("grad_output must have the dtype of value")
+    if L != lv.L:
+        raise ValueError("n_levels of sampling_offsets and spatial_shapes disagree")
+    dev = value.device
+    if grad_value is None:
+        grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)
+    if grad_reference_points is None:
+        grad_reference_points = torch.empty_like(reference_points)
+    if grad_sampling_offsets is None:
+        grad_sampling_offsets = torch.empty_like(sampling_offsets)
+    if grad_attention_logits is None:
+        grad_attention_logits = torch.empty_like(attention_logits)
+    prob = problem(value, Lq, L, K)
+    need = int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.msda_backward_fused(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
+                                    _dev(reference_points, "reference_points", torch.float32),
+                                    _dev(sampling_offsets, "sampling_offsets", torch.float32),
+                                    _dev(attention_logits, "attention_logits", torch.float32),
+                                    _dev(grad_output, "grad_output"), _dev(grad_value, "grad_value", torch.float32),
+                                    _dev(grad_reference_points, "grad_reference_points", torch.float32),
+                                    _dev(grad_sampling_offsets, "grad_sampling_offsets", torch.float32),
+                                    _dev(grad_attention_logits, "grad_attention_logits", torch.float32),
+                                    flags, ws_ptr, ws_bytes, _stream(stream, dev)))
+    return grad_value, grad_reference_points, grad_sampling_offsets, grad_attention_logits
 
 
 def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,

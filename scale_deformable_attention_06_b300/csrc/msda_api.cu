@@ -209,6 +209,46 @@ msda_status msda_backward(const msda_problem *problem, const void *value, const 
                        "msda_backward launch");
 }
 
+msda_status msda_backward_fused(const msda_problem *problem, const void *value, const int64_t *spatial_shapes,
+                                const int64_t *level_start_index, const float *reference_points,
+                                const float *sampling_offsets, const float *attention_logits, const void *grad_output,
+                                float *grad_value, float *grad_reference_points, float *grad_sampling_offsets,
+                                float *grad_attention_logits, unsigned flags, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    g_last_error[0] = 0;
+    msda::LaunchGeometry g;
+    msda_status st = make_geometry(problem, spatial_shapes, level_start_index, g);
+    if (st != MSDA_OK) return st;
+    if (flags & ~(MSDA_DETERMINISTIC | MSDA_ACCUMULATE_GRAD_VALUE))
+        return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const bool det = (flags & MSDA_DETERMINISTIC) != 0, acc = (flags & MSDA_ACCUMULATE_GRAD_VALUE) != 0;
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * problem->head_dim;
+    if (nval > 0 && !grad_value) return fail(MSDA_ERR_INVALID_ARG, "grad_value is NULL");
+    if (grad_value && !aligned(grad_value, 16)) return fail(MSDA_ERR_INVALID_ARG, "grad_value not 16-byte aligned");
+    if (g.d.rows > 0) {
+        if (!value || !reference_points || !sampling_offsets || !attention_logits || !grad_output ||
+            !grad_reference_points || !grad_sampling_offsets || !grad_attention_logits)
+            return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+        if (!aligned(value, 16) || !aligned(grad_output, 16) || !aligned(reference_points, 8) ||
+            !aligned(sampling_offsets, 8) || !aligned(grad_reference_points, 8) || !aligned(grad_sampling_offsets, 8) ||
+            !aligned(attention_logits, 4) || !aligned(grad_attention_logits, 4))
+            return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor");
+    }
+    const size_t need = msda::backward_workspace_bytes(g, problem->head_dim, det);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need)
+            return fail(MSDA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
+        if (!aligned(workspace, 256)) return fail(MSDA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    }
+    if (nval == 0 && g.d.rows == 0) return MSDA_OK;
+    if (g.d.rows == 0 && acc) return MSDA_OK;
+    return cuda_status(msda::launch_backward_fused(g, problem->dtype, problem->head_dim, value, reference_points,
+                                                   sampling_offsets, attention_logits, grad_output, grad_value,
+                                                   grad_reference_points, grad_sampling_offsets, grad_attention_logits,
+                                                   det, acc, workspace, static_cast<cudaStream_t>(stream)),
+                       "msda_backward_fused launch");
+}
+
 const char *msda_status_string(msda_status s) {
     switch (s) {
         case MSDA_OK: return "MSDA_OK";

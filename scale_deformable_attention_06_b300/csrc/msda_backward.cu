@@ -47,6 +47,9 @@ struct BwdArgs {
     float *grad_value;
     float *grad_loc;
     float *grad_attn;
+    const float *ref;              // fused: reference points [N][Len_q][L][2]
+    const float *off;              // fused: sampling offsets (pixels of the level)
+    const float *logits;           // fused: attention logits [N][Len_q][M][L*K]
     unsigned long long *fixed;     // deterministic: [N*Len_in*M*D] accumulators
     const unsigned *bound_bits;    // deterministic: bits of max row bound (a float)
     Dims d;
@@ -123,23 +126,26 @@ template <int HW, int RC, bool MERGE>
 struct BwdWarpSmem {
     uint4 rec[HW][RC + 1];             // corner records (padded rows)
     float4 res[HW][RC + 1];            // per sample: grad_attn, A*d/dpx, A*d/dpy
+    float2 stat[HW];                   // fused: softmax max and 1 / sum of each query
 };
 
 template <int HW, int RC>
 struct BwdWarpSmem<HW, RC, true> {
     uint4 rec[HW][RC + 1];
     float4 res[HW][RC + 1];
+    float2 stat[HW];
     unsigned key[kMergeSlots];         // corner pixel of the slot, kEmptyKey if free
     float4 alpha[kMergeSlots];         // per query of the warp: summed A * w_c (HW == 4)
     unsigned short list[kMergeSlots];  // occupied slots in order of first use
     int count;
 };
 
-template <typename T, int D, bool DET, bool MERGE>
+template <typename T, int D, bool DET, bool MERGE, bool FUSED>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
 msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int R = D / 4, HW = 32 / R;
     constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
+    static_assert(HW * RC == 64, "phase 1 and 3 give every lane two (query, sample) slots");
     static_assert(!MERGE || HW == 4, "the merge table holds four queries per slot");
     using WS = BwdWarpSmem<HW, RC, MERGE>;
     __shared__ WS smem[kWarpsPerBlock];
@@ -181,6 +187,24 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
         if (lane == 0) sm.count = 0;
         __syncwarp();
     }
+    if constexpr (FUSED) {
+        // softmax statistics of the warp's queries (the same arithmetic as the
+        // fused forward, so A is the same value there and here)
+        for (int hh = 0; hh < HW; ++hh) {
+            const int qq = qb * HW + hh;
+            if (qq >= dm.Len_q) break;                  // warp-uniform
+            const float *lg = a.logits + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P;
+            float mx = -INFINITY;
+            for (int s = lane; s < P; s += 32) mx = fmaxf(mx, __ldg(lg + s));
+            mx = warp_max(mx);
+            float sum = 0.f;
+            for (int s = lane; s < P; s += 32) sum += expf(__ldg(lg + s) - mx);
+            sum = warp_sum(sum);
+            if (lane == 0) sm.stat[hh] = make_float2(mx, 1.f / sum);
+        }
+        __syncwarp();
+    }
+    float dotp[2] = {0.f, 0.f};        // fused: this lane's part of sum_s A_s * grad_attn_s, per slot
 
     for (int r0 = 0; r0 < P; r0 += RC) {
         const int RJ = min(RC, P - r0);
@@ -194,12 +218,21 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 const int l = a.level_of[r0 + j];
                 const float Wf = a.lv.Wf[l], Hf = a.lv.Hf[l];
                 const size_t si = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + r0 + j;
-                const float2 lc = load_stream2(a.loc + 2 * si);
-                float x0, fx, y0, fy;
-                pixel_coord(lc.x, Wf, x0, fx);
-                pixel_coord(lc.y, Hf, y0, fy);
-                rc = pack_record(x0, fx, y0, fy, load_stream1(a.attn + si), a.lv.W[l], a.lv.H[l], Wf, Hf,
-                                 a.lv.start[l]);
+                float x0, fx, y0, fy, A;
+                if constexpr (FUSED) {
+                    const float2 rf = __ldg(reinterpret_cast<const float2 *>(a.ref) + (size_t)(n * dm.Len_q + qq) * dm.L + l);
+                    const float2 of = load_stream2(a.off + 2 * si);
+                    pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
+                    pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
+                    const float2 st = sm.stat[hh];
+                    A = expf(load_stream1(a.logits + si) - st.x) * st.y;
+                } else {
+                    const float2 lc = load_stream2(a.loc + 2 * si);
+                    pixel_coord(lc.x, Wf, x0, fx);
+                    pixel_coord(lc.y, Hf, y0, fy);
+                    A = load_stream1(a.attn + si);
+                }
+                rc = pack_record(x0, fx, y0, fy, A, a.lv.W[l], a.lv.H[l], Wf, Hf, a.lv.start[l]);
             }
             sm.rec[hh][j] = rc;
         }
@@ -308,18 +341,76 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
             s0 += J;
         }
         // ---- phase 3: per-sample gradients of the chunk
-        for (int i = lane; i < HW * RC; i += 32) {
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int i = lane + 32 * it;
             const int j = i % RC, hh = i / RC;
             const int qq = qb * HW + hh;
             if (j < RJ && qq < dm.Len_q) {
                 const int l = a.level_of[r0 + j];
                 const size_t si = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + r0 + j;
                 const float4 res = sm.res[hh][j];
-                __stcs(a.grad_attn + si, res.x);
-                __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si, make_float2(res.y * a.lv.Wf[l], res.z * a.lv.Hf[l]));
+                if constexpr (FUSED) {
+                    // offsets are pixels of the level: d loc / d off = 1 / (W, H)
+                    __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si, make_float2(res.y, res.z));
+                    a.grad_attn[si] = res.x;           // grad of A; read back below by this lane
+                    dotp[it] = __fmaf_rn(__uint_as_float(sm.rec[hh][j].w), res.x, dotp[it]);
+                } else {
+                    __stcs(a.grad_attn + si, res.x);
+                    __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si,
+                           make_float2(res.y * a.lv.Wf[l], res.z * a.lv.Hf[l]));
+                }
             }
         }
         __syncwarp();
+    }
+    if constexpr (FUSED) {
+        // softmax backward: grad_logit_s = A_s * (grad_A_s - sum_t A_t grad_A_t).
+        // Slot it of lane i covers query (lane + 32 it) / RC; the lanes of one
+        // query form an aligned group of min(RC, 32), summed in a fixed order.
+        constexpr int G = RC < 32 ? RC : 32;
+        float tot[2];
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            float v = dotp[it];
+#pragma unroll
+            for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            tot[it] = v;
+        }
+        for (int r0 = 0; r0 < P; r0 += RC) {
+            const int RJ = min(RC, P - r0);
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int i = lane + 32 * it;
+                const int j = i % RC, hh = i / RC;
+                const int qq = qb * HW + hh;
+                if (j < RJ && qq < dm.Len_q) {
+                    const size_t si = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + r0 + j;
+                    const float2 st = sm.stat[hh];
+                    const float A = expf(__ldg(a.logits + si) - st.x) * st.y;
+                    __stcs(a.grad_attn + si, A * (a.grad_attn[si] - tot[it]));
+                }
+            }
+        }
+    }
+}
+
+// grad_reference_points[n][q][l] = sum over heads and points of the location
+// gradient = (W_l, H_l) * sum of the offset gradients (loc = ref + off / (W, H)).
+// One thread per (n, q, l), summed in a fixed order.
+__global__ void ref_grad_kernel(const float *grad_off, float *grad_ref, int nql, int M, int L, int K, LevelTable lv) {
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nql; t += gridDim.x * blockDim.x) {
+        const int l = t % L, nq = t / L;
+        float sx = 0.f, sy = 0.f;
+        for (int m = 0; m < M; ++m) {
+            const float2 *g = reinterpret_cast<const float2 *>(grad_off) + (((size_t)nq * M + m) * L + l) * K;
+            for (int k = 0; k < K; ++k) {
+                const float2 v = g[k];
+                sx += v.x;
+                sy += v.y;
+            }
+        }
+        reinterpret_cast<float2 *>(grad_ref)[t] = make_float2(sx * lv.Wf[l], sy * lv.Hf[l]);
     }
 }
 
@@ -341,8 +432,11 @@ template <typename T, int D>
 __global__ void row_bound_kernel(const float *attn, const T *grad_out, int rows, int P, unsigned *bound_bits) {
     float best = 0.f;
     for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
-        float sa = 0.f;
-        for (int s = 0; s < P; ++s) sa += fabsf(attn[(size_t)r * P + s]);
+        float sa = 1.001f;             // softmax weights (fused call): they sum to 1
+        if (attn) {
+            sa = 0.f;
+            for (int s = 0; s < P; ++s) sa += fabsf(attn[(size_t)r * P + s]);
+        }
         float gm = 0.f;
         const T *g = grad_out + (size_t)r * D;
         for (int d = 0; d < D; ++d) gm = fmaxf(gm, fabsf((float)g[d]));
@@ -385,20 +479,49 @@ static unsigned merge_levels(const LaunchGeometry &g) {
     return mask;
 }
 
-template <typename T, int D>
-static cudaError_t launch_bwd_t(const LaunchGeometry &g, const void *value, const float *loc, const float *attn,
-                                const void *grad_out, float *grad_value, float *grad_loc, float *grad_attn,
-                                bool det, bool accumulate, void *workspace, cudaStream_t stream) {
+// Inputs and outputs of one backward launch.  Unfused: loc, attn -> grad_loc,
+// grad_attn.  Fused: ref, off, logits -> grad_off (in grad_loc), grad_logits
+// (in grad_attn), grad_ref.
+struct BwdIO {
+    const void *value;
+    const float *loc, *attn;              // unfused
+    const float *ref, *off, *logits;      // fused
+    const void *grad_out;
+    float *grad_value, *grad_loc, *grad_attn, *grad_ref;
+};
+
+template <typename T, int D, bool FUSED>
+static void launch_bwd_kernel(const BwdArgs &a, bool det, unsigned blocks, cudaStream_t stream) {
+    constexpr int HW = 32 / (D / 4);
+    constexpr int B = kWarpsPerBlock * 32;
+    const bool merge = a.merge_mask != 0;
+    if constexpr (HW == 4) {
+        if (det && merge) msda_backward_kernel<T, D, true, true, FUSED><<<blocks, B, 0, stream>>>(a);
+        else if (det) msda_backward_kernel<T, D, true, false, FUSED><<<blocks, B, 0, stream>>>(a);
+        else if (merge) msda_backward_kernel<T, D, false, true, FUSED><<<blocks, B, 0, stream>>>(a);
+        else msda_backward_kernel<T, D, false, false, FUSED><<<blocks, B, 0, stream>>>(a);
+    } else {
+        if (det) msda_backward_kernel<T, D, true, false, FUSED><<<blocks, B, 0, stream>>>(a);
+        else msda_backward_kernel<T, D, false, false, FUSED><<<blocks, B, 0, stream>>>(a);
+    }
+}
+
+template <typename T, int D, bool FUSED>
+static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool det, bool accumulate, void *workspace,
+                                cudaStream_t stream) {
     constexpr int HW = 32 / (D / 4);
     const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
     BwdArgs a{};
-    a.value = value;
-    a.loc = loc;
-    a.attn = attn;
-    a.grad_out = grad_out;
-    a.grad_value = grad_value;
-    a.grad_loc = grad_loc;
-    a.grad_attn = grad_attn;
+    a.value = io.value;
+    a.loc = io.loc;
+    a.attn = io.attn;
+    a.ref = io.ref;
+    a.off = io.off;
+    a.logits = io.logits;
+    a.grad_out = io.grad_out;
+    a.grad_value = io.grad_value;
+    a.grad_loc = io.grad_loc;
+    a.grad_attn = io.grad_attn;
     a.d = g.d;
     a.lv = g.lv;
     for (int s = 0; s < kMaxSamples; ++s) a.level_of[s] = g.level_of[s];
@@ -414,53 +537,76 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const void *value, cons
             static_cast<ulonglong2 *>(workspace), (nval * 8 + 256) / 16);
         if (g.d.rows > 0)
             row_bound_kernel<T, D><<<grid_for(g.d.rows, 256), 256, 0, stream>>>(
-                attn, static_cast<const T *>(grad_out), g.d.rows, g.d.P, hdr);
+                FUSED ? nullptr : io.attn, static_cast<const T *>(io.grad_out), g.d.rows, g.d.P, hdr);
     } else if (!accumulate && nval > 0) {
-        zero_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(reinterpret_cast<float4 *>(grad_value), nval / 4);
+        zero_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(reinterpret_cast<float4 *>(io.grad_value),
+                                                                      nval / 4);
     }
     if (g.d.rows > 0) {
         const long long tasks = (long long)g.d.N * a.qblocks * g.d.M;
-        const unsigned blocks = (unsigned)((tasks + kWarpsPerBlock - 1) / kWarpsPerBlock);
-        const bool merge = a.merge_mask != 0;
-        if constexpr (HW == 4) {
-            if (det && merge) msda_backward_kernel<T, D, true, true><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
-            else if (det) msda_backward_kernel<T, D, true, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
-            else if (merge) msda_backward_kernel<T, D, false, true><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
-            else msda_backward_kernel<T, D, false, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
-        } else {
-            if (det) msda_backward_kernel<T, D, true, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
-            else msda_backward_kernel<T, D, false, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+        launch_bwd_kernel<T, D, FUSED>(a, det, (unsigned)((tasks + kWarpsPerBlock - 1) / kWarpsPerBlock), stream);
+        if (FUSED) {
+            const int nql = g.d.N * g.d.Len_q * g.d.L;
+            ref_grad_kernel<<<grid_for(nql, 256), 256, 0, stream>>>(io.grad_loc, io.grad_ref, nql, g.d.M, g.d.L,
+                                                                   g.d.K, g.lv);
         }
     }
     if (det && nval > 0)
-        fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(a.fixed, a.bound_bits, g.d.rows, grad_value,
+        fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(a.fixed, a.bound_bits, g.d.rows, io.grad_value,
                                                                       nval, accumulate ? 1 : 0);
     return cudaGetLastError();
+}
+
+template <bool FUSED>
+static cudaError_t dispatch_bwd(const LaunchGeometry &g, int dtype, int D, const BwdIO &io, bool det, bool accumulate,
+                                void *workspace, cudaStream_t stream) {
+    if (dtype == 0) {
+        switch (D) {
+            case 8: return launch_bwd_t<float, 8, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 16: return launch_bwd_t<float, 16, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 32: return launch_bwd_t<float, 32, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 64: return launch_bwd_t<float, 64, FUSED>(g, io, det, accumulate, workspace, stream);
+        }
+    } else {
+        switch (D) {
+            case 8: return launch_bwd_t<__nv_bfloat16, 8, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 16: return launch_bwd_t<__nv_bfloat16, 16, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 32: return launch_bwd_t<__nv_bfloat16, 32, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 64: return launch_bwd_t<__nv_bfloat16, 64, FUSED>(g, io, det, accumulate, workspace, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_backward(const LaunchGeometry &g, int dtype, int D, const void *value, const float *loc,
                             const float *attn, const void *grad_out, float *grad_value, float *grad_loc,
                             float *grad_attn, bool det, bool accumulate, void *workspace, cudaStream_t stream) {
-#define MSDA_BWD(T, DD) \
-    return launch_bwd_t<T, DD>(g, value, loc, attn, grad_out, grad_value, grad_loc, grad_attn, det, accumulate, \
-                               workspace, stream)
-    if (dtype == 0) {
-        switch (D) {
-            case 8: MSDA_BWD(float, 8);
-            case 16: MSDA_BWD(float, 16);
-            case 32: MSDA_BWD(float, 32);
-            case 64: MSDA_BWD(float, 64);
-        }
-    } else {
-        switch (D) {
-            case 8: MSDA_BWD(__nv_bfloat16, 8);
-            case 16: MSDA_BWD(__nv_bfloat16, 16);
-            case 32: MSDA_BWD(__nv_bfloat16, 32);
-            case 64: MSDA_BWD(__nv_bfloat16, 64);
-        }
-    }
-#undef MSDA_BWD
-    return cudaErrorInvalidValue;
+    BwdIO io{};
+    io.value = value;
+    io.loc = loc;
+    io.attn = attn;
+    io.grad_out = grad_out;
+    io.grad_value = grad_value;
+    io.grad_loc = grad_loc;
+    io.grad_attn = grad_attn;
+    return dispatch_bwd<false>(g, dtype, D, io, det, accumulate, workspace, stream);
+}
+
+cudaError_t launch_backward_fused(const LaunchGeometry &g, int dtype, int D, const void *value, const float *ref,
+                                  const float *off, const float *logits, const void *grad_out, float *grad_value,
+                                  float *grad_ref, float *grad_off, float *grad_logits, bool det, bool accumulate,
+                                  void *workspace, cudaStream_t stream) {
+    BwdIO io{};
+    io.value = value;
+    io.ref = ref;
+    io.off = off;
+    io.logits = logits;
+    io.grad_out = grad_out;
+    io.grad_value = grad_value;
+    io.grad_loc = grad_off;
+    io.grad_attn = grad_logits;
+    io.grad_ref = grad_ref;
+    return dispatch_bwd<true>(g, dtype, D, io, det, accumulate, workspace, stream);
 }
 
 }  // namespace msda

@@ -31,4 +31,11 @@ cudaError_t launch_backward(const LaunchGeometry &g, int dtype, int D, const voi
                             float *grad_attn, bool deterministic, bool accumulate, void *workspace,
                             cudaStream_t stream);
 
+// Fused backward: gradients with respect to the raw reference points,
+// sampling offsets (pixels of their level) and attention logits.
+cudaError_t launch_backward_fused(const LaunchGeometry &g, int dtype, int D, const void *value, const float *ref,
+                                  const float *off, const float *logits, const void *grad_out, float *grad_value,
+                                  float *grad_ref, float *grad_off, float *grad_logits, bool det, bool accumulate,
+                                  void *workspace, cudaStream_t stream);
+
 }  // namespace msda

@@ -88,6 +88,9 @@ def test_host_checks_reject_before_launch(msda, kw, shapes, starts, expect):
     assert rc == expect
     rc = msda.lib().msda_backward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None, 0, None)
     assert rc == expect
+    rc = msda.lib().msda_backward_fused(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                        0, None, 0, None)
+    assert rc == expect
 
 
 def test_null_and_misaligned_pointers(msda):
@@ -102,6 +105,13 @@ def test_null_and_misaligned_pointers(msda):
     assert lib.msda_backward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, None, 0, None) == 1
     # deterministic mode without a workspace
     assert lib.msda_backward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, None, 0, None) == 4
+    # fused backward: a missing gradient output, a misaligned offset tensor, a bad flag, no workspace
+    fb = lib.msda_backward_fused
+    assert fb(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 0, None, 0, None) == 1
+    assert fb(ctypes.byref(p), FAKE, sh, st, FAKE, ctypes.c_void_p(0x10004), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+              0, None, 0, None) == 1
+    assert fb(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, None, 0, None) == 1
+    assert fb(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, None, 0, None) == 4
 
 
 def test_workspace_size(msda):

@@ -48,6 +48,25 @@ def _run_backward(msda, w, p, flags=0):
     return gv.cpu().numpy(), gl.cpu().numpy(), ga.cpu().numpy()
 
 
+def _run_backward_fused(msda, w, p, flags=0):
+    dt = H.storage_dtype(w)
+    outs = msda.msda_backward_fused(H.dev(p["value"], dt), p["spatial_shapes"], p["level_start_index"],
+                                    H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]),
+                                    H.dev(p["attention_logits"]), H.dev(p["grad_output"], dt), flags=flags)
+    return tuple(o.cpu().numpy() for o in outs)
+
+
+def _oracle_backward_fused(p):
+    return oracle.backward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
+                                 p["sampling_offsets"], p["attention_logits"], p["grad_output"])
+
+
+def _check_backward_fused(w, got, ref):
+    names = ("grad_value", "grad_reference_points", "grad_sampling_offsets", "grad_attention_logits")
+    for name, g, r in zip(names, got, ref):
+        H.assert_bwd(g.reshape(r.shape), r, "f32", f"{w.name} fused {name}")
+
+
 def _oracle_forward(p):
     return oracle.forward(p["value"], p["spatial_shapes"], p["level_start_index"], p["sampling_locations"],
                           p["attention_weights"])
@@ -243,3 +262,46 @@ def test_invalid_arguments_return_errors(msda):
     assert e.value.name == "MSDA_ERR_UNSUPPORTED"
     with pytest.raises(ValueError):
         msda.msda_forward(value.cpu(), p["spatial_shapes"], p["level_start_index"], loc, attn)
+
+
+# ----------------------------------------------------------------- fused backward (a9)
+@pytest.mark.parametrize("name", ["encoder_train", "decoder"])
+def test_fused_backward_workloads(msda, name):
+    """Gradients with respect to reference points, offsets and logits on the
+    encoder training workload (fp32) and the decoder workload (bf16 value)."""
+    w = workloads.WORKLOADS[name]
+    p = H.prepared(w)
+    ref = _oracle_backward_fused(p)
+    _check_backward_fused(w, _run_backward_fused(msda, w, p), ref)
+    det = [_run_backward_fused(msda, w, p, msda.MSDA_DETERMINISTIC) for _ in range(2)]
+    _check_backward_fused(w, det[0], ref)
+    for a, b in zip(det[0], det[1]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), "deterministic fused backward is not bitwise stable"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("D,L,K", [(8, 4, 3), (16, 1, 4), (32, 5, 7), (64, 2, 2), (32, 16, 16)])
+def test_fused_backward_shapes(msda, dtype, D, L, K):
+    """Ragged Len_q, every head_dim, L*K up to 256 (several record chunks per
+    query), samples partly outside the maps."""
+    levels = [(3 + (l % 4), 2 + (l * 3) % 7) for l in range(L)]
+    w = workloads.custom(N=2, M=3, D=D, levels=levels, K=K, Len_q=23, dtype=dtype, refs="uniform",
+                         ref_range=(-0.05, 1.05), offset_sigma=0.2, seed=500 + D + 7 * L + K)
+    p = H.prepared(w)
+    _check_backward_fused(w, _run_backward_fused(msda, w, p), _oracle_backward_fused(p))
+
+
+def test_fused_backward_dense_merge_and_accumulate(msda):
+    """Dense small maps (merge table on every level) and MSDA_ACCUMULATE_GRAD_VALUE."""
+    w = workloads.custom(N=1, M=2, D=32, levels=[(4, 6), (2, 3)], K=4, Len_q=203, refs="uniform",
+                         ref_range=(0.0, 1.0), offset_sigma=0.15, seed=808)
+    p = H.prepared(w)
+    ref = _oracle_backward_fused(p)
+    _check_backward_fused(w, _run_backward_fused(msda, w, p), ref)
+    gv0 = np.random.Generator(np.random.PCG64(9)).standard_normal(p["value"].shape).astype(np.float32)
+    for flags in (msda.MSDA_ACCUMULATE_GRAD_VALUE, msda.MSDA_ACCUMULATE_GRAD_VALUE | msda.MSDA_DETERMINISTIC):
+        gv = H.dev(gv0)
+        msda.msda_backward_fused(H.dev(p["value"]), p["spatial_shapes"], p["level_start_index"],
+                                 H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]),
+                                 H.dev(p["attention_logits"]), H.dev(p["grad_output"]), grad_value=gv, flags=flags)
+        H.assert_bwd(gv.cpu().numpy(), gv0 + ref[0], "f32", "fused accumulated grad_value")
