@@ -215,8 +215,12 @@ def run_ours(args):
                                  flags=flags)
 
     def step():
-        fwd()
-        bwd()
+        if args.step == "fused":
+            fused()
+            fused_bwd()
+        else:
+            fwd()
+            bwd()
 
     def timed(fn, iters, pre=None):
         """Sum of per-call device times (ms) with an L2 flush before each call."""
@@ -278,14 +282,20 @@ def run_ours(args):
     traffic = profiled_traffic(name)
 
     # ---- end to end from pinned host memory through the same calls
-    h_in = [t.pin_memory() for t in (value_h, loc_h, attn_h, gout_h)]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, gv, gl, ga)]
+    if args.step == "fused":
+        d_in = (value, ref_d, off_d, logit_d, gout)
+        d_out = (out, gv, gref, goff, glog)
+    else:
+        d_in = (value, loc, attn, gout)
+        d_out = (out, gv, gl, ga)
+    h_in = [t.cpu().pin_memory() for t in d_in]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in d_out]
 
     def e2e_step():
-        for h, d in zip(h_in, (value, loc, attn, gout)):
+        for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
         step()
-        for h, d in zip(h_out, (out, gv, gl, ga)):
+        for h, d in zip(h_out, d_out):
             h.copy_(d, non_blocking=True)
 
     for _ in range(2):
@@ -314,7 +324,8 @@ def run_ours(args):
         "config": {"workload": "Deformable DETR encoder fwd+bwd: N=2, M=8, D=32, L=4 levels 100x167, 50x84, "
                                "25x42, 13x21 (Len_in=22223), Len_q=Len_in, K=4, fp32"
                                if args.workload == WORKLOAD else args.workload,
-                   "step": "msda_forward + msda_backward (atomic grad_value)", "per_rank_batch": w.N,
+                   "step": ("msda_forward_fused + msda_backward_fused" if args.step == "fused" else
+                            "msda_forward + msda_backward") + " (atomic grad_value)", "per_rank_batch": w.N,
                    "sampled_points_per_step_per_rank": pts,
                    "l2": "flushed before every step (256 MB write); per-step events exclude the flush",
                    "parallelism": f"dp{world} (independent batches per rank)"},
@@ -333,7 +344,9 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": ab[dom], "launch_ms": ms},
         "e2e": {"value": aggregate(pts, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
-        "gpu_launches": 3 * args.steps,
+        # per step: forward 1; backward: grad_value zeroing + backward kernel
+        # (+ reference-point reduction in the fused step)
+        "gpu_launches": (4 if args.step == "fused" else 3) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
         "library": msda.LIBRARY,
@@ -341,6 +354,97 @@ def run_ours(args):
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- every workload
+def run_sweep(args):
+    """Per-call device times on every workload (one JSON line each): forward,
+    fused forward, backward (fp32 atomics and deterministic), fused backward,
+    with the algorithmic bytes of each call; the oracle's single-core time on a
+    bounded query sample beside them."""
+    import torch
+    import scale_deformable_attention_06_b300 as msda
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, _ = measured_peak()
+
+    def timed(fn, iters, pre=None):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for _ in range(3):
+            fn()
+        for e0, e1 in evs:
+            flush.fill_(1.0)
+            if pre is not None:
+                pre()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+    for name in ("tiny", "encoder", "decoder", "encoder_train", "large"):
+        w = workloads.WORKLOADS[name]
+        raw = workloads.draw(w)
+        sh, starts = torch.from_numpy(raw["spatial_shapes"]), raw["level_start_index"]
+        vdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        if "sampling_locations" in raw:
+            loc_h = torch.from_numpy(raw["sampling_locations"])
+            # a reference point at the first sample's location and offsets to the others, in pixels
+            ref_h = loc_h[:, :, 0, :, 0, :].clone().contiguous()
+            whf = sh[:, [1, 0]].float()
+            off_h = ((loc_h - ref_h[:, :, None, :, None, :]) * whf[None, None, None, :, None, :]).contiguous()
+        else:
+            ref_h = torch.from_numpy(raw["reference_points"])
+            off_h = torch.from_numpy(raw["sampling_offsets"])
+            wh = sh[:, [1, 0]].to(torch.float64)
+            loc_h = (ref_h.double()[:, :, None, :, None, :] + off_h.double() / wh[None, None, None, :, None, :]).float()
+        lg_h = torch.from_numpy(raw["attention_logits"])
+        attn_h = torch.softmax(lg_h.double(), -1).float().reshape(loc_h.shape[:-1]).contiguous()
+        value = torch.from_numpy(raw["value"]).to(vdt).to(dev)
+        gout = torch.from_numpy(raw["grad_output"]).to(vdt).to(dev)
+        loc, attn, ref, off, lg = (t.contiguous().to(dev) for t in (loc_h, attn_h, ref_h, off_h, lg_h))
+        out = torch.empty((w.N, w.Lq, w.M * w.D), dtype=vdt, device=dev)
+        gv = torch.empty(value.shape, dtype=torch.float32, device=dev)
+        gl, ga = torch.empty_like(loc), torch.empty_like(attn)
+        gr, go, glg = torch.empty_like(ref), torch.empty_like(off), torch.empty_like(lg)
+        acc = msda.MSDA_ACCUMULATE_GRAD_VALUE
+        reps = 20
+        t = {
+            "fwd": timed(lambda: msda.msda_forward(value, sh, starts, loc, attn, output=out), reps),
+            "fused_fwd": timed(lambda: msda.msda_forward_fused(value, sh, starts, ref, off, lg, output=out), reps),
+            "bwd": timed(lambda: msda.msda_backward(value, sh, starts, loc, attn, gout, grad_value=gv,
+                                                    grad_sampling_locations=gl, grad_attention_weights=ga,
+                                                    flags=acc), reps, pre=lambda: gv.zero_()),
+            "bwd_deterministic": timed(lambda: msda.msda_backward(value, sh, starts, loc, attn, gout, grad_value=gv,
+                                                                  grad_sampling_locations=gl,
+                                                                  grad_attention_weights=ga,
+                                                                  flags=msda.MSDA_DETERMINISTIC), 5),
+            "fused_bwd": timed(lambda: msda.msda_backward_fused(value, sh, starts, ref, off, lg, gout,
+                                                                grad_value=gv, grad_reference_points=gr,
+                                                                grad_sampling_offsets=go,
+                                                                grad_attention_logits=glg, flags=acc), reps,
+                               pre=lambda: gv.zero_()),
+        }
+        ab = algorithmic_bytes(w)
+        ab["bwd_deterministic"] = ab["bwd"]
+        calls = {}
+        for k, ms in t.items():
+            gbs = ab[k] / (ms / 1e3) / 1e9
+            calls[k] = {"us": ms * 1e3, "points_per_s": w.samples / (ms / 1e3), "gbs": gbs,
+                        "frac_of_measured_hbm_peak": gbs / peak, "algorithmic_bytes": ab[k]}
+        # oracle, single core, forward + backward on a bounded query sample of this workload
+        q = max(1, min(w.Lq, int(2.0e5 // (w.M * w.L * w.K * max(w.N, 1)))))
+        smp = _oracle_sample(w, raw, loc_h.numpy(), attn_h.numpy(), value.float().cpu().numpy(),
+                             gout.float().cpu().numpy(), 0, q)
+        t0 = time.perf_counter()
+        _oracle_step(smp)
+        el = time.perf_counter() - t0
+        pts = w.N * q * w.M * w.L * w.K
+        print(json.dumps({"sweep": True, "workload": name, "dtype": w.dtype, "samples": w.samples, "calls": calls,
+                          "oracle_fwd_bwd_points_per_s_1core": pts / el,
+                          "oracle_sample": f"{q} of {w.Lq} queries x {w.N} batches"}))
 
 
 # ----------------------------------------------------------------------------- oracle timings
@@ -415,10 +519,16 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-step", action="store_true", help="time the step only (for profiler runs)")
+    ap.add_argument("--sweep", action="store_true", help="per-call times on every workload (one JSON line each)")
+    ap.add_argument("--step", choices=["unfused", "fused"], default="unfused",
+                    help="unfused: msda_forward + msda_backward on locations and weights; fused: msda_forward_fused + "
+                         "msda_backward_fused on reference points, offsets and logits")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
