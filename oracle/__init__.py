@@ -28,10 +28,10 @@ def bind(path):
     lp = ctypes.POINTER(ctypes.c_int64)
     lib.msda_oracle_locations.argtypes = [i64] * 5 + [lp, dp, dp, dp]
     lib.msda_oracle_softmax.argtypes = [i64, i64, dp, dp]
-    lib.msda_oracle_forward.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp]
-    lib.msda_oracle_forward_fused.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp]
-    lib.msda_oracle_backward.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp]
-    lib.msda_oracle_backward_fused.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, dp, dp]
+    lib.msda_oracle_forward.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, i64]
+    lib.msda_oracle_forward_fused.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, i64]
+    lib.msda_oracle_backward.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, i64]
+    lib.msda_oracle_backward_fused.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, dp, dp, i64]
     for f in ("msda_oracle_locations", "msda_oracle_softmax", "msda_oracle_forward",
               "msda_oracle_forward_fused", "msda_oracle_backward", "msda_oracle_backward_fused"):
         getattr(lib, f).restype = ctypes.c_int
@@ -75,6 +75,11 @@ def _dims(value, shapes, loc_like):
     return N, S, M, D, Lq, L, K
 
 
+# option bits of the forward and backward functions (msda_oracle.c header)
+PER_LEVEL_SOFTMAX = 1   # the fused calls normalise each level's n_points logits separately
+ALIGN_CORNERS = 2       # px = loc * (W - 1) instead of loc * W - 0.5
+
+
 def locations(spatial_shapes, reference_points, sampling_offsets):
     """a1: loc = ref + off / (W_l, H_l); offsets in pixels of their level."""
     lib = _load()
@@ -99,7 +104,7 @@ def softmax(logits):
     return out
 
 
-def forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights):
+def forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, options=0):
     """a3-a5.  Returns output [N, Len_q, M*D] in float64."""
     lib = _load()
     v, vp = _d(value)
@@ -109,12 +114,12 @@ def forward(value, spatial_shapes, level_start_index, sampling_locations, attent
     a, ap = _d(attention_weights)
     N, S, M, D, Lq, L, K = _dims(v, sh, loc)
     out = np.zeros((N, Lq, M * D))
-    _check(lib.msda_oracle_forward(N, S, M, D, Lq, L, K, vp, shp, stp, locp, ap, _d(out)[1]), "forward")
+    _check(lib.msda_oracle_forward(N, S, M, D, Lq, L, K, vp, shp, stp, locp, ap, _d(out)[1], options), "forward")
     return out
 
 
 def forward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
-                  attention_logits):
+                  attention_logits, options=0):
     """a1-a5.  attention_logits is [N, Len_q, M, L*K] (or [N,Lq,M,L,K])."""
     lib = _load()
     v, vp = _d(value)
@@ -125,12 +130,13 @@ def forward_fused(value, spatial_shapes, level_start_index, reference_points, sa
     lg, lgp = _d(attention_logits)
     N, S, M, D, Lq, L, K = _dims(v, sh, off)
     out = np.zeros((N, Lq, M * D))
-    _check(lib.msda_oracle_forward_fused(N, S, M, D, Lq, L, K, vp, shp, stp, refp, offp, lgp, _d(out)[1]),
-           "forward_fused")
+    _check(lib.msda_oracle_forward_fused(N, S, M, D, Lq, L, K, vp, shp, stp, refp, offp, lgp, _d(out)[1],
+                                         options), "forward_fused")
     return out
 
 
-def backward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, grad_output):
+def backward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, grad_output,
+             options=0):
     """a6-a8.  Returns (grad_value [N,S,M,D], grad_loc [N,Lq,M,L,K,2], grad_attn [N,Lq,M,L,K])."""
     lib = _load()
     v, vp = _d(value)
@@ -144,12 +150,12 @@ def backward(value, spatial_shapes, level_start_index, sampling_locations, atten
     gl = np.zeros(loc.shape)
     ga = np.zeros(a.shape)
     _check(lib.msda_oracle_backward(N, S, M, D, Lq, L, K, vp, shp, stp, locp, ap, gp,
-                                    _d(gv)[1], _d(gl)[1], _d(ga)[1]), "backward")
+                                    _d(gv)[1], _d(gl)[1], _d(ga)[1], options), "backward")
     return gv, gl, ga
 
 
 def backward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
-                   attention_logits, grad_output):
+                   attention_logits, grad_output, options=0):
     """a9.  Returns (grad_value, grad_reference_points, grad_sampling_offsets, grad_attention_logits)."""
     lib = _load()
     v, vp = _d(value)
@@ -165,6 +171,7 @@ def backward_fused(value, spatial_shapes, level_start_index, reference_points, s
     go = np.zeros(off.shape)
     gl = np.zeros(lg.shape)
     _check(lib.msda_oracle_backward_fused(N, S, M, D, Lq, L, K, vp, shp, stp, refp, offp, lgp, gp,
-                                          _d(gv)[1], _d(gr)[1], _d(go)[1], _d(gl)[1]), "backward_fused")
+                                          _d(gv)[1], _d(gr)[1], _d(go)[1], _d(gl)[1], options),
+           "backward_fused")
     return gv, gr, go, gl
 

@@ -44,8 +44,20 @@
  *     may pick neighbouring cells; bilinear interpolation is continuous there,
  *     so only the (one-sided) location gradient depends on the choice.
  *
+ * Options (the last argument of the forward and backward entry points; bits):
+ *   1  per-level softmax: the fused calls normalise the n_points logits of each
+ *      level separately.  [MSDA-tut] §2.2 prose says the normalisation runs over
+ *      k, per level; its §3.2 code normalises over all n_levels*n_points.  Both
+ *      readings are offered; 0 is the code's.
+ *   2  align_corners: px = loc_x * (W_l - 1), py = loc_y * (H_l - 1), the pixel
+ *      centres sit at i / (W_l - 1) (grid_sample with align_corners=True, the
+ *      convention of the DAT pages' sampler); the fused location is still
+ *      loc = ref + off / (W_l, H_l).
+ *
  * Return value of every entry point: 0 on success, -1 on a bad argument.
  */
+#define OPT_PER_LEVEL_SOFTMAX 1
+#define OPT_ALIGN_CORNERS 2
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -56,21 +68,37 @@
 /* Compiled with -ffp-contract=off so that each float operation rounds once.  */
 /* ------------------------------------------------------------------------- */
 
-/* Unfused path: the corner is floor(RN(RN(loc * size) - 0.5)). */
-static int64_t decide_floor_unfused(double loc, int64_t size)
+/* Unfused path: the corner is floor(RN(RN(loc * size) - 0.5)), or with
+ * align_corners floor(RN(loc * (size - 1))). */
+static int64_t decide_floor_unfused(double loc, int64_t size, int align)
 {
     float lf = (float)loc;
+    if (align) {
+        float sf = (float)(size - 1);
+        float p = lf * sf;
+        return (int64_t)floorf(p);
+    }
     float sf = (float)size;
     float p = lf * sf;
     float ph = p - 0.5f;
     return (int64_t)floorf(ph);
 }
 
-/* Fused path: the corner is floor(RN(RN(ref * size) + RN(off - 0.5))). */
-static int64_t decide_floor_fused(double ref, double off, int64_t size)
+/* Fused path: the corner is floor(RN(RN(ref * size) + RN(off - 0.5))), or with
+ * align_corners floor(RN(RN(ref * (size - 1)) + RN(off * r))), r the fp32
+ * quotient (size - 1) / size (the offset is in pixels of size). */
+static int64_t decide_floor_fused(double ref, double off, int64_t size, int align)
 {
     float rf = (float)ref;
     float of = (float)off;
+    if (align) {
+        float sm1 = (float)(size - 1);
+        float r = sm1 / (float)size;
+        float p = rf * sm1;
+        float t = of * r;
+        float s = p + t;
+        return (int64_t)floorf(s);
+    }
     float sf = (float)size;
     float p = rf * sf;
     float t = of - 0.5f;
@@ -153,24 +181,25 @@ static void make_corners(int64_t x0, int64_t y0, double fx, double fy, int64_t H
         }
 }
 
-static void corners_unfused(double lx, double ly, int64_t H, int64_t W, int64_t start, corners_t *c)
+static void corners_unfused(double lx, double ly, int64_t H, int64_t W, int64_t start, int align,
+                            corners_t *c)
 {
-    int64_t x0 = decide_floor_unfused(lx, W);
-    int64_t y0 = decide_floor_unfused(ly, H);
-    double px = lx * (double)W - 0.5;   /* align_corners=False */
-    double py = ly * (double)H - 0.5;
+    int64_t x0 = decide_floor_unfused(lx, W, align);
+    int64_t y0 = decide_floor_unfused(ly, H, align);
+    double px = align ? lx * (double)(W - 1) : lx * (double)W - 0.5;
+    double py = align ? ly * (double)(H - 1) : ly * (double)H - 0.5;
     make_corners(x0, y0, px - (double)x0, py - (double)y0, H, W, start, c);
 }
 
 static void corners_fused(double rx, double ry, double ox, double oy, int64_t H, int64_t W,
-                          int64_t start, corners_t *c)
+                          int64_t start, int align, corners_t *c)
 {
-    int64_t x0 = decide_floor_fused(rx, ox, W);
-    int64_t y0 = decide_floor_fused(ry, oy, H);
+    int64_t x0 = decide_floor_fused(rx, ox, W, align);
+    int64_t y0 = decide_floor_fused(ry, oy, H, align);
     double lx = rx + ox / (double)W;    /* step a1 */
     double ly = ry + oy / (double)H;
-    double px = lx * (double)W - 0.5;   /* step a3 */
-    double py = ly * (double)H - 0.5;
+    double px = align ? lx * (double)(W - 1) : lx * (double)W - 0.5;   /* step a3 */
+    double py = align ? ly * (double)(H - 1) : ly * (double)H - 0.5;
     make_corners(x0, y0, px - (double)x0, py - (double)y0, H, W, start, c);
 }
 
@@ -206,8 +235,9 @@ static int forward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, i
                         int64_t Len_q, int64_t n_levels, int64_t n_points,
                         const double *value, const int64_t *shapes, const int64_t *starts,
                         const double *loc_or_ref, const double *offsets, const double *attn,
-                        double *out)
+                        double *out, int64_t options)
 {
+    int align = (options & OPT_ALIGN_CORNERS) != 0;
     if (N < 0 || Len_in < 0 || n_heads <= 0 || D <= 0 || Len_q < 0 || n_levels <= 0 || n_points <= 0)
         return -1;
     if (check_levels(Len_in, n_levels, shapes, starts)) return -1;
@@ -226,9 +256,9 @@ static int forward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, i
                         if (fused) {
                             const double *ref = loc_or_ref + ((n * Len_q + q) * n_levels + l) * 2;
                             corners_fused(ref[0], ref[1], offsets[2 * s], offsets[2 * s + 1], H, W,
-                                          starts[l], &c);
+                                          starts[l], align, &c);
                         } else {
-                            corners_unfused(loc_or_ref[2 * s], loc_or_ref[2 * s + 1], H, W, starts[l], &c);
+                            corners_unfused(loc_or_ref[2 * s], loc_or_ref[2 * s + 1], H, W, starts[l], align, &c);
                         }
                         gather_sample(value, Len_in, n_heads, D, n, m, &c, sample);
                         for (int64_t d = 0; d < D; ++d) o[d] += attn[s] * sample[d];
@@ -243,10 +273,20 @@ int msda_oracle_forward(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, i
                         int64_t n_levels, int64_t n_points, const double *value,
                         const int64_t *spatial_shapes, const int64_t *level_start_index,
                         const double *sampling_locations, const double *attention_weights,
-                        double *output)
+                        double *output, int64_t options)
 {
     return forward_impl(0, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
-                        level_start_index, sampling_locations, NULL, attention_weights, output);
+                        level_start_index, sampling_locations, NULL, attention_weights, output, options);
+}
+
+/* The softmax of step a2 with the grouping the options select: all
+ * n_levels*n_points logits of a (query, head), or each level's n_points. */
+static int softmax_groups(int64_t rows, int64_t n_levels, int64_t n_points, const double *logits,
+                          double *weights, int64_t options)
+{
+    if (options & OPT_PER_LEVEL_SOFTMAX)
+        return msda_oracle_softmax(rows * n_levels, n_points, logits, weights);
+    return msda_oracle_softmax(rows, n_levels * n_points, logits, weights);
 }
 
 /* Steps a1-a5: softmax (a2) of the raw logits, then the sampling with the
@@ -255,16 +295,16 @@ int msda_oracle_forward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64_
                               int64_t n_levels, int64_t n_points, const double *value,
                               const int64_t *spatial_shapes, const int64_t *level_start_index,
                               const double *reference_points, const double *sampling_offsets,
-                              const double *attention_logits, double *output)
+                              const double *attention_logits, double *output, int64_t options)
 {
     int64_t rows = N * Len_q * n_heads, cols = n_levels * n_points;
     if (rows < 0 || cols <= 0) return -1;
     double *attn = (double *)malloc(sizeof(double) * (size_t)(rows * cols + 1));
     if (!attn) return -1;
-    int rc = msda_oracle_softmax(rows, cols, attention_logits, attn);
+    int rc = softmax_groups(rows, n_levels, n_points, attention_logits, attn, options);
     if (!rc)
         rc = forward_impl(1, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
-                          level_start_index, reference_points, sampling_offsets, attn, output);
+                          level_start_index, reference_points, sampling_offsets, attn, output, options);
     free(attn);
     return rc;
 }
@@ -289,8 +329,9 @@ static int backward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, 
                          int64_t Len_q, int64_t n_levels, int64_t n_points, const double *value,
                          const int64_t *shapes, const int64_t *starts, const double *loc_or_ref,
                          const double *offsets, const double *attn, const double *grad_out,
-                         grads_t *gr)
+                         grads_t *gr, int64_t options)
 {
+    int align = (options & OPT_ALIGN_CORNERS) != 0;
     if (N < 0 || Len_in < 0 || n_heads <= 0 || D <= 0 || Len_q < 0 || n_levels <= 0 || n_points <= 0)
         return -1;
     if (check_levels(Len_in, n_levels, shapes, starts)) return -1;
@@ -309,9 +350,9 @@ static int backward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, 
                         if (fused) {
                             const double *ref = loc_or_ref + ((n * Len_q + q) * n_levels + l) * 2;
                             corners_fused(ref[0], ref[1], offsets[2 * s], offsets[2 * s + 1], H, W,
-                                          starts[l], &c);
+                                          starts[l], align, &c);
                         } else {
-                            corners_unfused(loc_or_ref[2 * s], loc_or_ref[2 * s + 1], H, W, starts[l], &c);
+                            corners_unfused(loc_or_ref[2 * s], loc_or_ref[2 * s + 1], H, W, starts[l], align, &c);
                         }
                         for (int ci = 0; ci < 4; ++ci)
                             for (int64_t d = 0; d < D; ++d)
@@ -328,8 +369,9 @@ static int backward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, 
                             gy += g[d] * dsy;
                         }
                         gr->grad_attn[s] = ga;
-                        gr->grad_loc[2 * s + 0] = attn[s] * gx * (double)W;
-                        gr->grad_loc[2 * s + 1] = attn[s] * gy * (double)H;
+                        /* d px / d loc_x = W (W - 1 with align_corners) */
+                        gr->grad_loc[2 * s + 0] = attn[s] * gx * (double)(align ? W - 1 : W);
+                        gr->grad_loc[2 * s + 1] = attn[s] * gy * (double)(align ? H - 1 : H);
                         for (int ci = 0; ci < 4; ++ci) {
                             if (c.row[ci] < 0) continue;
                             double *gv = gr->grad_value + ((n * Len_in + c.row[ci]) * n_heads + m) * D;
@@ -347,12 +389,12 @@ int msda_oracle_backward(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, 
                          const int64_t *spatial_shapes, const int64_t *level_start_index,
                          const double *sampling_locations, const double *attention_weights,
                          const double *grad_output, double *grad_value,
-                         double *grad_sampling_locations, double *grad_attention_weights)
+                         double *grad_sampling_locations, double *grad_attention_weights, int64_t options)
 {
     grads_t gr = {grad_value, grad_sampling_locations, grad_attention_weights};
     return backward_impl(0, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
                          level_start_index, sampling_locations, NULL, attention_weights,
-                         grad_output, &gr);
+                         grad_output, &gr, options);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -367,7 +409,7 @@ int msda_oracle_backward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64
                                const double *reference_points, const double *sampling_offsets,
                                const double *attention_logits, const double *grad_output,
                                double *grad_value, double *grad_reference_points,
-                               double *grad_sampling_offsets, double *grad_attention_logits)
+                               double *grad_sampling_offsets, double *grad_attention_logits, int64_t options)
 {
     int64_t rows = N * Len_q * n_heads, cols = n_levels * n_points;
     if (rows < 0 || cols <= 0) return -1;
@@ -377,11 +419,11 @@ int msda_oracle_backward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64
     double *gattn = (double *)malloc(sizeof(double) * ns);
     int rc = -1;
     if (!attn || !gloc || !gattn) goto done;
-    rc = msda_oracle_softmax(rows, cols, attention_logits, attn);
+    rc = softmax_groups(rows, n_levels, n_points, attention_logits, attn, options);
     if (rc) goto done;
     grads_t gr = {grad_value, gloc, gattn};
     rc = backward_impl(1, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
-                       level_start_index, reference_points, sampling_offsets, attn, grad_output, &gr);
+                       level_start_index, reference_points, sampling_offsets, attn, grad_output, &gr, options);
     if (rc) goto done;
     for (int64_t i = 0; i < N * Len_q * n_levels * 2; ++i) grad_reference_points[i] = 0.0;
     for (int64_t n = 0; n < N; ++n)
@@ -399,10 +441,14 @@ int msda_oracle_backward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64
                         gref[1] += gloc[2 * s + 1];
                     }
                 }
-                double dot = 0.0;
-                for (int64_t j = 0; j < cols; ++j) dot += attn[r * cols + j] * gattn[r * cols + j];
-                for (int64_t j = 0; j < cols; ++j)
-                    grad_attention_logits[r * cols + j] = attn[r * cols + j] * (gattn[r * cols + j] - dot);
+                /* the softmax's groups: the whole row, or each level's n_points */
+                int64_t g = (options & OPT_PER_LEVEL_SOFTMAX) ? n_points : cols;
+                for (int64_t j0 = 0; j0 < cols; j0 += g) {
+                    double dot = 0.0;
+                    for (int64_t j = j0; j < j0 + g; ++j) dot += attn[r * cols + j] * gattn[r * cols + j];
+                    for (int64_t j = j0; j < j0 + g; ++j)
+                        grad_attention_logits[r * cols + j] = attn[r * cols + j] * (gattn[r * cols + j] - dot);
+                }
             }
 done:
     free(attn);

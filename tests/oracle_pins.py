@@ -25,6 +25,15 @@ What pins what:
   adjoint             <grad_value, dV> = <g, forward(dV)> (the forward is linear in value).
   fused_*             a9 and the fused forward: finite differences through
                       a1-a2, sum of logit gradients is 0, composition with a1/a2.
+  align_*             the align_corners option (px = loc * (W - 1)): torch
+                      grid_sample(align_corners=True) forward and autograd in
+                      float64, and exact gathers at loc = i / (W - 1).
+  per_level_*         the per-level softmax option: logits = log p with each
+                      level's p summing to 1 give A = p; a constant added to one
+                      level's logits changes nothing (it would change the
+                      whole-row softmax); with one level it equals the whole-row
+                      softmax; finite differences of the fused backward and
+                      zero-sum logit gradients per level.
 """
 import math
 import os
@@ -199,7 +208,7 @@ def pin_far_outside():
     return float(np.abs(out).max()), 0.0
 
 
-def _grid_sample_forward(value, shapes, starts, loc, attn):
+def _grid_sample_forward(value, shapes, starts, loc, attn, align_corners=False):
     """The tutorial module's per-level grid_sample path, in float64 torch."""
     N, S, M, D = value.shape
     _, Lq, _, L, K, _ = loc.shape
@@ -209,7 +218,7 @@ def _grid_sample_forward(value, shapes, starts, loc, attn):
         s0 = int(starts[l])
         v_l = value[:, s0:s0 + H * W].reshape(N, H, W, M, D).permute(0, 3, 4, 1, 2).reshape(N * M, D, H, W)
         grid = (2.0 * loc[:, :, :, l] - 1.0).permute(0, 2, 1, 3, 4).reshape(N * M, Lq, K, 2)
-        smp = F.grid_sample(v_l, grid, mode="bilinear", padding_mode="zeros", align_corners=False)
+        smp = F.grid_sample(v_l, grid, mode="bilinear", padding_mode="zeros", align_corners=align_corners)
         a = attn[:, :, :, l].permute(0, 2, 1, 3).reshape(N * M, 1, Lq, K)
         out = out + (smp * a).sum(-1)                       # (N*M, D, Lq)
     return out.reshape(N, M, D, Lq).permute(0, 3, 1, 2).reshape(N, Lq, M * D)
@@ -389,6 +398,128 @@ def pin_fused_backward():
     return worst, 1e-6
 
 
+# --------------------------------------------------------------------------- options
+AL = oracle.ALIGN_CORNERS
+PL = oracle.PER_LEVEL_SOFTMAX
+
+
+def pin_align_grid_sample():
+    worst = 0.0
+    for seed, lv in [(31, ((8, 8), (4, 4))), (32, ((5, 9), (3, 2), (2, 2)))]:
+        t = _tiny(seed=seed, levels=lv, loc_lo=-0.3, loc_hi=1.3, Lq=25, K=3, M=3, D=5)
+        out = oracle.forward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"], options=AL)
+        ref = _grid_sample_forward(torch.from_numpy(t["value"]), t["shapes"], t["starts"],
+                                   torch.from_numpy(t["loc"]), torch.from_numpy(t["attn"]),
+                                   align_corners=True).numpy()
+        worst = max(worst, _err(out, ref))
+    return worst, 1e-12
+
+
+def pin_align_pixel_centres():
+    """With align_corners the pixel centres sit at i / (W - 1), the borders included."""
+    t = _tiny(seed=33, levels=((5, 7), (3, 4)), Lq=30, K=2, M=2, D=3)
+    rng = np.random.Generator(np.random.PCG64(34))
+    loc = np.empty_like(t["loc"])
+    expect = np.zeros((t["N"], t["Lq"], t["M"], t["D"]))
+    for l, (H, W) in enumerate(t["shapes"]):
+        ix = rng.integers(0, W, size=loc[..., l, :, 0].shape)
+        iy = rng.integers(0, H, size=loc[..., l, :, 1].shape)
+        ix[..., 0, 0] = W - 1          # the far border is a pixel centre too
+        iy[..., 0, 0] = 0
+        loc[..., l, :, 0] = ix / (W - 1)
+        loc[..., l, :, 1] = iy / (H - 1)
+        rows = t["starts"][l] + iy * W + ix
+        for n in range(t["N"]):
+            for q in range(t["Lq"]):
+                for m in range(t["M"]):
+                    for k in range(t["K"]):
+                        expect[n, q, m] += t["attn"][n, q, m, l, k] * t["value"][n, rows[n, q, m, k], m]
+    out = oracle.forward(t["value"], t["shapes"], t["starts"], loc, t["attn"], options=AL)
+    return _err(out, expect.reshape(out.shape)), 1e-12
+
+
+def pin_align_backward_autograd():
+    t = _tiny(seed=35, levels=((8, 8), (4, 4), (3, 5)), loc_lo=-0.2, loc_hi=1.2, Lq=20, K=2, M=2, D=4)
+    v = torch.from_numpy(t["value"]).requires_grad_(True)
+    loc = torch.from_numpy(t["loc"]).requires_grad_(True)
+    a = torch.from_numpy(t["attn"]).requires_grad_(True)
+    out = _grid_sample_forward(v, t["shapes"], t["starts"], loc, a, align_corners=True)
+    out.backward(torch.from_numpy(t["g"]))
+    gv, gl, ga = oracle.backward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"], t["g"], options=AL)
+    worst = max(_rel(gv, v.grad.numpy()), _rel(gl, loc.grad.numpy()), _rel(ga, a.grad.numpy()))
+    return worst, 1e-12
+
+
+def pin_per_level_closed():
+    f = _fused_inputs(36, Lq=10, M=2, K=3, D=4)
+    L, K = f["shapes"].shape[0], 3
+    rng = np.random.Generator(np.random.PCG64(37))
+    p = rng.uniform(0.1, 1.0, size=f["logits"].shape).reshape(-1, L, K)
+    p /= p.sum(-1, keepdims=True)                      # each level's K weights sum to 1
+    logits = np.log(p).reshape(f["logits"].shape)
+    loc = oracle.locations(f["shapes"], f["ref"], f["off"])
+    out = oracle.forward_fused(f["value"], f["shapes"], f["starts"], f["ref"], f["off"], logits, options=PL)
+    worst = _err(out, oracle.forward(f["value"], f["shapes"], f["starts"], loc, p.reshape(loc.shape[:-1])))
+    # a constant added to one level's logits does not move that level's weights
+    shifted = logits.reshape(-1, L, K).copy()
+    shifted[:, 1, :] += 3.0
+    out2 = oracle.forward_fused(f["value"], f["shapes"], f["starts"], f["ref"], f["off"],
+                                shifted.reshape(logits.shape), options=PL)
+    worst = max(worst, _err(out2, out))
+    # one level: the per-level softmax is the whole-row softmax
+    f1 = _fused_inputs(38, levels=((6, 7),), Lq=9, M=2, K=4, D=3)
+    a = oracle.forward_fused(f1["value"], f1["shapes"], f1["starts"], f1["ref"], f1["off"], f1["logits"], options=PL)
+    b = oracle.forward_fused(f1["value"], f1["shapes"], f1["starts"], f1["ref"], f1["off"], f1["logits"])
+    return max(worst, _err(a, b)), 1e-12
+
+
+def pin_options_fused_backward():
+    """Finite differences through the fused forward with each option, and the
+    per-level zero sum of the logit gradients."""
+    worst = 0.0
+    for opt, seed in ((PL, 39), (AL, 40), (PL | AL, 41)):
+        f = _fused_inputs(seed, Lq=4, K=2, D=3)
+        gv, gr, go, gl = oracle.backward_fused(f["value"], f["shapes"], f["starts"], f["ref"], f["off"],
+                                               f["logits"], f["g"], options=opt)
+
+        def J(ref=None, off=None, logits=None):
+            out = oracle.forward_fused(f["value"], f["shapes"], f["starts"], f["ref"] if ref is None else ref,
+                                       f["off"] if off is None else off,
+                                       f["logits"] if logits is None else logits, options=opt)
+            return float((out * f["g"]).sum())
+
+        h = 1e-6
+        loc = oracle.locations(f["shapes"], f["ref"], f["off"])
+        kink = np.zeros(loc.shape[:-1], dtype=bool)
+        for l, (H, W) in enumerate(f["shapes"]):
+            for c, size in ((0, W), (1, H)):
+                px = loc[..., l, :, c] * (size - 1) if opt & AL else _px(loc[..., l, :, c], size)
+                kink[..., l, :] |= np.abs(px - np.round(px)) < 1e-3
+        for idx in np.ndindex(f["off"].shape):
+            if kink[idx[:-1]]:
+                continue
+            p, m = f["off"].copy(), f["off"].copy()
+            p[idx] += h
+            m[idx] -= h
+            worst = max(worst, abs((J(off=p) - J(off=m)) / (2 * h) - go[idx]) / (1 + abs(go[idx])))
+        for idx in np.ndindex(f["ref"].shape):
+            if kink[idx[0], idx[1], :, idx[2]].any():
+                continue
+            p, m = f["ref"].copy(), f["ref"].copy()
+            p[idx] += h
+            m[idx] -= h
+            worst = max(worst, abs((J(ref=p) - J(ref=m)) / (2 * h) - gr[idx]) / (1 + abs(gr[idx])))
+        for idx in np.ndindex(f["logits"].shape):
+            p, m = f["logits"].copy(), f["logits"].copy()
+            p[idx] += h
+            m[idx] -= h
+            worst = max(worst, abs((J(logits=p) - J(logits=m)) / (2 * h) - gl[idx]) / (1 + abs(gl[idx])))
+        if opt & PL:
+            L = f["shapes"].shape[0]
+            worst = max(worst, float(np.abs(gl.reshape(gl.shape[:-1] + (L, -1)).sum(-1)).max()))
+    return worst, 1e-6
+
+
 ALL_PINS = {
     "worked_example": pin_worked_example,
     "softmax_closed": pin_softmax_closed,
@@ -403,6 +534,11 @@ ALL_PINS = {
     "adjoint": pin_adjoint,
     "fused_composition": pin_fused_composition,
     "fused_backward": pin_fused_backward,
+    "align_grid_sample": pin_align_grid_sample,
+    "align_pixel_centres": pin_align_pixel_centres,
+    "align_backward_autograd": pin_align_backward_autograd,
+    "per_level_closed": pin_per_level_closed,
+    "options_fused_backward": pin_options_fused_backward,
 }
 
 

@@ -15,8 +15,14 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "msda_oracle.c")
 
 # (name, text to find, replacement): each is a mistake someone could make
 MUTANTS = [
-    ("half_pixel_sign", "double px = lx * (double)W - 0.5;", "double px = lx * (double)W + 0.5;"),
-    ("align_corners_true", "double px = lx * (double)W - 0.5;", "double px = lx * (double)(W - 1);"),
+    ("half_pixel_sign", "lx * (double)(W - 1) : lx * (double)W - 0.5;", "lx * (double)(W - 1) : lx * (double)W + 0.5;"),
+    ("align_corners_true", "lx * (double)(W - 1) : lx * (double)W - 0.5;", "lx * (double)(W - 1) : lx * (double)(W - 1);"),
+    ("align_corners_ignored", "int align = (options & OPT_ALIGN_CORNERS) != 0;", "int align = 0;"),
+    ("align_corners_uses_W", "lx * (double)(W - 1) : lx", "lx * (double)W : lx"),
+    ("align_grad_uses_W", "(double)(align ? W - 1 : W)", "(double)W"),
+    ("per_level_softmax_over_row", "return msda_oracle_softmax(rows * n_levels, n_points, logits, weights);",
+     "return msda_oracle_softmax(rows, n_levels * n_points, logits, weights);"),
+    ("per_level_softmax_grad_over_row", "? n_points : cols;", "? cols : cols;"),
     ("swapped_x_weights", "(i ? fx : 1.0 - fx)", "(i ? 1.0 - fx : fx)"),
     ("x_uses_fy", "(i ? fx : 1.0 - fx) * (j ? fy : 1.0 - fy)", "(i ? fy : 1.0 - fy) * (j ? fy : 1.0 - fy)"),
     ("bounds_off_by_one", "xc < W && yc >= 0", "xc <= W && yc >= 0"),
@@ -28,7 +34,7 @@ MUTANTS = [
     ("softmax_not_shifted", "y[j] = exp(x[j] - mx);", "y[j] = exp(x[j]);"),
     ("offset_x_scaled_by_H", "sampling_offsets[i + 0] / W;", "sampling_offsets[i + 0] / H;"),
     ("fused_offset_x_scaled_by_H", "double lx = rx + ox / (double)W;", "double lx = rx + ox / (double)H;"),
-    ("grad_loc_missing_scale", "attn[s] * gx * (double)W", "attn[s] * gx"),
+    ("grad_loc_missing_scale", "attn[s] * gx * (double)(align ? W - 1 : W)", "attn[s] * gx"),
     ("grad_loc_wrong_sign", "(1.0 - c.fy) * (v[D + d] - v[d])", "(1.0 - c.fy) * (v[d] - v[D + d])"),
     ("grad_loc_y_uses_fy", "(1.0 - c.fx) * (v[2 * D + d] - v[d]) + c.fx",
      "(1.0 - c.fy) * (v[2 * D + d] - v[d]) + c.fy"),
