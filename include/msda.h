@@ -99,7 +99,24 @@ typedef struct msda_problem {
     int32_t n_levels;   /* L */
     int32_t n_points;   /* K, samples per level per head */
     int32_t dtype;      /* msda_dtype */
+    uint32_t options;   /* MSDA_OPT_* bits, 0 for the default method */
 } msda_problem;
+
+/* msda_problem.options: readings of the method the pages leave open.
+ *
+ * MSDA_OPT_PER_LEVEL_SOFTMAX  the fused calls normalise the n_points logits
+ *     of each level separately ("可变形注意力…" §2.2 prose: the normalisation
+ *     runs over k for each level) instead of all n_levels*n_points of the
+ *     (query, head) (its §3.2 module code; the default).  The unfused calls
+ *     take the weights as given and ignore this bit.
+ * MSDA_OPT_ALIGN_CORNERS  pixel coordinate px = loc_x * (W_l - 1),
+ *     py = loc_y * (H_l - 1): pixel centres at i / (W_l - 1), as a sampler
+ *     with grid_sample(align_corners=True) places them (the DAT pages'
+ *     sampler).  The fused location is still loc = ref + off / (W_l, H_l);
+ *     gradients follow (d px / d loc_x = W_l - 1).  Default: px = loc_x * W_l
+ *     - 0.5 (align_corners=False). */
+#define MSDA_OPT_PER_LEVEL_SOFTMAX  1u
+#define MSDA_OPT_ALIGN_CORNERS      2u
 
 /* msda_backward flags */
 #define MSDA_DETERMINISTIC          1u  /* bitwise reproducible grad_value (fixed-point sums) */

@@ -6,10 +6,11 @@ signatures: msda_forward, msda_forward_fused, msda_backward,
 msda_backward_fused.
 """
 from ._capi import (EXPORTED, LIBRARY, MSDA_ACCUMULATE_GRAD_VALUE, MSDA_BF16, MSDA_DETERMINISTIC, MSDA_F32,
-                    MSDAError, lib, msda_backward, msda_backward_fused, msda_backward_noalloc,
+                    MSDA_OPT_ALIGN_CORNERS, MSDA_OPT_PER_LEVEL_SOFTMAX, MSDAError, lib, msda_backward, msda_backward_fused, msda_backward_noalloc,
                     msda_backward_workspace_size, msda_forward, msda_forward_fused, msda_problem)
 
 __all__ = ["msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_fused",
            "msda_backward_workspace_size", "msda_backward_noalloc", "MSDAError",
-           "MSDA_DETERMINISTIC", "MSDA_ACCUMULATE_GRAD_VALUE", "MSDA_F32", "MSDA_BF16", "LIBRARY", "EXPORTED",
+           "MSDA_DETERMINISTIC", "MSDA_ACCUMULATE_GRAD_VALUE", "MSDA_F32", "MSDA_BF16",
+           "MSDA_OPT_PER_LEVEL_SOFTMAX", "MSDA_OPT_ALIGN_CORNERS", "LIBRARY", "EXPORTED",
            "lib", "msda_problem"]

@@ -19,6 +19,8 @@ MSDA_F32 = 0
 MSDA_BF16 = 1
 MSDA_DETERMINISTIC = 1
 MSDA_ACCUMULATE_GRAD_VALUE = 2
+MSDA_OPT_PER_LEVEL_SOFTMAX = 1
+MSDA_OPT_ALIGN_CORNERS = 2
 
 EXPORTED = ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_fused",
             "msda_backward_workspace_size", "msda_backward_noalloc", "msda_status_string", "msda_last_error",
@@ -35,7 +37,7 @@ class MSDAError(RuntimeError):
 class msda_problem(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int32), ("Len_in", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("Len_q", ctypes.c_int32), ("n_levels", ctypes.c_int32),
-                ("n_points", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("n_points", ctypes.c_int32), ("dtype", ctypes.c_int32), ("options", ctypes.c_uint32)]
 
 
 def _load():
@@ -116,13 +118,13 @@ def _stream(stream, device):
     return ctypes.c_void_p(int(stream))
 
 
-def problem(value, Len_q, n_levels, n_points):
+def problem(value, Len_q, n_levels, n_points, options=0):
     N, S, M, D = value.shape
-    return msda_problem(N, S, M, D, Len_q, n_levels, n_points, _dtype_code(value))
+    return msda_problem(N, S, M, D, Len_q, n_levels, n_points, _dtype_code(value), options)
 
 
 def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
-                 output=None, stream=None):
+                 output=None, stream=None, options=0):
     """out[N, Len_q, M*D] from value [N,Len_in,M,D] (f32|bf16), sampling_locations
     [N,Len_q,M,L,K,2] f32 and attention_weights [N,Len_q,M,L,K] f32."""
     lv = _HostLevels(spatial_shapes, level_start_index)
@@ -138,7 +140,7 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
         output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
     elif tuple(output.shape) != (N, Lq, M * D) or output.dtype != value.dtype:
         raise ValueError("output must be [N, Len_q, M*D] with the dtype of value")
-    prob = problem(value, Lq, L, K)
+    prob = problem(value, Lq, L, K, options)
     _check(_lib.msda_forward(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
                              _dev(sampling_locations, "sampling_locations", torch.float32),
                              _dev(attention_weights, "attention_weights", torch.float32),
@@ -147,7 +149,7 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
 
 
 def msda_forward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
-                       attention_logits, output=None, stream=None):
+                       attention_logits, output=None, stream=None, options=0):
     """out[N, Len_q, M*D] from reference_points [N,Len_q,L,2], sampling_offsets
     [N,Len_q,M,L,K,2] (pixels of each level) and attention_logits [N,Len_q,M,L*K]."""
     lv = _HostLevels(spatial_shapes, level_start_index)
@@ -163,7 +165,7 @@ def msda_forward_fused(value, spatial_shapes, level_start_index, reference_point
         raise ValueError("n_levels of sampling_offsets and spatial_shapes disagree")
     if output is None:
         output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
-    prob = problem(value, Lq, L, K)
+    prob = problem(value, Lq, L, K, options)
     _check(_lib.msda_forward_fused(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
                                    _dev(reference_points, "reference_points", torch.float32),
                                    _dev(sampling_offsets, "sampling_offsets", torch.float32),
@@ -173,13 +175,13 @@ def msda_forward_fused(value, spatial_shapes, level_start_index, reference_point
 
 
 def msda_backward_workspace_size(value, Len_q, n_levels, n_points, flags=0):
-    prob = problem(value, Len_q, n_levels, n_points)
+    prob = problem(value, Len_q, n_levels, n_points)  # the size does not depend on the options
     return int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
 
 
 def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, grad_output,
                   grad_value=None, grad_sampling_locations=None, grad_attention_weights=None, flags=0,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, options=0):
     """Returns (grad_value f32 [N,Len_in,M,D], grad_sampling_locations, grad_attention_weights)."""
     lv = _HostLevels(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
@@ -195,7 +197,7 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, 
         grad_sampling_locations = torch.empty_like(sampling_locations)
     if grad_attention_weights is None:
         grad_attention_weights = torch.empty_like(attention_weights)
-    prob = problem(value, Lq, L, K)
+    prob = problem(value, Lq, L, K, options)
     need = int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -214,7 +216,7 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, 
 def msda_backward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
                         attention_logits, grad_output, grad_value=None, grad_reference_points=None,
                         grad_sampling_offsets=None, grad_attention_logits=None, flags=0, workspace=None,
-                        stream=None):
+                        stream=None, options=0):
     """Gradient of msda_forward_fused.  Returns (grad_value f32 [N,Len_in,M,D],
     grad_reference_points [N,Len_q,L,2], grad_sampling_offsets [N,Len_q,M,L,K,2],
     grad_attention_logits shaped like attention_logits)."""
@@ -240,7 +242,7 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
         grad_sampling_offsets = torch.empty_like(sampling_offsets)
     if grad_attention_logits is None:
         grad_attention_logits = torch.empty_like(attention_logits)
-    prob = problem(value, Lq, L, K)
+    prob = problem(value, Lq, L, K, options)
     need = int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -260,14 +262,14 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
 
 def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
                           grad_output, grad_value, grad_sampling_locations, grad_attention_weights, flags=0,
-                          stream=None):
+                          stream=None, options=0):
     """Deterministic backward with the library's built-in scratch (no workspace,
     no allocation anywhere, the outputs included: the caller passes them).
     For callers that may not allocate device memory; see include/msda.h for
     the size limit and for why overlapping calls race."""
     lv = _HostLevels(spatial_shapes, level_start_index)
     Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
-    prob = problem(value, Lq, L, K)
+    prob = problem(value, Lq, L, K, options)
     _check(_lib.msda_backward_noalloc(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
                                       _dev(sampling_locations, "sampling_locations", torch.float32),
                                       _dev(attention_weights, "attention_weights", torch.float32),

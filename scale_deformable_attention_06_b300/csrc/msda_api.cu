@@ -31,6 +31,8 @@ msda_status make_geometry(const msda_problem *p, const int64_t *shapes, const in
         return fail(MSDA_ERR_INVALID_ARG, "negative size (N=%d Len_q=%d Len_in=%d)", p->N, p->Len_q, p->Len_in);
     if (p->n_heads < 1 || p->n_points < 1 || p->n_levels < 1)
         return fail(MSDA_ERR_INVALID_ARG, "n_heads, n_levels and n_points must be >= 1");
+    if (p->options & ~(MSDA_OPT_PER_LEVEL_SOFTMAX | MSDA_OPT_ALIGN_CORNERS))
+        return fail(MSDA_ERR_INVALID_ARG, "unknown option bits 0x%x", p->options);
     if (p->dtype != MSDA_F32 && p->dtype != MSDA_BF16)
         return fail(MSDA_ERR_UNSUPPORTED, "dtype %d is not MSDA_F32 or MSDA_BF16", p->dtype);
     if (p->head_dim != 8 && p->head_dim != 16 && p->head_dim != 32 && p->head_dim != 64)
@@ -74,12 +76,21 @@ msda_status make_geometry(const msda_problem *p, const int64_t *shapes, const in
     g.d.rows = (int)rows;
     g.d.qm = p->Len_q * p->n_heads;
     g.d.pix = (int)pix;
+    const bool align = (p->options & MSDA_OPT_ALIGN_CORNERS) != 0;
+    g.d.per_level_softmax = (p->options & MSDA_OPT_PER_LEVEL_SOFTMAX) != 0;
+    g.lv.shift = align ? 0.f : 0.5f;
     for (int l = 0; l < p->n_levels; ++l) {
         g.lv.H[l] = (int)shapes[2 * l];
         g.lv.W[l] = (int)shapes[2 * l + 1];
         g.lv.start[l] = (int)starts[l];
         g.lv.Hf[l] = (float)shapes[2 * l];
         g.lv.Wf[l] = (float)shapes[2 * l + 1];
+        // pixel scale, and the fp32 factor from offset pixels to the pixel
+        // coordinate: S / size, 1 without align_corners
+        g.lv.Sx[l] = align ? (float)(shapes[2 * l + 1] - 1) : g.lv.Wf[l];
+        g.lv.Sy[l] = align ? (float)(shapes[2 * l] - 1) : g.lv.Hf[l];
+        g.lv.Rx[l] = align ? g.lv.Sx[l] / g.lv.Wf[l] : 1.f;
+        g.lv.Ry[l] = align ? g.lv.Sy[l] / g.lv.Hf[l] : 1.f;
     }
     for (int s = 0; s < g.d.P; ++s) g.level_of[s] = (unsigned char)(s / p->n_points);
     return MSDA_OK;

@@ -127,6 +127,7 @@ struct BwdWarpSmem {
     uint4 rec[HW][RC + 1];             // corner records (padded rows)
     float4 res[HW][RC + 1];            // per sample: grad_attn, A*d/dpx, A*d/dpy
     float2 stat[HW];                   // fused: softmax max and 1 / sum of each query
+    float gdot[HW][kMaxLevels];        // fused, per-level softmax: sum_k A_k grad_A_k
 };
 
 template <int HW, int RC>
@@ -134,13 +135,16 @@ struct BwdWarpSmem<HW, RC, true> {
     uint4 rec[HW][RC + 1];
     float4 res[HW][RC + 1];
     float2 stat[HW];
+    float gdot[HW][kMaxLevels];
     unsigned key[kMergeSlots];         // corner pixel of the slot, kEmptyKey if free
     float4 alpha[kMergeSlots];         // per query of the warp: summed A * w_c (HW == 4)
     unsigned short list[kMergeSlots];  // occupied slots in order of first use
     int count;
 };
 
-template <typename T, int D, bool DET, bool MERGE, bool FUSED>
+// OPTS: the problem sets option bits (fused calls); without them the kernel
+// carries none of the option code.
+template <typename T, int D, bool DET, bool MERGE, bool FUSED, bool OPTS>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
 msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int R = D / 4, HW = 32 / R;
@@ -187,7 +191,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
         if (lane == 0) sm.count = 0;
         __syncwarp();
     }
-    if constexpr (FUSED) {
+    if (FUSED && !(OPTS && dm.per_level_softmax)) {
         // softmax statistics of the warp's queries (the same arithmetic as the
         // fused forward, so A is the same value there and here)
         for (int hh = 0; hh < HW; ++hh) {
@@ -222,14 +226,24 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 if constexpr (FUSED) {
                     const float2 rf = __ldg(reinterpret_cast<const float2 *>(a.ref) + (size_t)(n * dm.Len_q + qq) * dm.L + l);
                     const float2 of = load_stream2(a.off + 2 * si);
-                    pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
-                    pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
-                    const float2 st = sm.stat[hh];
+                    float2 st;
+                    if constexpr (OPTS) {
+                        pixel_coord_fused(rf.x, of.x, a.lv.Sx[l], a.lv.Rx[l], a.lv.shift, x0, fx);
+                        pixel_coord_fused(rf.y, of.y, a.lv.Sy[l], a.lv.Ry[l], a.lv.shift, y0, fy);
+                        if (dm.per_level_softmax)
+                            group_softmax_stats(a.logits + (si - (r0 + j)) + l * dm.K, dm.K, st.x, st.y);
+                        else
+                            st = sm.stat[hh];
+                    } else {
+                        pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
+                        pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
+                        st = sm.stat[hh];
+                    }
                     A = expf(load_stream1(a.logits + si) - st.x) * st.y;
                 } else {
                     const float2 lc = load_stream2(a.loc + 2 * si);
-                    pixel_coord(lc.x, Wf, x0, fx);
-                    pixel_coord(lc.y, Hf, y0, fy);
+                    pixel_coord(lc.x, a.lv.Sx[l], a.lv.shift, x0, fx);
+                    pixel_coord(lc.y, a.lv.Sy[l], a.lv.shift, y0, fy);
                     A = load_stream1(a.attn + si);
                 }
                 rc = pack_record(x0, fx, y0, fy, A, a.lv.W[l], a.lv.H[l], Wf, Hf, a.lv.start[l]);
@@ -351,14 +365,19 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 const size_t si = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + r0 + j;
                 const float4 res = sm.res[hh][j];
                 if constexpr (FUSED) {
-                    // offsets are pixels of the level: d loc / d off = 1 / (W, H)
-                    __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si, make_float2(res.y, res.z));
+                    // offsets are pixels of the level: d px / d off = S / W = Rx
+                    if constexpr (OPTS)
+                        __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si,
+                               make_float2(res.y * a.lv.Rx[l], res.z * a.lv.Ry[l]));
+                    else
+                        __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si, make_float2(res.y, res.z));
                     a.grad_attn[si] = res.x;           // grad of A; read back below by this lane
                     dotp[it] = __fmaf_rn(__uint_as_float(sm.rec[hh][j].w), res.x, dotp[it]);
                 } else {
                     __stcs(a.grad_attn + si, res.x);
+                    // d px / d loc = S (W, or W - 1 with align_corners)
                     __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si,
-                           make_float2(res.y * a.lv.Wf[l], res.z * a.lv.Hf[l]));
+                           make_float2(res.y * a.lv.Sx[l], res.z * a.lv.Sy[l]));
                 }
             }
         }
@@ -377,6 +396,28 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
             for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
             tot[it] = v;
         }
+        if (OPTS && dm.per_level_softmax) {
+            // groups are the levels.  Their K grad_A were written by several
+            // lanes (and a level may straddle two record chunks), so first every
+            // (query, level) dot sum_k A_k grad_A_k, one lane each in a fixed
+            // order, while all grad_A are still in place.
+            __syncwarp();
+            for (int u = lane; u < HW * dm.L; u += 32) {
+                const int hh = u / dm.L, l = u % dm.L;
+                const int qq = qb * HW + hh;
+                float dot = 0.f;
+                if (qq < dm.Len_q) {
+                    const size_t g0 = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + (size_t)l * dm.K;
+                    float mx, inv;
+                    group_softmax_stats(a.logits + g0, dm.K, mx, inv);
+                    for (int k = 0; k < dm.K; ++k)
+                        dot = __fmaf_rn(expf(__ldg(a.logits + g0 + k) - mx) * inv, __ldcg(a.grad_attn + g0 + k), dot);
+                }
+                sm.gdot[hh][l] = dot;
+            }
+            __syncwarp();
+        }
+        // grad_logit = A * (grad_A - dot); each lane rewrites only the samples it wrote
         for (int r0 = 0; r0 < P; r0 += RC) {
             const int RJ = min(RC, P - r0);
 #pragma unroll
@@ -386,9 +427,20 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 const int qq = qb * HW + hh;
                 if (j < RJ && qq < dm.Len_q) {
                     const size_t si = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + r0 + j;
-                    const float2 st = sm.stat[hh];
-                    const float A = expf(__ldg(a.logits + si) - st.x) * st.y;
-                    __stcs(a.grad_attn + si, A * (a.grad_attn[si] - tot[it]));
+                    float A, dot;
+                    if (OPTS && dm.per_level_softmax) {
+                        const int l = a.level_of[r0 + j];
+                        float mx, inv;
+                        group_softmax_stats(a.logits + (si - (r0 + j)) + (size_t)l * dm.K, dm.K, mx, inv);
+                        A = expf(__ldg(a.logits + si) - mx) * inv;
+                        dot = sm.gdot[hh][l];
+                    } else {
+                        const float2 st = sm.stat[hh];
+                        A = expf(__ldg(a.logits + si) - st.x) * st.y;
+                        dot = tot[it];
+                    }
+                    // own write: the plain load sees it (per-level groups read L2 above)
+                    __stcs(a.grad_attn + si, A * (a.grad_attn[si] - dot));
                 }
             }
         }
@@ -490,19 +542,19 @@ struct BwdIO {
     float *grad_value, *grad_loc, *grad_attn, *grad_ref;
 };
 
-template <typename T, int D, bool FUSED>
+template <typename T, int D, bool FUSED, bool OPTS>
 static void launch_bwd_kernel(const BwdArgs &a, bool det, unsigned blocks, cudaStream_t stream) {
     constexpr int HW = 32 / (D / 4);
     constexpr int B = kWarpsPerBlock * 32;
     const bool merge = a.merge_mask != 0;
     if constexpr (HW == 4) {
-        if (det && merge) msda_backward_kernel<T, D, true, true, FUSED><<<blocks, B, 0, stream>>>(a);
-        else if (det) msda_backward_kernel<T, D, true, false, FUSED><<<blocks, B, 0, stream>>>(a);
-        else if (merge) msda_backward_kernel<T, D, false, true, FUSED><<<blocks, B, 0, stream>>>(a);
-        else msda_backward_kernel<T, D, false, false, FUSED><<<blocks, B, 0, stream>>>(a);
+        if (det && merge) msda_backward_kernel<T, D, true, true, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
+        else if (det) msda_backward_kernel<T, D, true, false, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
+        else if (merge) msda_backward_kernel<T, D, false, true, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
+        else msda_backward_kernel<T, D, false, false, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
     } else {
-        if (det) msda_backward_kernel<T, D, true, false, FUSED><<<blocks, B, 0, stream>>>(a);
-        else msda_backward_kernel<T, D, false, false, FUSED><<<blocks, B, 0, stream>>>(a);
+        if (det) msda_backward_kernel<T, D, true, false, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
+        else msda_backward_kernel<T, D, false, false, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
     }
 }
 
@@ -544,7 +596,11 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
     }
     if (g.d.rows > 0) {
         const long long tasks = (long long)g.d.N * a.qblocks * g.d.M;
-        launch_bwd_kernel<T, D, FUSED>(a, det, (unsigned)((tasks + kWarpsPerBlock - 1) / kWarpsPerBlock), stream);
+        const unsigned blocks = (unsigned)((tasks + kWarpsPerBlock - 1) / kWarpsPerBlock);
+        if (FUSED && (g.d.per_level_softmax || g.lv.shift != 0.5f))
+            launch_bwd_kernel<T, D, FUSED, true>(a, det, blocks, stream);
+        else
+            launch_bwd_kernel<T, D, FUSED, false>(a, det, blocks, stream);
         if (FUSED) {
             const int nql = g.d.N * g.d.Len_q * g.d.L;
             ref_grad_kernel<<<grid_for(nql, 256), 256, 0, stream>>>(io.grad_loc, io.grad_ref, nql, g.d.M, g.d.L,

@@ -27,10 +27,16 @@ struct LevelTable {
     int start[kMaxLevels];     // first value row of the level
     float Hf[kMaxLevels];
     float Wf[kMaxLevels];
+    float Sx[kMaxLevels];      // pixel scale: W (W - 1 with align_corners)
+    float Sy[kMaxLevels];      // H (H - 1 with align_corners)
+    float Rx[kMaxLevels];      // offset pixels to pixel coordinate: Sx / W (fp32)
+    float Ry[kMaxLevels];      // Sy / H
+    float shift;               // 0.5 (0 with align_corners)
 };
 
 struct Dims {
     int N, Len_in, M, Len_q, L, K;
+    int per_level_softmax;     // fused calls: softmax over each level's K logits
     int P;          // L * K samples per row
     int rows;       // N * Len_q * M rows (one row = one (n, q, m))
     int qm;         // Len_q * M rows per batch element
@@ -131,25 +137,29 @@ __device__ __forceinline__ void load_row_f32(const T *p, float (&g)[V]) {
 }
 
 // ---- pixel coordinates ------------------------------------------------------
-// Unfused: px = x * size - 0.5.  The floor is taken of RN(RN(x*size) - 0.5);
-// the fraction adds back the exact rounding error of the product (fma), so it
-// is accurate to about 1e-7 px instead of half an ulp of px.
-__device__ __forceinline__ void pixel_coord(float x, float size, float &fl, float &frac) {
-    float p = __fmul_rn(x, size);
-    float e = __fmaf_rn(x, size, -p);          // x*size = p + e exactly
-    float ph = __fsub_rn(p, 0.5f);
+// Unfused: px = x * S - shift (S = W, shift = 0.5; with align_corners S = W - 1,
+// shift = 0).  The floor is taken of RN(RN(x*S) - shift); the fraction adds
+// back the exact rounding error of the product (fma), so it is accurate to
+// about 1e-7 px instead of half an ulp of px.
+__device__ __forceinline__ void pixel_coord(float x, float S, float shift, float &fl, float &frac) {
+    float p = __fmul_rn(x, S);
+    float e = __fmaf_rn(x, S, -p);             // x*S = p + e exactly
+    float ph = __fsub_rn(p, shift);
     fl = floorf(ph);
     frac = __fadd_rn(__fsub_rn(ph, fl), e);
 }
 
-// Fused: px = ref * size + off - 0.5 (= (ref + off/size) * size - 0.5).  The
-// floor is taken of RN(RN(ref*size) + RN(off - 0.5)); the fraction carries the
-// rounding errors of all three operations (fma and two-sum).
+// Fused: px = ref * S + off * Rr - shift, the same point as (ref + off / W) * S
+// - shift with Rr = S / W (1 without align_corners).  The floor is taken of
+// RN(RN(ref*S) + RN(RN(off*Rr) - shift)); the fraction carries the rounding
+// errors of every operation (fma and two-sum).
 __device__ __forceinline__ float two_sum_err(float a, float b, float s) {
     float bb = __fsub_rn(s, a);
     return __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+// Default convention (S = size, Rr = 1, shift = 0.5): RN(RN(ref*size) + RN(off - 0.5)),
+// three roundings.
 __device__ __forceinline__ void pixel_coord_fused(float ref, float off, float size, float &fl, float &frac) {
     float p = __fmul_rn(ref, size);
     float e1 = __fmaf_rn(ref, size, -p);
@@ -159,6 +169,33 @@ __device__ __forceinline__ void pixel_coord_fused(float ref, float off, float si
     float e3 = two_sum_err(p, t, s);
     fl = floorf(s);
     frac = __fadd_rn(__fsub_rn(s, fl), __fadd_rn(e1, __fadd_rn(e2, e3)));
+}
+
+// Any convention; for the default one it gives the same floor and fraction as
+// the function above (off * 1 and its error term 0 are exact).
+__device__ __forceinline__ void pixel_coord_fused(float ref, float off, float S, float Rr, float shift, float &fl,
+                                                  float &frac) {
+    float p = __fmul_rn(ref, S);
+    float e1 = __fmaf_rn(ref, S, -p);
+    float t0 = __fmul_rn(off, Rr);
+    float ea = __fmaf_rn(off, Rr, -t0);
+    float t = __fsub_rn(t0, shift);
+    float eb = two_sum_err(t0, -shift, t);
+    float s = __fadd_rn(p, t);
+    float e3 = two_sum_err(p, t, s);
+    fl = floorf(s);
+    frac = __fadd_rn(__fsub_rn(s, fl), __fadd_rn(e1, __fadd_rn(ea, __fadd_rn(eb, e3))));
+}
+
+// Attention weight of sample k of a softmax group of n logits at lg (max
+// subtracted, then a multiply by 1/sum): one fixed order, so every kernel that
+// calls it gets the same value.
+__device__ __forceinline__ void group_softmax_stats(const float *lg, int n, float &mx, float &inv) {
+    mx = -INFINITY;
+    for (int i = 0; i < n; ++i) mx = fmaxf(mx, __ldg(lg + i));
+    float sum = 0.f;
+    for (int i = 0; i < n; ++i) sum += expf(__ldg(lg + i) - mx);
+    inv = 1.f / sum;
 }
 
 // One sample's four corners: element offsets (relative to the row's value

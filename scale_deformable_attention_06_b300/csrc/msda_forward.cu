@@ -34,9 +34,12 @@ struct FwdArgs {
     Dims d;
     LevelTable lv;
     unsigned char level_of[kMaxSamples];   // level of sample s = l*K + k
+    int opts;                              // any option bit set
 };
 
-template <typename T, int D, bool FUSED>
+// OPTS: the problem sets option bits (fused calls); without them the kernel
+// carries none of the option code.
+template <typename T, int D, bool FUSED, bool OPTS>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 msda_forward_kernel(const __grid_constant__ FwdArgs a) {
     using Lay = Layout<T, D>;
@@ -53,7 +56,7 @@ msda_forward_kernel(const __grid_constant__ FwdArgs a) {
     if (row0 >= dm.rows) return;
     const int P = dm.P;
 
-    if constexpr (FUSED) {
+    if (FUSED && !(OPTS && a.d.per_level_softmax)) {
         // softmax statistics of each row: max and 1/sum of exp(logit - max)
         for (int h = 0; h < HW; ++h) {
             const int row = row0 + h;
@@ -101,14 +104,24 @@ msda_forward_kernel(const __grid_constant__ FwdArgs a) {
                     const int nq = r / dm.M;            // (n, q) of this row
                     const float2 rf = __ldg(reinterpret_cast<const float2 *>(a.ref) + (size_t)nq * dm.L + l);
                     const float2 of = load_stream2(a.off + 2 * si);
-                    pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
-                    pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
-                    const float2 st = s_stat[warp][hh];
+                    float2 st;
+                    if constexpr (OPTS) {
+                        pixel_coord_fused(rf.x, of.x, a.lv.Sx[l], a.lv.Rx[l], a.lv.shift, x0, fx);
+                        pixel_coord_fused(rf.y, of.y, a.lv.Sy[l], a.lv.Ry[l], a.lv.shift, y0, fy);
+                        if (dm.per_level_softmax)       // the level's K logits are this sample's group
+                            group_softmax_stats(a.logits + (size_t)r * P + l * dm.K, dm.K, st.x, st.y);
+                        else
+                            st = s_stat[warp][hh];
+                    } else {
+                        pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
+                        pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
+                        st = s_stat[warp][hh];
+                    }
                     A = expf(load_stream1(a.logits + si) - st.x) * st.y;
                 } else {
                     const float2 lc = load_stream2(a.loc + 2 * si);
-                    pixel_coord(lc.x, Wf, x0, fx);
-                    pixel_coord(lc.y, Hf, y0, fy);
+                    pixel_coord(lc.x, a.lv.Sx[l], a.lv.shift, x0, fx);
+                    pixel_coord(lc.y, a.lv.Sy[l], a.lv.shift, y0, fy);
                     A = load_stream1(a.attn + si);
                 }
                 Corners c = make_corners(x0, fx, y0, fy, a.lv.W[l], a.lv.H[l], Wf, Hf, a.lv.start[l], dm.pix);
@@ -143,7 +156,10 @@ static cudaError_t launch_fwd(const FwdArgs &args, cudaStream_t stream) {
     constexpr int HW = Layout<T, D>::HW;
     const long long warps = ((long long)args.d.rows + HW - 1) / HW;
     const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    msda_forward_kernel<T, D, FUSED><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    if (FUSED && args.opts)
+        msda_forward_kernel<T, D, FUSED, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    else
+        msda_forward_kernel<T, D, FUSED, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
     return cudaGetLastError();
 }
 
@@ -170,6 +186,7 @@ static cudaError_t dispatch_fwd(const FwdArgs &args, int dtype, int D, cudaStrea
 static void fill_common(FwdArgs &fa, const LaunchGeometry &g) {
     fa.d = g.d;
     fa.lv = g.lv;
+    fa.opts = g.d.per_level_softmax || g.lv.shift != 0.5f;
     for (int s = 0; s < kMaxSamples; ++s) fa.level_of[s] = g.level_of[s];
 }
 

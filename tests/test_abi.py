@@ -77,6 +77,7 @@ FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails i
     (dict(), [8, 0, 4, 4], [0, 0], 1),
     (dict(N=-1), [8, 8, 4, 4], [0, 64], 1),
     (dict(n_heads=0), [8, 8, 4, 4], [0, 64], 1),
+    (dict(options=4), [8, 8, 4, 4], [0, 64], 1),
 ])
 def test_host_checks_reject_before_launch(msda, kw, shapes, starts, expect):
     p = _problem(msda, **kw)

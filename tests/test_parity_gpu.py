@@ -305,3 +305,56 @@ def test_fused_backward_dense_merge_and_accumulate(msda):
                                  H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]),
                                  H.dev(p["attention_logits"]), H.dev(p["grad_output"]), grad_value=gv, flags=flags)
         H.assert_bwd(gv.cpu().numpy(), gv0 + ref[0], "f32", "fused accumulated grad_value")
+
+
+# ----------------------------------------------------------------- options (per-level softmax, align_corners)
+OPT_CASES = [("per_level", 1), ("align", 2), ("both", 3)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("D", [8, 32])
+@pytest.mark.parametrize("oname,opt", OPT_CASES, ids=[c[0] for c in OPT_CASES])
+def test_options_all_calls(msda, dtype, D, oname, opt):
+    """Every call under each option, against the oracle with the same option.
+    L*K = 35 with K = 7: levels straddle the record chunks of the backward."""
+    levels = [(5, 7), (3, 4), (1, 1), (6, 2), (2, 3)]
+    w = workloads.custom(N=2, M=3, D=D, levels=levels, K=7, Len_q=27, dtype=dtype, refs="uniform",
+                         ref_range=(-0.05, 1.05), offset_sigma=0.2, seed=900 + D + opt)
+    p = H.prepared(w)
+    dt = H.storage_dtype(w)
+    v, g = H.dev(p["value"], dt), H.dev(p["grad_output"], dt)
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+    ref, off, lg = H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]), H.dev(p["attention_logits"])
+    loc, attn = H.dev(p["sampling_locations"]), H.dev(p["attention_weights"])
+    # unfused calls (the per-level bit has no effect there)
+    out = msda.msda_forward(v, sh, st, loc, attn, options=opt).float().cpu().numpy()
+    H.assert_fwd(out, oracle.forward(p["value"], sh, st, p["sampling_locations"], p["attention_weights"],
+                                     options=opt), dtype, f"{oname} forward")
+    ref_b = oracle.backward(p["value"], sh, st, p["sampling_locations"], p["attention_weights"], p["grad_output"],
+                            options=opt)
+    for flags in (0, msda.MSDA_DETERMINISTIC):
+        got = msda.msda_backward(v, sh, st, loc, attn, g, flags=flags, options=opt)
+        _check_backward(w, [t.cpu().numpy() for t in got], ref_b)
+    # fused calls
+    fo = msda.msda_forward_fused(v, sh, st, ref, off, lg, options=opt).float().cpu().numpy()
+    H.assert_fwd(fo, oracle.forward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
+                                          p["attention_logits"], options=opt), dtype, f"{oname} fused forward")
+    ref_fb = oracle.backward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
+                                   p["attention_logits"], p["grad_output"], options=opt)
+    for flags in (0, msda.MSDA_DETERMINISTIC):
+        got = msda.msda_backward_fused(v, sh, st, ref, off, lg, g, flags=flags, options=opt)
+        _check_backward_fused(w, [t.cpu().numpy() for t in got], ref_fb)
+
+
+def test_options_dense_merge_path(msda):
+    """Both options on dense small maps (merge table on every level)."""
+    w = workloads.custom(N=1, M=2, D=32, levels=[(4, 6), (2, 3)], K=4, Len_q=203, refs="uniform",
+                         ref_range=(0.0, 1.0), offset_sigma=0.15, seed=811)
+    p = H.prepared(w)
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+    got = msda.msda_backward_fused(H.dev(p["value"]), sh, st, H.dev(p["reference_points"]),
+                                   H.dev(p["sampling_offsets"]), H.dev(p["attention_logits"]),
+                                   H.dev(p["grad_output"]), options=3)
+    ref = oracle.backward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
+                                p["attention_logits"], p["grad_output"], options=3)
+    _check_backward_fused(w, [t.cpu().numpy() for t in got], ref)
