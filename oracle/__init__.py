@@ -32,8 +32,11 @@ def bind(path):
     lib.msda_oracle_forward_fused.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, i64]
     lib.msda_oracle_backward.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, i64]
     lib.msda_oracle_backward_fused.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, dp, dp, i64]
+    lib.msda_oracle_forward3d.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, i64]
+    lib.msda_oracle_backward3d.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, i64]
     for f in ("msda_oracle_locations", "msda_oracle_softmax", "msda_oracle_forward",
-              "msda_oracle_forward_fused", "msda_oracle_backward", "msda_oracle_backward_fused"):
+              "msda_oracle_forward_fused", "msda_oracle_backward", "msda_oracle_backward_fused",
+              "msda_oracle_forward3d", "msda_oracle_backward3d"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -175,3 +178,40 @@ def backward_fused(value, spatial_shapes, level_start_index, reference_points, s
            "backward_fused")
     return gv, gr, go, gl
 
+
+
+def forward3d(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, options=0):
+    """3-D variant, a3-a5 with trilinear sampling.  spatial_shapes [L,3] = (D,H,W),
+    sampling_locations [N,Lq,M,L,K,3] (x,y,z).  Returns output [N, Len_q, M*D]."""
+    lib = _load()
+    v, vp = _d(value)
+    sh, shp = _l(np.asarray(spatial_shapes).reshape(-1, 3))
+    st, stp = _l(level_start_index)
+    loc, locp = _d(sampling_locations)
+    a, ap = _d(attention_weights)
+    N, S, M, D = v.shape
+    Lq, L, K = loc.shape[1], sh.shape[0], loc.shape[4]
+    out = np.zeros((N, Lq, M * D))
+    _check(lib.msda_oracle_forward3d(N, S, M, D, Lq, L, K, vp, shp, stp, locp, ap, _d(out)[1], options),
+           "forward3d")
+    return out
+
+
+def backward3d(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, grad_output,
+               options=0):
+    """3-D variant of a6-a8.  Returns (grad_value, grad_loc [..,3], grad_attn)."""
+    lib = _load()
+    v, vp = _d(value)
+    sh, shp = _l(np.asarray(spatial_shapes).reshape(-1, 3))
+    st, stp = _l(level_start_index)
+    loc, locp = _d(sampling_locations)
+    a, ap = _d(attention_weights)
+    g, gp = _d(grad_output)
+    N, S, M, D = v.shape
+    Lq, L, K = loc.shape[1], sh.shape[0], loc.shape[4]
+    gv = np.zeros(v.shape)
+    gl = np.zeros(loc.shape)
+    ga = np.zeros(a.shape)
+    _check(lib.msda_oracle_backward3d(N, S, M, D, Lq, L, K, vp, shp, stp, locp, ap, gp,
+                                      _d(gv)[1], _d(gl)[1], _d(ga)[1], options), "backward3d")
+    return gv, gl, ga

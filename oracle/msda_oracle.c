@@ -456,3 +456,136 @@ done:
     free(gattn);
     return rc;
 }
+
+/* ========================================================================= */
+/* The 3-D (volumetric / temporal) variant: "可变形注意力…" §5.3 -- on voxel */
+/* or video features the offsets gain a z (or time) component and bilinear   */
+/* interpolation becomes trilinear; everything else is as in 2-D.  Readings: */
+/* a level is a volume (D_l, H_l, W_l) flattened as start + (z*H + y)*W + x; */
+/* locations are (x, y, z) in [0,1]; pz = z*D - 0.5 (z*(D-1) with            */
+/* align_corners); a corner outside the volume contributes 0.                */
+/*   value [N][Len_in][n_heads][head_dim], spatial_shapes [L][3] = (D, H, W), */
+/*   sampling_locations [N][Len_q][n_heads][L][K][3], output as in 2-D.       */
+/* ========================================================================= */
+typedef struct {
+    int64_t row[8];     /* value row of corner c (or -1 outside); c = 4*k + 2*j + i */
+    double w[8];        /* trilinear weight of corner c */
+    double f[3];        /* fx, fy, fz */
+} corners3_t;
+
+static void corners3(const double *loc, int64_t Dd, int64_t H, int64_t W, int64_t start, int align, corners3_t *c)
+{
+    int64_t size[3] = {W, H, Dd};
+    int64_t i0[3];
+    double p[3];
+    for (int a = 0; a < 3; ++a) {
+        i0[a] = decide_floor_unfused(loc[a], size[a], align);
+        p[a] = align ? loc[a] * (double)(size[a] - 1) : loc[a] * (double)size[a] - 0.5;
+        c->f[a] = p[a] - (double)i0[a];
+    }
+    for (int k = 0; k < 2; ++k)
+        for (int j = 0; j < 2; ++j)
+            for (int i = 0; i < 2; ++i) {
+                int ci = 4 * k + 2 * j + i;
+                int64_t xc = i0[0] + i, yc = i0[1] + j, zc = i0[2] + k;
+                c->w[ci] = (i ? c->f[0] : 1.0 - c->f[0]) * (j ? c->f[1] : 1.0 - c->f[1]) * (k ? c->f[2] : 1.0 - c->f[2]);
+                c->row[ci] = (xc >= 0 && xc < W && yc >= 0 && yc < H && zc >= 0 && zc < Dd)
+                                 ? start + (zc * H + yc) * W + xc : -1;
+            }
+}
+
+static int check_levels3(int64_t Len_in, int64_t n_levels, const int64_t *shapes, const int64_t *starts)
+{
+    int64_t expect = 0;
+    for (int64_t l = 0; l < n_levels; ++l) {
+        if (shapes[3 * l] <= 0 || shapes[3 * l + 1] <= 0 || shapes[3 * l + 2] <= 0) return -1;
+        if (starts[l] != expect) return -1;
+        expect += shapes[3 * l] * shapes[3 * l + 1] * shapes[3 * l + 2];
+    }
+    return expect == Len_in ? 0 : -1;
+}
+
+int msda_oracle_forward3d(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
+                          int64_t n_levels, int64_t n_points, const double *value,
+                          const int64_t *spatial_shapes, const int64_t *level_start_index,
+                          const double *sampling_locations, const double *attention_weights,
+                          double *output, int64_t options)
+{
+    if (N < 0 || Len_in < 0 || n_heads <= 0 || D <= 0 || Len_q < 0 || n_levels <= 0 || n_points <= 0)
+        return -1;
+    if (check_levels3(Len_in, n_levels, spatial_shapes, level_start_index)) return -1;
+    int align = (options & OPT_ALIGN_CORNERS) != 0;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t q = 0; q < Len_q; ++q)
+            for (int64_t m = 0; m < n_heads; ++m) {
+                double *o = output + ((n * Len_q + q) * n_heads + m) * D;
+                for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+                for (int64_t l = 0; l < n_levels; ++l) {
+                    const int64_t *sh = spatial_shapes + 3 * l;
+                    for (int64_t k = 0; k < n_points; ++k) {
+                        int64_t s = (((n * Len_q + q) * n_heads + m) * n_levels + l) * n_points + k;
+                        corners3_t c;
+                        corners3(sampling_locations + 3 * s, sh[0], sh[1], sh[2], level_start_index[l], align, &c);
+                        for (int ci = 0; ci < 8; ++ci) {
+                            if (c.row[ci] < 0) continue;
+                            const double *v = value + ((n * Len_in + c.row[ci]) * n_heads + m) * D;
+                            for (int64_t d = 0; d < D; ++d) o[d] += attention_weights[s] * c.w[ci] * v[d];
+                        }
+                    }
+                }
+            }
+    return 0;
+}
+
+/* Backward of the 3-D forward.  For corner c = (i, j, k) the weight is
+ * u_x(i) u_y(j) u_z(k) with u(0) = 1 - f, u(1) = f, so d w_c / d f_x =
+ * (i ? 1 : -1) u_y(j) u_z(k), and likewise for y and z. */
+int msda_oracle_backward3d(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
+                           int64_t n_levels, int64_t n_points, const double *value,
+                           const int64_t *spatial_shapes, const int64_t *level_start_index,
+                           const double *sampling_locations, const double *attention_weights,
+                           const double *grad_output, double *grad_value,
+                           double *grad_sampling_locations, double *grad_attention_weights, int64_t options)
+{
+    if (N < 0 || Len_in < 0 || n_heads <= 0 || D <= 0 || Len_q < 0 || n_levels <= 0 || n_points <= 0)
+        return -1;
+    if (check_levels3(Len_in, n_levels, spatial_shapes, level_start_index)) return -1;
+    int align = (options & OPT_ALIGN_CORNERS) != 0;
+    for (int64_t i = 0; i < N * Len_in * n_heads * D; ++i) grad_value[i] = 0.0;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t q = 0; q < Len_q; ++q)
+            for (int64_t m = 0; m < n_heads; ++m) {
+                const double *g = grad_output + ((n * Len_q + q) * n_heads + m) * D;
+                for (int64_t l = 0; l < n_levels; ++l) {
+                    const int64_t *sh = spatial_shapes + 3 * l;
+                    double scale[3] = {(double)(align ? sh[2] - 1 : sh[2]), (double)(align ? sh[1] - 1 : sh[1]),
+                                       (double)(align ? sh[0] - 1 : sh[0])};
+                    for (int64_t k = 0; k < n_points; ++k) {
+                        int64_t s = (((n * Len_q + q) * n_heads + m) * n_levels + l) * n_points + k;
+                        corners3_t c;
+                        corners3(sampling_locations + 3 * s, sh[0], sh[1], sh[2], level_start_index[l], align, &c);
+                        double ga = 0.0, gd[3] = {0.0, 0.0, 0.0};
+                        for (int ci = 0; ci < 8; ++ci) {
+                            if (c.row[ci] < 0) continue;     /* outside: value 0 */
+                            const double *v = value + ((n * Len_in + c.row[ci]) * n_heads + m) * D;
+                            double gv = 0.0;
+                            for (int64_t d = 0; d < D; ++d) gv += g[d] * v[d];
+                            int bit[3] = {ci & 1, (ci >> 1) & 1, (ci >> 2) & 1};
+                            ga += c.w[ci] * gv;
+                            for (int a = 0; a < 3; ++a) {
+                                double dw = bit[a] ? 1.0 : -1.0;
+                                for (int b = 0; b < 3; ++b)
+                                    if (b != a) dw *= bit[b] ? c.f[b] : 1.0 - c.f[b];
+                                gd[a] += dw * gv;
+                            }
+                            double *gvp = grad_value + ((n * Len_in + c.row[ci]) * n_heads + m) * D;
+                            for (int64_t d = 0; d < D; ++d) gvp[d] += attention_weights[s] * c.w[ci] * g[d];
+                        }
+                        grad_attention_weights[s] = ga;
+                        for (int a = 0; a < 3; ++a)
+                            grad_sampling_locations[3 * s + a] = attention_weights[s] * gd[a] * scale[a];
+                    }
+                }
+            }
+    return 0;
+}

@@ -34,6 +34,10 @@ What pins what:
                       whole-row softmax); with one level it equals the whole-row
                       softmax; finite differences of the fused backward and
                       zero-sum logit gradients per level.
+  trilinear_*         the 3-D variant: torch grid_sample on 5-D volumes (trilinear,
+                      zeros, both align_corners settings) forward and autograd in
+                      float64; one-slice volumes sampled at their centre plane
+                      give the 2-D result; finite differences.
 """
 import math
 import os
@@ -520,6 +524,96 @@ def pin_options_fused_backward():
     return worst, 1e-6
 
 
+# --------------------------------------------------------------------------- 3-D variant
+def _vol_inputs(seed, levels, N=1, Lq=9, M=2, K=3, D=4, lo=-0.2, hi=1.2):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shapes = np.asarray(levels, dtype=np.int64).reshape(-1, 3)
+    sizes = shapes.prod(-1)
+    starts = np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(np.int64)
+    S = int(sizes.sum())
+    L = len(levels)
+    value = rng.standard_normal((N, S, M, D))
+    loc = rng.uniform(lo, hi, size=(N, Lq, M, L, K, 3))
+    attn = rng.standard_normal((N, Lq, M, L, K))
+    g = rng.standard_normal((N, Lq, M * D))
+    return dict(shapes=shapes, starts=starts, value=value, loc=loc, attn=attn, g=g)
+
+
+def _grid_sample_3d(value, shapes, starts, loc, attn, align_corners):
+    """Per-level 5-D grid_sample (trilinear) in float64 torch."""
+    N, S, M, D = value.shape
+    _, Lq, _, L, K, _ = loc.shape
+    out = 0
+    for l in range(L):
+        Dd, H, W = (int(x) for x in shapes[l])
+        s0 = int(starts[l])
+        v_l = value[:, s0:s0 + Dd * H * W].reshape(N, Dd, H, W, M, D).permute(0, 4, 5, 1, 2, 3).reshape(N * M, D, Dd, H, W)
+        grid = (2.0 * loc[:, :, :, l] - 1.0).permute(0, 2, 1, 3, 4).reshape(N * M, Lq, K, 1, 3)
+        smp = F.grid_sample(v_l, grid, mode="bilinear", padding_mode="zeros", align_corners=align_corners)
+        a = attn[:, :, :, l].permute(0, 2, 1, 3).reshape(N * M, 1, Lq, K, 1)
+        out = out + (smp * a).sum((-1, -2))
+    return out.reshape(N, M, D, Lq).permute(0, 3, 1, 2).reshape(N, Lq, M * D)
+
+
+def pin_trilinear_grid_sample():
+    worst = 0.0
+    for seed, lv, opt in [(51, ((3, 4, 5), (2, 2, 3)), 0), (52, ((4, 3, 6), (1, 2, 2), (2, 5, 1)), 0),
+                          (53, ((3, 4, 5), (2, 3, 2)), AL)]:
+        t = _vol_inputs(seed, lv)
+        out = oracle.forward3d(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"], options=opt)
+        ref = _grid_sample_3d(torch.from_numpy(t["value"]), t["shapes"], t["starts"], torch.from_numpy(t["loc"]),
+                              torch.from_numpy(t["attn"]), align_corners=bool(opt & AL)).numpy()
+        worst = max(worst, _err(out, ref))
+    return worst, 1e-12
+
+
+def pin_trilinear_one_slice():
+    """A one-slice volume sampled at its centre plane (pz = 0) is the 2-D map."""
+    lv2 = ((5, 6), (3, 4))
+    t = _tiny(seed=54, levels=lv2, Lq=12, K=3, M=2, D=4)
+    shapes3 = np.asarray([[1, h, w] for (h, w) in lv2], dtype=np.int64)
+    loc3 = np.concatenate([t["loc"], np.full(t["loc"].shape[:-1] + (1,), 0.5)], axis=-1)
+    out3 = oracle.forward3d(t["value"], shapes3, t["starts"], loc3, t["attn"])
+    out2 = oracle.forward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"])
+    return _err(out3, out2), 1e-12
+
+
+def pin_trilinear_backward():
+    worst = 0.0
+    for seed, opt in ((55, 0), (56, AL)):
+        t = _vol_inputs(seed, ((3, 4, 5), (2, 3, 2)), Lq=7)
+        v = torch.from_numpy(t["value"]).requires_grad_(True)
+        loc = torch.from_numpy(t["loc"]).requires_grad_(True)
+        a = torch.from_numpy(t["attn"]).requires_grad_(True)
+        out = _grid_sample_3d(v, t["shapes"], t["starts"], loc, a, align_corners=bool(opt & AL))
+        out.backward(torch.from_numpy(t["g"]))
+        gv, gl, ga = oracle.backward3d(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"], t["g"], options=opt)
+        worst = max(worst, _rel(gv, v.grad.numpy()), _rel(gl, loc.grad.numpy()), _rel(ga, a.grad.numpy()))
+    return worst, 1e-12
+
+
+def pin_trilinear_fd():
+    """Central finite differences of the 3-D forward in the locations, away from the kinks."""
+    t = _vol_inputs(57, ((3, 4, 5), (2, 2, 3)), Lq=4, K=2, D=3, lo=-0.1, hi=1.1)
+    gv, gl, ga = oracle.backward3d(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"], t["g"])
+
+    def J(loc):
+        return float((oracle.forward3d(t["value"], t["shapes"], t["starts"], loc, t["attn"]) * t["g"]).sum())
+
+    h = 1e-6
+    worst = 0.0
+    for idx in np.ndindex(t["loc"].shape):
+        size = t["shapes"][idx[3]][2 - idx[5]]          # (D, H, W) against (x, y, z)
+        p = t["loc"][idx] * size - 0.5
+        if abs(p - round(p)) < 1e-3:
+            continue
+        pl, mi = t["loc"].copy(), t["loc"].copy()
+        pl[idx] += h
+        mi[idx] -= h
+        worst = max(worst, abs((J(pl) - J(mi)) / (2 * h) - gl[idx]) / (1 + abs(gl[idx])))
+    return worst, 1e-6
+
+
 ALL_PINS = {
     "worked_example": pin_worked_example,
     "softmax_closed": pin_softmax_closed,
@@ -539,6 +633,10 @@ ALL_PINS = {
     "align_backward_autograd": pin_align_backward_autograd,
     "per_level_closed": pin_per_level_closed,
     "options_fused_backward": pin_options_fused_backward,
+    "trilinear_grid_sample": pin_trilinear_grid_sample,
+    "trilinear_one_slice": pin_trilinear_one_slice,
+    "trilinear_backward": pin_trilinear_backward,
+    "trilinear_fd": pin_trilinear_fd,
 }
 
 

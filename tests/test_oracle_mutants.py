@@ -43,6 +43,11 @@ MUTANTS = [
     ("fused_grad_offset_scaled_wrong", "gloc[2 * s + 0] / W;", "gloc[2 * s + 0] * W;"),
     ("softmax_grad_missing_dot", "(gattn[r * cols + j] - dot)", "(gattn[r * cols + j])"),
     ("grad_ref_not_summed", "gref[0] += gloc[2 * s + 0];", "gref[0] = gloc[2 * s + 0];"),
+    ("trilinear_drops_z_weight", "* (k ? c->f[2] : 1.0 - c->f[2]);", ";"),
+    ("trilinear_z_stride", "start + (zc * H + yc) * W + xc", "start + (zc * W + yc) * W + xc"),
+    ("trilinear_z_bound", "zc >= 0 && zc < Dd)", "zc >= 0 && zc <= Dd)"),
+    ("trilinear_grad_z_scale", "(double)(align ? sh[0] - 1 : sh[0])};", "(double)(align ? sh[1] - 1 : sh[1])};"),
+    ("trilinear_grad_sign", "double dw = bit[a] ? 1.0 : -1.0;", "double dw = bit[a] ? -1.0 : 1.0;"),
 ]
 
 
