@@ -265,6 +265,36 @@ MSDA_API msda_status msda_backward_noalloc(const msda_problem *problem, const vo
                                            float *grad_sampling_locations, float *grad_attention_weights,
                                            unsigned flags, void *stream);
 
+/*
+ * msda3d_forward / msda3d_backward -- the 3-D (volumetric or temporal)
+ * variant: "可变形注意力…" §5.3, sampling points on voxel or video features,
+ * offsets with a z (time) component, trilinear in place of bilinear
+ * interpolation, the rest as msda_forward / msda_backward.
+ *
+ *   spatial_shapes      in   host [L][3] = (D_l, H_l, W_l); Len_in = sum D*H*W,
+ *                            a level flattened z-major: row start + (z*H + y)*W + x
+ *   sampling_locations  in   [N][Len_q][M][L][K][3] f32, (x, y, z) normalised
+ *   attention_weights   in   [N][Len_q][M][L][K] f32 (as given)
+ *   output              out  [N][Len_q][M*D], dtype
+ *   grad_sampling_locations out [N][Len_q][M][L][K][3] f32
+ *   the rest            as msda_forward / msda_backward (same workspace size)
+ * pz = z * D_l - 0.5 (z * (D_l - 1) with MSDA_OPT_ALIGN_CORNERS), and likewise
+ * x, y; each of the eight neighbours outside the volume contributes zero.
+ * Locations and weights need 4-byte alignment; value, output, grad_output and
+ * grad_value 16 bytes.  Len_in must stay below 2^28 and Len_in * M * D below 2^31.
+ */
+MSDA_API msda_status msda3d_forward(const msda_problem *problem, const void *value,
+                                    const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                    const float *sampling_locations, const float *attention_weights,
+                                    void *output, void *stream);
+
+MSDA_API msda_status msda3d_backward(const msda_problem *problem, const void *value,
+                                     const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                     const float *sampling_locations, const float *attention_weights,
+                                     const void *grad_output, float *grad_value, float *grad_sampling_locations,
+                                     float *grad_attention_weights, unsigned flags, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
 /* Name of a status code (static string). */
 MSDA_API const char *msda_status_string(msda_status status);
 

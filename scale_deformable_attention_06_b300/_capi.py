@@ -23,8 +23,8 @@ MSDA_OPT_PER_LEVEL_SOFTMAX = 1
 MSDA_OPT_ALIGN_CORNERS = 2
 
 EXPORTED = ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_fused",
-            "msda_backward_workspace_size", "msda_backward_noalloc", "msda_status_string", "msda_last_error",
-            "msda_version")
+            "msda_backward_workspace_size", "msda_backward_noalloc", "msda3d_forward", "msda3d_backward",
+            "msda_status_string", "msda_last_error", "msda_version")
 
 
 class MSDAError(RuntimeError):
@@ -52,10 +52,13 @@ def _load():
     lib.msda_backward_fused.argtypes = [pp, vp, i64p, i64p, fp, fp, fp, vp, fp, fp, fp, fp, ctypes.c_uint, vp,
                                         ctypes.c_size_t, vp]
     lib.msda_backward_noalloc.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, fp, fp, fp, ctypes.c_uint, vp]
+    lib.msda3d_forward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, vp]
+    lib.msda3d_backward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, fp, fp, fp, ctypes.c_uint, vp, ctypes.c_size_t, vp]
     lib.msda_backward_noalloc.restype = ctypes.c_int
     lib.msda_backward_workspace_size.argtypes = [pp, ctypes.c_uint]
     lib.msda_backward_workspace_size.restype = ctypes.c_size_t
-    for f in ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_fused"):
+    for f in ("msda_forward", "msda_forward_fused", "msda_backward", "msda_backward_fused", "msda3d_forward",
+              "msda3d_backward"):
         getattr(lib, f).restype = ctypes.c_int
     lib.msda_status_string.argtypes = [ctypes.c_int]
     lib.msda_status_string.restype = ctypes.c_char_p
@@ -277,4 +280,69 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
                                       _dev(grad_sampling_locations, "grad_sampling_locations", torch.float32),
                                       _dev(grad_attention_weights, "grad_attention_weights", torch.float32),
                                       flags, _stream(stream, value.device)))
+    return grad_value, grad_sampling_locations, grad_attention_weights
+
+
+class _HostVolumes:
+    """spatial_shapes [L,3] = (D,H,W) and level_start_index [L] as host int64 arrays."""
+
+    def __init__(self, spatial_shapes, level_start_index):
+        sh = torch.as_tensor(spatial_shapes).detach().to("cpu", torch.int64).contiguous().reshape(-1, 3)
+        st = torch.as_tensor(level_start_index).detach().to("cpu", torch.int64).contiguous().reshape(-1)
+        self.sh, self.st = sh, st
+        self.L = sh.shape[0]
+        self.shp = ctypes.cast(sh.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+        self.stp = ctypes.cast(st.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+
+
+def msda3d_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, output=None,
+                   stream=None, options=0):
+    """3-D variant: out[N, Len_q, M*D] from value [N,Len_in,M,D], spatial_shapes [L,3] (D,H,W),
+    sampling_locations [N,Len_q,M,L,K,3] (x,y,z) and attention_weights [N,Len_q,M,L,K]."""
+    lv = _HostVolumes(spatial_shapes, level_start_index)
+    N, S, M, D = value.shape
+    if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != 3:
+        raise ValueError("sampling_locations must be [N, Len_q, M, L, K, 3]")
+    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
+    if tuple(attention_weights.shape) != (N, Lq, M, L, K) or L != lv.L:
+        raise ValueError("attention_weights / spatial_shapes disagree with sampling_locations")
+    if output is None:
+        output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
+    prob = problem(value, Lq, L, K, options)
+    _check(_lib.msda3d_forward(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
+                               _dev(sampling_locations, "sampling_locations", torch.float32),
+                               _dev(attention_weights, "attention_weights", torch.float32),
+                               _dev(output, "output"), _stream(stream, value.device)))
+    return output
+
+
+def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, grad_output,
+                    grad_value=None, grad_sampling_locations=None, grad_attention_weights=None, flags=0,
+                    workspace=None, stream=None, options=0):
+    """3-D variant of msda_backward.  Returns (grad_value, grad_sampling_locations [..,3], grad_attention_weights)."""
+    lv = _HostVolumes(spatial_shapes, level_start_index)
+    N, S, M, D = value.shape
+    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
+    if tuple(grad_output.shape) != (N, Lq, M * D) or grad_output.dtype != value.dtype:
+        raise ValueError("grad_output must be [N, Len_q, M*D] with the dtype of value")
+    dev = value.device
+    if grad_value is None:
+        grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)
+    if grad_sampling_locations is None:
+        grad_sampling_locations = torch.empty_like(sampling_locations)
+    if grad_attention_weights is None:
+        grad_attention_weights = torch.empty_like(attention_weights)
+    prob = problem(value, Lq, L, K, options)
+    need = int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.msda3d_backward(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
+                                _dev(sampling_locations, "sampling_locations", torch.float32),
+                                _dev(attention_weights, "attention_weights", torch.float32),
+                                _dev(grad_output, "grad_output"), _dev(grad_value, "grad_value", torch.float32),
+                                _dev(grad_sampling_locations, "grad_sampling_locations", torch.float32),
+                                _dev(grad_attention_weights, "grad_attention_weights", torch.float32),
+                                flags, ws_ptr, ws_bytes, _stream(stream, dev)))
     return grad_value, grad_sampling_locations, grad_attention_weights

@@ -1,0 +1,383 @@
+// msda3d.cu -- the 3-D (volumetric / temporal) variant of the MSDeformAttn
+// core.  "可变形注意力：多尺度稀疏采样与视觉检测实战解析" §5.3: on voxel or video
+// features the sampling offsets gain a z (time) component and bilinear
+// interpolation becomes trilinear; the rest is the 2-D method.
+//
+//   out[n][q][m*D+d] = sum_{l,k} A[n,q,m,l,k] * trilinear_l(value[n,:,m,d], loc[n,q,m,l,k])
+//
+// A level is a volume (Dz_l, H_l, W_l) flattened z-major: value row
+// start_l + (z*H_l + y)*W_l + x.  The pixel coordinate is px = x*W - shift
+// (likewise y, z; W - 1 and shift 0 with align_corners); the eight integer
+// neighbours are weighted u_x(i) u_y(j) u_z(k), u(0) = 1 - f, u(1) = f, and a
+// neighbour outside the volume contributes zero.
+//
+// Forward: the 2-D forward's decomposition (msda_forward.cu): a warp owns HW
+// rows (n, q, m), R lanes per row with 16 bytes of channels each; phase 1
+// stages one 32-byte corner record per (row, sample); phase 2 issues eight
+// 16-byte gathers per sample.  Backward: the 2-D backward's (msda_backward.cu):
+// a warp owns HW consecutive queries of one head, 4 channels per lane; per
+// sample the lane's partial grad_attn and d/dpx, d/dpy, d/dpz are summed over
+// the query's lanes by one reduce-scatter (the fourth slot carries d/dpz), and
+// A * w_c * g goes into grad_value by one vector reduction per corner.
+#include "msda_device.cuh"
+#include "msda_launch.h"
+
+namespace msda {
+
+// ---- 32-byte corner record ----------------------------------------------------
+// a.x  value row of corner 000 clamped into the volume (< 2^28)
+// a.y  validity bits: 1 x0, 2 x0+1, 4 y0, 8 y0+1, 16 z0, 32 z0+1 inside
+// a.z  fx   a.w  fy   b.x  fz   b.y  attention weight
+// Corners step from the clamped corner 000 by one column / row / slice only
+// when both neighbours along that axis are inside, so every address is
+// inside the volume and an inside corner keeps its true address.
+struct Rec3 {
+    uint4 a, b;
+};
+
+__device__ __forceinline__ Rec3 pack_record3(const float (&f0)[3], const float (&fr)[3], float A, int W, int H,
+                                             int Dz, float Wf, float Hf, float Dzf, int start) {
+    const int x0 = (int)fminf(fmaxf(f0[0], -2.f), Wf + 1.f);
+    const int y0 = (int)fminf(fmaxf(f0[1], -2.f), Hf + 1.f);
+    const int z0 = (int)fminf(fmaxf(f0[2], -2.f), Dzf + 1.f);
+    const uint32_t fl = ((unsigned)x0 < (unsigned)W ? 1u : 0u) | ((unsigned)(x0 + 1) < (unsigned)W ? 2u : 0u) |
+                        ((unsigned)y0 < (unsigned)H ? 4u : 0u) | ((unsigned)(y0 + 1) < (unsigned)H ? 8u : 0u) |
+                        ((unsigned)z0 < (unsigned)Dz ? 16u : 0u) | ((unsigned)(z0 + 1) < (unsigned)Dz ? 32u : 0u);
+    const int cx = min(max(x0, 0), W - 1), cy = min(max(y0, 0), H - 1), cz = min(max(z0, 0), Dz - 1);
+    Rec3 r;
+    r.a = make_uint4((uint32_t)(start + (cz * H + cy) * W + cx), fl, __float_as_uint(fr[0]), __float_as_uint(fr[1]));
+    r.b = make_uint4(__float_as_uint(fr[2]), __float_as_uint(A), 0u, 0u);
+    return r;
+}
+
+struct Unpacked3 {
+    uint32_t pix[8];    // corner c = 4k + 2j + i: (x0+i, y0+j, z0+k), always inside the volume
+    float w[8];         // trilinear weights, 0 outside
+    bool in[8];
+    float f[3], A;
+    float u[3][2];      // masked axis factors u_a(0), u_a(1)
+};
+
+__device__ __forceinline__ Unpacked3 unpack_record3(const Rec3 &r, int W, int HW) {
+    Unpacked3 u;
+    const uint32_t fl = r.a.y;
+    const uint32_t p = r.a.x;
+    const uint32_t dx = ((fl & 3u) == 3u) ? 1u : 0u;
+    const uint32_t dy = ((fl & 12u) == 12u) ? (uint32_t)W : 0u;
+    const uint32_t dz = ((fl & 48u) == 48u) ? (uint32_t)HW : 0u;
+    u.f[0] = __uint_as_float(r.a.z);
+    u.f[1] = __uint_as_float(r.a.w);
+    u.f[2] = __uint_as_float(r.b.x);
+    u.A = __uint_as_float(r.b.y);
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        u.u[a][0] = (fl & (1u << (2 * a))) ? 1.f - u.f[a] : 0.f;
+        u.u[a][1] = (fl & (2u << (2 * a))) ? u.f[a] : 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int i = c & 1, j = (c >> 1) & 1, k = (c >> 2) & 1;
+        u.pix[c] = p + (i ? dx : 0u) + (j ? dy : 0u) + (k ? dz : 0u);
+        u.w[c] = u.u[0][i] * u.u[1][j] * u.u[2][k];
+        u.in[c] = (fl & (1u << i)) && (fl & (4u << j)) && (fl & (16u << k));
+    }
+    return u;
+}
+
+struct Args3 {
+    const void *value;
+    const float *loc;      // [N][Len_q][M][L][K][3]
+    const float *attn;
+    void *out;             // forward
+    const void *grad_out;  // backward
+    float *grad_value;
+    float *grad_loc;
+    float *grad_attn;
+    unsigned long long *fixed;
+    const unsigned *bound_bits;
+    Dims d;
+    LevelTable3 lv;
+    unsigned char level_of[kMaxSamples];
+    int qblocks;
+};
+
+// corner record of sample s of row r
+__device__ __forceinline__ Rec3 record3(const Args3 &a, int r, int s) {
+    const int l = a.level_of[s];
+    const size_t si = (size_t)r * a.d.P + s;
+    const float *lp = a.loc + 3 * si;
+    const float S[3] = {a.lv.Sx[l], a.lv.Sy[l], a.lv.Sz[l]};
+    float f0[3], fr[3];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) pixel_coord(load_stream1(lp + c), S[c], a.lv.shift, f0[c], fr[c]);
+    return pack_record3(f0, fr, load_stream1(a.attn + si), a.lv.W[l], a.lv.H[l], a.lv.Dz[l], a.lv.Wf[l], a.lv.Hf[l],
+                        a.lv.Dzf[l], a.lv.start[l]);
+}
+
+// ---- forward ------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+msda3d_forward_kernel(const __grid_constant__ Args3 a) {
+    using Lay = Layout<T, D>;
+    constexpr int V = Lay::V, R = Lay::R, HW = Lay::HW;
+    constexpr int JC = kRecordsPerWarp / HW;
+    __shared__ Rec3 s_rec[kWarpsPerBlock][HW][JC + 1];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * kWarpsPerBlock + warp) * HW;
+    const Dims &dm = a.d;
+    if (row0 >= dm.rows) return;
+    const int P = dm.P;
+    const int h = lane / R, ch = lane % R;
+    const int row = row0 + h;
+    const bool row_ok = row < dm.rows;
+    const int rowc = row_ok ? row : dm.rows - 1;
+    const int n = rowc / dm.qm, m = rowc % dm.M;
+    const T *vbase = static_cast<const T *>(a.value) + ((size_t)n * dm.Len_in * dm.M + m) * D + ch * V;
+    const uint64_t pol = l2_keep_policy();
+
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+
+    for (int s0 = 0; s0 < P; s0 += JC) {
+        const int J = min(JC, P - s0);
+        for (int i = lane; i < HW * JC; i += 32) {
+            const int j = i % JC, hh = i / JC;
+            if (j >= J) continue;
+            Rec3 rc;
+            rc.a = make_uint4(0u, 0u, 0u, 0u);      // outside every volume: weight 0, row 0
+            rc.b = make_uint4(0u, 0u, 0u, 0u);
+            if (row0 + hh < dm.rows) rc = record3(a, row0 + hh, s0 + j);
+            s_rec[warp][hh][j] = rc;
+        }
+        __syncwarp();
+#pragma unroll 2
+        for (int j = 0; j < J; ++j) {
+            const int l = a.level_of[s0 + j];
+            const Unpacked3 u = unpack_record3(s_rec[warp][h][j], a.lv.W[l], a.lv.H[l] * a.lv.W[l]);
+            Vec<T> v[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v[c] = load_value(vbase + (size_t)u.pix[c] * dm.pix, pol);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) fma_row<T, V>(acc, u.w[c] * u.A, v[c]);
+        }
+        __syncwarp();
+    }
+    if (row_ok) store_row<T, V>(static_cast<T *>(a.out) + (size_t)row * D + ch * V, acc);
+}
+
+// ---- backward -----------------------------------------------------------------
+template <typename T, int D, bool DET>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 3)
+msda3d_backward_kernel(const __grid_constant__ Args3 a) {
+    constexpr int R = D / 4, HW = 32 / R;
+    constexpr int RC = kRecordsPerWarp / HW;
+    static_assert(HW * RC == 64, "phase 1 and 3 give every lane two (query, sample) slots");
+    __shared__ Rec3 s_rec[kWarpsPerBlock][HW][RC + 1];
+    __shared__ float4 s_res[kWarpsPerBlock][HW][RC + 1];   // grad_attn, A*d/dpx, A*d/dpy, A*d/dpz
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Dims &dm = a.d;
+    const int task = blockIdx.x * kWarpsPerBlock + warp;
+    if (task >= dm.N * a.qblocks * dm.M) return;       // warp-uniform
+    const int m = task % dm.M, t2 = task / dm.M;
+    const int qb = t2 % a.qblocks, n = t2 / a.qblocks;
+    const int P = dm.P;
+    const int h = lane / R, ch = lane % R;
+    const int q = qb * HW + h;
+    const bool row_ok = q < dm.Len_q;
+    const int row = (n * dm.Len_q + (row_ok ? q : qb * HW)) * dm.M + m;
+    const size_t vhead = ((size_t)n * dm.Len_in * dm.M + m) * D + ch * 4;
+    const T *vbase = static_cast<const T *>(a.value) + vhead;
+    const uint64_t pol = l2_keep_policy();
+
+    float4 g = load4_stream<T>(static_cast<const T *>(a.grad_out) + (size_t)row * D + ch * 4);
+    if (!row_ok) g = make_float4(0.f, 0.f, 0.f, 0.f);
+    float scale = 1.f;
+    if constexpr (DET) scale = ldexpf(1.f, fixed_shift(*a.bound_bits, dm.rows));
+
+    for (int r0 = 0; r0 < P; r0 += RC) {
+        const int RJ = min(RC, P - r0);
+        // ---- phase 1: corner records
+        for (int i = lane; i < HW * RC; i += 32) {
+            const int j = i % RC, hh = i / RC;
+            if (j >= RJ) continue;
+            const int qq = qb * HW + hh;
+            Rec3 rc;
+            rc.a = make_uint4(0u, 0u, 0u, 0u);
+            rc.b = make_uint4(0u, 0u, 0u, 0u);
+            if (qq < dm.Len_q) rc = record3(a, (n * dm.Len_q + qq) * dm.M + m, r0 + j);
+            s_rec[warp][hh][j] = rc;
+        }
+        __syncwarp();
+        // ---- phase 2: gather, partial sums, reduce-scatter, grad_value
+#pragma unroll 1
+        for (int j = 0; j < RJ; ++j) {
+            const int l = a.level_of[r0 + j];
+            const Unpacked3 u = unpack_record3(s_rec[warp][h][j], a.lv.W[l], a.lv.H[l] * a.lv.W[l]);
+            float t[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 v = load4_value(vbase + (size_t)u.pix[c] * dm.pix, pol);
+                t[c] = __fmaf_rn(g.w, v.w, __fmaf_rn(g.z, v.z, __fmaf_rn(g.y, v.y, g.x * v.x)));
+            }
+            // partial grad_attn and d/dp along each axis; outside corners read as zero
+            float pga = 0.f, pd[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int i = c & 1, jj = (c >> 1) & 1, k = (c >> 2) & 1;
+                const float tc = u.in[c] ? t[c] : 0.f;
+                pga = __fmaf_rn(u.w[c], tc, pga);
+                // d w_c / d f_x = (i ? 1 : -1) u_y(j) u_z(k), unmasked along x
+                const float wyz = (jj ? u.f[1] : 1.f - u.f[1]) * (k ? u.f[2] : 1.f - u.f[2]);
+                const float wxz = (i ? u.f[0] : 1.f - u.f[0]) * (k ? u.f[2] : 1.f - u.f[2]);
+                const float wxy = (i ? u.f[0] : 1.f - u.f[0]) * (jj ? u.f[1] : 1.f - u.f[1]);
+                pd[0] = __fmaf_rn(i ? wyz : -wyz, tc, pd[0]);
+                pd[1] = __fmaf_rn(jj ? wxz : -wxz, tc, pd[1]);
+                pd[2] = __fmaf_rn(k ? wxy : -wxy, tc, pd[2]);
+            }
+            float tot[2];
+            int first;
+            reduce_scatter4<R>(pga, pd[0], pd[1], pd[2], ch, tot, first);
+            if (R <= 4 || (ch & (R / 4 - 1)) == 0) {
+                float *rs = reinterpret_cast<float *>(&s_res[warp][h][j]);
+                rs[first] = first == 0 ? tot[0] : u.A * tot[0];
+                if (R == 2) rs[first + 1] = u.A * tot[1];
+            }
+            if (row_ok) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    if (!u.in[c]) continue;
+                    const float cw = u.A * u.w[c];
+                    const size_t dst = vhead + (size_t)u.pix[c] * dm.pix;
+                    if constexpr (DET) {
+                        unsigned long long *p = a.fixed + dst;
+                        red_add_u64(p + 0, __float2ll_rn(cw * g.x * scale));
+                        red_add_u64(p + 1, __float2ll_rn(cw * g.y * scale));
+                        red_add_u64(p + 2, __float2ll_rn(cw * g.z * scale));
+                        red_add_u64(p + 3, __float2ll_rn(cw * g.w * scale));
+                    } else {
+                        red_add_v4(a.grad_value + dst, make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w));
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        // ---- phase 3: per-sample gradients
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int i = lane + 32 * it;
+            const int j = i % RC, hh = i / RC;
+            const int qq = qb * HW + hh;
+            if (j < RJ && qq < dm.Len_q) {
+                const int l = a.level_of[r0 + j];
+                const size_t si = ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + r0 + j;
+                const float4 res = s_res[warp][hh][j];
+                __stcs(a.grad_attn + si, res.x);
+                // d px / d loc = S (size, or size - 1 with align_corners)
+                __stcs(a.grad_loc + 3 * si + 0, res.y * a.lv.Sx[l]);
+                __stcs(a.grad_loc + 3 * si + 1, res.z * a.lv.Sy[l]);
+                __stcs(a.grad_loc + 3 * si + 2, res.w * a.lv.Sz[l]);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// ---- launchers ------------------------------------------------------------------
+static void fill3(Args3 &a, const LaunchGeometry3 &g) {
+    a.d = g.g.d;
+    a.lv = g.lv;
+    for (int s = 0; s < kMaxSamples; ++s) a.level_of[s] = g.g.level_of[s];
+}
+
+template <typename T, int D>
+static cudaError_t fwd3_t(const Args3 &a, cudaStream_t stream) {
+    constexpr int HW = Layout<T, D>::HW;
+    const long long warps = ((long long)a.d.rows + HW - 1) / HW;
+    msda3d_forward_kernel<T, D><<<(unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock), kWarpsPerBlock * 32, 0,
+                                  stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_forward3d(const LaunchGeometry3 &g, int dtype, int D, const void *value, const float *loc,
+                             const float *attn, void *out, cudaStream_t stream) {
+    Args3 a{};
+    fill3(a, g);
+    a.value = value;
+    a.loc = loc;
+    a.attn = attn;
+    a.out = out;
+    if (dtype == 0) {
+        switch (D) {
+            case 8: return fwd3_t<float, 8>(a, stream);
+            case 16: return fwd3_t<float, 16>(a, stream);
+            case 32: return fwd3_t<float, 32>(a, stream);
+            case 64: return fwd3_t<float, 64>(a, stream);
+        }
+    } else {
+        switch (D) {
+            case 8: return fwd3_t<__nv_bfloat16, 8>(a, stream);
+            case 16: return fwd3_t<__nv_bfloat16, 16>(a, stream);
+            case 32: return fwd3_t<__nv_bfloat16, 32>(a, stream);
+            case 64: return fwd3_t<__nv_bfloat16, 64>(a, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T, int D>
+static cudaError_t bwd3_t(Args3 &a, bool det, cudaStream_t stream) {
+    constexpr int HW = 32 / (D / 4);
+    a.qblocks = (a.d.Len_q + HW - 1) / HW;
+    const long long tasks = (long long)a.d.N * a.qblocks * a.d.M;
+    const unsigned blocks = (unsigned)((tasks + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    if (det) msda3d_backward_kernel<T, D, true><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+    else msda3d_backward_kernel<T, D, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backward3d(const LaunchGeometry3 &g, int dtype, int D, const void *value, const float *loc,
+                              const float *attn, const void *grad_out, float *grad_value, float *grad_loc,
+                              float *grad_attn, bool det, bool accumulate, void *workspace, cudaStream_t stream) {
+    Args3 a{};
+    fill3(a, g);
+    a.value = value;
+    a.loc = loc;
+    a.attn = attn;
+    a.grad_out = grad_out;
+    a.grad_value = grad_value;
+    a.grad_loc = grad_loc;
+    a.grad_attn = grad_attn;
+    unsigned long long *fixed = nullptr;
+    const unsigned *bound = nullptr;
+    cudaError_t e = backward_prepare(g.g, dtype, D, attn, grad_out, grad_value, det, accumulate, workspace, &fixed,
+                                     &bound, stream);
+    if (e != cudaSuccess) return e;
+    a.fixed = fixed;
+    a.bound_bits = bound;
+    if (g.g.d.rows > 0) {
+        if (dtype == 0) {
+            switch (D) {
+                case 8: e = bwd3_t<float, 8>(a, det, stream); break;
+                case 16: e = bwd3_t<float, 16>(a, det, stream); break;
+                case 32: e = bwd3_t<float, 32>(a, det, stream); break;
+                case 64: e = bwd3_t<float, 64>(a, det, stream); break;
+                default: return cudaErrorInvalidValue;
+            }
+        } else {
+            switch (D) {
+                case 8: e = bwd3_t<__nv_bfloat16, 8>(a, det, stream); break;
+                case 16: e = bwd3_t<__nv_bfloat16, 16>(a, det, stream); break;
+                case 32: e = bwd3_t<__nv_bfloat16, 32>(a, det, stream); break;
+                case 64: e = bwd3_t<__nv_bfloat16, 64>(a, det, stream); break;
+                default: return cudaErrorInvalidValue;
+            }
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return backward_finish(g.g, D, grad_value, det, accumulate, fixed, bound, stream);
+}
+
+}  // namespace msda

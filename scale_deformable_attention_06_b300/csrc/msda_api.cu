@@ -96,6 +96,82 @@ msda_status make_geometry(const msda_problem *p, const int64_t *shapes, const in
     return MSDA_OK;
 }
 
+// The 3-D variant: spatial_shapes is [L][3] = (D, H, W).  Same checks, with
+// volumes in place of maps; the per-level softmax bit has no 3-D call to act on.
+msda_status make_geometry3(const msda_problem *p, const int64_t *shapes, const int64_t *starts,
+                           msda::LaunchGeometry3 &g3) {
+    if (!p) return fail(MSDA_ERR_INVALID_ARG, "problem is NULL");
+    if (p->N < 0 || p->Len_q < 0 || p->Len_in < 0)
+        return fail(MSDA_ERR_INVALID_ARG, "negative size (N=%d Len_q=%d Len_in=%d)", p->N, p->Len_q, p->Len_in);
+    if (p->n_heads < 1 || p->n_points < 1 || p->n_levels < 1)
+        return fail(MSDA_ERR_INVALID_ARG, "n_heads, n_levels and n_points must be >= 1");
+    if (p->options & ~(MSDA_OPT_PER_LEVEL_SOFTMAX | MSDA_OPT_ALIGN_CORNERS))
+        return fail(MSDA_ERR_INVALID_ARG, "unknown option bits 0x%x", p->options);
+    if (p->dtype != MSDA_F32 && p->dtype != MSDA_BF16)
+        return fail(MSDA_ERR_UNSUPPORTED, "dtype %d is not MSDA_F32 or MSDA_BF16", p->dtype);
+    if (p->head_dim != 8 && p->head_dim != 16 && p->head_dim != 32 && p->head_dim != 64)
+        return fail(MSDA_ERR_UNSUPPORTED, "head_dim %d not in {8, 16, 32, 64}", p->head_dim);
+    if (p->n_levels > msda::kMaxLevels)
+        return fail(MSDA_ERR_UNSUPPORTED, "n_levels %d above %d", p->n_levels, msda::kMaxLevels);
+    if ((int64_t)p->n_levels * p->n_points > msda::kMaxSamples)
+        return fail(MSDA_ERR_UNSUPPORTED, "n_levels * n_points = %lld above %d",
+                    (long long)p->n_levels * p->n_points, msda::kMaxSamples);
+    if (!shapes || !starts) return fail(MSDA_ERR_INVALID_ARG, "spatial_shapes / level_start_index is NULL");
+    int64_t expect = 0;
+    for (int l = 0; l < p->n_levels; ++l) {
+        const int64_t Dz = shapes[3 * l], H = shapes[3 * l + 1], W = shapes[3 * l + 2];
+        if (Dz < 1 || H < 1 || W < 1)
+            return fail(MSDA_ERR_INVALID_ARG, "level %d has shape (%lld, %lld, %lld)", l, (long long)Dz,
+                        (long long)H, (long long)W);
+        if (Dz > (1 << 24) || H > (1 << 24) || W > (1 << 24))
+            return fail(MSDA_ERR_UNSUPPORTED, "level %d side above 2^24 (float pixel coordinates)", l);
+        if (starts[l] != expect)
+            return fail(MSDA_ERR_INVALID_ARG, "level_start_index[%d] = %lld, expected %lld", l, (long long)starts[l],
+                        (long long)expect);
+        expect += Dz * H * W;
+        if (expect >= (int64_t(1) << 28)) break;
+    }
+    if (expect != p->Len_in)
+        return fail(MSDA_ERR_INVALID_ARG, "sum of D*H*W over levels is %lld but Len_in is %d", (long long)expect,
+                    p->Len_in);
+    if (p->Len_in >= (int64_t(1) << 28))
+        return fail(MSDA_ERR_UNSUPPORTED, "Len_in %d is not below 2^28 (voxel index of a corner record)", p->Len_in);
+    const int64_t pix = (int64_t)p->n_heads * p->head_dim;
+    if ((int64_t)p->Len_in * pix >= (int64_t(1) << 31))
+        return fail(MSDA_ERR_UNSUPPORTED, "Len_in * n_heads * head_dim exceeds 2^31");
+    const int64_t rows = (int64_t)p->N * p->Len_q * p->n_heads;
+    if (rows >= (int64_t(1) << 31)) return fail(MSDA_ERR_UNSUPPORTED, "N * Len_q * n_heads exceeds 2^31");
+
+    std::memset(&g3, 0, sizeof(g3));
+    msda::Dims &d = g3.g.d;
+    d.N = p->N;
+    d.Len_in = p->Len_in;
+    d.M = p->n_heads;
+    d.Len_q = p->Len_q;
+    d.L = p->n_levels;
+    d.K = p->n_points;
+    d.P = p->n_levels * p->n_points;
+    d.rows = (int)rows;
+    d.qm = p->Len_q * p->n_heads;
+    d.pix = (int)pix;
+    const bool align = (p->options & MSDA_OPT_ALIGN_CORNERS) != 0;
+    g3.lv.shift = align ? 0.f : 0.5f;
+    for (int l = 0; l < p->n_levels; ++l) {
+        g3.lv.Dz[l] = (int)shapes[3 * l];
+        g3.lv.H[l] = (int)shapes[3 * l + 1];
+        g3.lv.W[l] = (int)shapes[3 * l + 2];
+        g3.lv.start[l] = (int)starts[l];
+        g3.lv.Dzf[l] = (float)g3.lv.Dz[l];
+        g3.lv.Hf[l] = (float)g3.lv.H[l];
+        g3.lv.Wf[l] = (float)g3.lv.W[l];
+        g3.lv.Sx[l] = align ? (float)(g3.lv.W[l] - 1) : g3.lv.Wf[l];
+        g3.lv.Sy[l] = align ? (float)(g3.lv.H[l] - 1) : g3.lv.Hf[l];
+        g3.lv.Sz[l] = align ? (float)(g3.lv.Dz[l] - 1) : g3.lv.Dzf[l];
+    }
+    for (int s = 0; s < d.P; ++s) g3.g.level_of[s] = (unsigned char)(s / p->n_points);
+    return MSDA_OK;
+}
+
 msda_status cuda_status(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return MSDA_OK;
     return fail(MSDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -258,6 +334,61 @@ msda_status msda_backward_fused(const msda_problem *problem, const void *value, 
                                                    grad_reference_points, grad_sampling_offsets, grad_attention_logits,
                                                    det, acc, workspace, static_cast<cudaStream_t>(stream)),
                        "msda_backward_fused launch");
+}
+
+msda_status msda3d_forward(const msda_problem *problem, const void *value, const int64_t *spatial_shapes,
+                           const int64_t *level_start_index, const float *sampling_locations,
+                           const float *attention_weights, void *output, void *stream) {
+    g_last_error[0] = 0;
+    msda::LaunchGeometry3 g;
+    msda_status st = make_geometry3(problem, spatial_shapes, level_start_index, g);
+    if (st != MSDA_OK) return st;
+    if (g.g.d.rows == 0) return MSDA_OK;
+    if (!value || !sampling_locations || !attention_weights || !output)
+        return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!aligned(value, 16) || !aligned(output, 16) || !aligned(sampling_locations, 4) || !aligned(attention_weights, 4))
+        return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor (value/output 16 B, locations and weights 4 B)");
+    return cuda_status(msda::launch_forward3d(g, problem->dtype, problem->head_dim, value, sampling_locations,
+                                              attention_weights, output, static_cast<cudaStream_t>(stream)),
+                       "msda3d_forward launch");
+}
+
+msda_status msda3d_backward(const msda_problem *problem, const void *value, const int64_t *spatial_shapes,
+                            const int64_t *level_start_index, const float *sampling_locations,
+                            const float *attention_weights, const void *grad_output, float *grad_value,
+                            float *grad_sampling_locations, float *grad_attention_weights, unsigned flags,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    g_last_error[0] = 0;
+    msda::LaunchGeometry3 g;
+    msda_status st = make_geometry3(problem, spatial_shapes, level_start_index, g);
+    if (st != MSDA_OK) return st;
+    if (flags & ~(MSDA_DETERMINISTIC | MSDA_ACCUMULATE_GRAD_VALUE))
+        return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const bool det = (flags & MSDA_DETERMINISTIC) != 0, acc = (flags & MSDA_ACCUMULATE_GRAD_VALUE) != 0;
+    const size_t nval = (size_t)g.g.d.N * g.g.d.Len_in * g.g.d.M * problem->head_dim;
+    if (nval > 0 && !grad_value) return fail(MSDA_ERR_INVALID_ARG, "grad_value is NULL");
+    if (grad_value && !aligned(grad_value, 16)) return fail(MSDA_ERR_INVALID_ARG, "grad_value not 16-byte aligned");
+    if (g.g.d.rows > 0) {
+        if (!value || !sampling_locations || !attention_weights || !grad_output || !grad_sampling_locations ||
+            !grad_attention_weights)
+            return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+        if (!aligned(value, 16) || !aligned(grad_output, 16) || !aligned(sampling_locations, 4) ||
+            !aligned(grad_sampling_locations, 4) || !aligned(attention_weights, 4) || !aligned(grad_attention_weights, 4))
+            return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor");
+    }
+    const size_t need = msda::backward_workspace_bytes(g.g, problem->head_dim, det);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need)
+            return fail(MSDA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
+        if (!aligned(workspace, 256)) return fail(MSDA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    }
+    if (nval == 0 && g.g.d.rows == 0) return MSDA_OK;
+    if (g.g.d.rows == 0 && acc) return MSDA_OK;
+    return cuda_status(msda::launch_backward3d(g, problem->dtype, problem->head_dim, value, sampling_locations,
+                                               attention_weights, grad_output, grad_value, grad_sampling_locations,
+                                               grad_attention_weights, det, acc, workspace,
+                                               static_cast<cudaStream_t>(stream)),
+                       "msda3d_backward launch");
 }
 
 const char *msda_status_string(msda_status s) {

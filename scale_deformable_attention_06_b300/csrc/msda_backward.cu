@@ -59,26 +59,6 @@ struct BwdArgs {
     unsigned merge_mask;           // bit l: merge grad_value contributions on level l
 };
 
-__device__ __forceinline__ void red_add_v4(float *p, float4 v) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void red_add_u64(unsigned long long *p, long long v) {
-    asm volatile("red.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Power-of-two scale of the fixed-point sums: every partial sum is at most
-// rows * max_row_bound < 2^62 after scaling.
-__device__ __forceinline__ int fixed_shift(unsigned bits, int rows) {
-    const double bound = (double)__uint_as_float(bits) * (double)rows;
-    if (!(bound > 0.0)) return 0;
-    int e;
-    frexp(bound, &e);          // bound < 2^e
-    int shift = 62 - e;
-    return shift < -60 ? -60 : (shift > 100 ? 100 : shift);
-}
-
 // grad_value[dst .. dst + 4) += v (fp32 reduction, or fixed point)
 template <bool DET>
 __device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, float4 v, float scale) {
@@ -90,31 +70,6 @@ __device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, float4 v,
         red_add_u64(p + 3, __float2ll_rn(v.w * scale));
     } else {
         red_add_v4(a.grad_value + dst, v);
-    }
-}
-
-// Sums three per-lane partials over the R lanes of a query (lanes h*R .. h*R+R-1
-// of the warp).  Afterwards the lane holds in out[0] the total of value
-// `first` (0: x0, 1: x1, 2: x2, 3: nothing) and, for R == 2, in out[1] the total
-// of value first + 1.  All 32 lanes must call it.
-template <int R>
-__device__ __forceinline__ void reduce_scatter3(float x0, float x1, float x2, int ch, float (&out)[2], int &first) {
-    const bool hb = (ch & (R / 2)) != 0;
-    const float s0 = __shfl_xor_sync(0xffffffffu, hb ? x0 : x2, R / 2);
-    const float s1 = __shfl_xor_sync(0xffffffffu, hb ? x1 : 0.f, R / 2);
-    const float y0 = (hb ? x2 : x0) + s0, y1 = (hb ? 0.f : x1) + s1;
-    if constexpr (R == 2) {
-        out[0] = y0;
-        out[1] = y1;
-        first = hb ? 2 : 0;
-    } else {
-        const bool lb = (ch & (R / 4)) != 0;
-        float z = (lb ? y1 : y0) + __shfl_xor_sync(0xffffffffu, lb ? y0 : y1, R / 4);
-#pragma unroll
-        for (int o = R / 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        out[0] = z;
-        out[1] = 0.f;
-        first = (hb ? 2 : 0) + (lb ? 1 : 0);
     }
 }
 
@@ -282,7 +237,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                                   (u.in[3] ? u.fx * t[3] : 0.f) - (u.in[1] ? u.fx * t[1] : 0.f);
                 float tot[2];
                 int first;
-                reduce_scatter3<R>(pga, pdx, pdy, ch, tot, first);
+                reduce_scatter4<R>(pga, pdx, pdy, 0.f, ch, tot, first);
                 if (R <= 4 || (ch & (R / 4 - 1)) == 0) {
                     float *rs = reinterpret_cast<float *>(&sm.res[h][j]);
                     if (first < 3) rs[first] = first == 0 ? tot[0] : u.A * tot[0];
@@ -529,6 +484,56 @@ static unsigned merge_levels(const LaunchGeometry &g) {
         if ((double)g.d.Len_q * g.d.K >= 32.0 * pixels) mask |= 1u << l;
     }
     return mask;
+}
+
+// grad_value preparation and completion, shared by the 2-D and 3-D
+// backward: zeroing (fp32 mode) or the fixed-point accumulators and their
+// scale bound (deterministic mode); then the conversion back to fp32.
+cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const float *attn, const void *grad_out,
+                             float *grad_value, bool det, bool accumulate, void *workspace,
+                             unsigned long long **fixed, const unsigned **bound, cudaStream_t stream) {
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
+    *fixed = nullptr;
+    *bound = nullptr;
+    if (det) {
+        unsigned *hdr = static_cast<unsigned *>(workspace);
+        *fixed = reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + 256);
+        *bound = hdr;
+        zero_u64_kernel<<<grid_for((nval * 8 + 256) / 16, 256), 256, 0, stream>>>(
+            static_cast<ulonglong2 *>(workspace), (nval * 8 + 256) / 16);
+        if (g.d.rows > 0) {
+#define MSDA_BOUND(T, DD) row_bound_kernel<T, DD><<<grid_for(g.d.rows, 256), 256, 0, stream>>>( \
+        attn, static_cast<const T *>(grad_out), g.d.rows, g.d.P, hdr)
+            if (dtype == 0) {
+                switch (D) {
+                    case 8: MSDA_BOUND(float, 8); break;
+                    case 16: MSDA_BOUND(float, 16); break;
+                    case 32: MSDA_BOUND(float, 32); break;
+                    case 64: MSDA_BOUND(float, 64); break;
+                }
+            } else {
+                switch (D) {
+                    case 8: MSDA_BOUND(__nv_bfloat16, 8); break;
+                    case 16: MSDA_BOUND(__nv_bfloat16, 16); break;
+                    case 32: MSDA_BOUND(__nv_bfloat16, 32); break;
+                    case 64: MSDA_BOUND(__nv_bfloat16, 64); break;
+                }
+            }
+#undef MSDA_BOUND
+        }
+    } else if (!accumulate && nval > 0) {
+        zero_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(reinterpret_cast<float4 *>(grad_value), nval / 4);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t backward_finish(const LaunchGeometry &g, int D, float *grad_value, bool det, bool accumulate,
+                            const unsigned long long *fixed, const unsigned *bound, cudaStream_t stream) {
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
+    if (det && nval > 0)
+        fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(fixed, bound, g.d.rows, grad_value, nval,
+                                                                      accumulate ? 1 : 0);
+    return cudaGetLastError();
 }
 
 // Inputs and outputs of one backward launch.  Unfused: loc, attn -> grad_loc,

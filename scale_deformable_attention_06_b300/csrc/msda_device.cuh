@@ -314,6 +314,53 @@ __device__ __forceinline__ float4 ffma4(float a, float4 x, float4 y) {
     return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
+// Sums four per-lane partials over the R lanes of a row group (lanes h*R ..
+// h*R+R-1 of the warp) with 2 + log2(R/4) shuffles.  Afterwards the lane holds
+// in out[0] the total of value `first` (0: x0, 1: x1, 2: x2, 3: x3) and, for
+// R == 2, in out[1] the total of value first + 1.  All 32 lanes must call it.
+template <int R>
+__device__ __forceinline__ void reduce_scatter4(float x0, float x1, float x2, float x3, int ch, float (&out)[2],
+                                                int &first) {
+    const bool hb = (ch & (R / 2)) != 0;
+    const float s0 = __shfl_xor_sync(0xffffffffu, hb ? x0 : x2, R / 2);
+    const float s1 = __shfl_xor_sync(0xffffffffu, hb ? x1 : x3, R / 2);
+    const float y0 = (hb ? x2 : x0) + s0, y1 = (hb ? x3 : x1) + s1;
+    if constexpr (R == 2) {
+        out[0] = y0;
+        out[1] = y1;
+        first = hb ? 2 : 0;
+    } else {
+        const bool lb = (ch & (R / 4)) != 0;
+        float z = (lb ? y1 : y0) + __shfl_xor_sync(0xffffffffu, lb ? y0 : y1, R / 4);
+#pragma unroll
+        for (int o = R / 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        out[0] = z;
+        out[1] = 0.f;
+        first = (hb ? 2 : 0) + (lb ? 1 : 0);
+    }
+}
+
+// ---- grad_value reductions ----------------------------------------------------
+__device__ __forceinline__ void red_add_v4(float *p, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void red_add_u64(unsigned long long *p, long long v) {
+    asm volatile("red.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Power-of-two scale of the fixed-point sums: every partial sum is at most
+// rows * max_row_bound < 2^62 after scaling.
+__device__ __forceinline__ int fixed_shift(unsigned bits, int rows) {
+    const double bound = (double)__uint_as_float(bits) * (double)rows;
+    if (!(bound > 0.0)) return 0;
+    int e;
+    frexp(bound, &e);          // bound < 2^e
+    int shift = 62 - e;
+    return shift < -60 ? -60 : (shift > 100 ? 100 : shift);
+}
+
 // acc[0..V) += w * v
 template <typename T, int V>
 __device__ __forceinline__ void fma_row(float (&acc)[V], float w, const Vec<T> &v) {

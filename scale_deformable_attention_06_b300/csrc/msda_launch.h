@@ -38,4 +38,31 @@ cudaError_t launch_backward_fused(const LaunchGeometry &g, int dtype, int D, con
                                   float *grad_ref, float *grad_off, float *grad_logits, bool det, bool accumulate,
                                   void *workspace, cudaStream_t stream);
 
+// grad_value preparation (zeroing, or deterministic accumulators and bound)
+// and completion (fixed point to fp32), shared by the 2-D and 3-D backward.
+cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const float *attn, const void *grad_out,
+                             float *grad_value, bool det, bool accumulate, void *workspace,
+                             unsigned long long **fixed, const unsigned **bound, cudaStream_t stream);
+cudaError_t backward_finish(const LaunchGeometry &g, int D, float *grad_value, bool det, bool accumulate,
+                            const unsigned long long *fixed, const unsigned *bound, cudaStream_t stream);
+
+// 3-D (trilinear) variant: volumes (Dz, H, W) per level.
+struct LevelTable3 {
+    int Dz[kMaxLevels], H[kMaxLevels], W[kMaxLevels], start[kMaxLevels];
+    float Dzf[kMaxLevels], Hf[kMaxLevels], Wf[kMaxLevels];
+    float Sx[kMaxLevels], Sy[kMaxLevels], Sz[kMaxLevels];   // pixel scales (size, or size - 1)
+    float shift;                                            // 0.5, or 0 with align_corners
+};
+
+struct LaunchGeometry3 {
+    LaunchGeometry g;      // sizes, sample -> level map (its level table is unused)
+    LevelTable3 lv;
+};
+
+cudaError_t launch_forward3d(const LaunchGeometry3 &g, int dtype, int D, const void *value, const float *loc,
+                             const float *attn, void *out, cudaStream_t stream);
+cudaError_t launch_backward3d(const LaunchGeometry3 &g, int dtype, int D, const void *value, const float *loc,
+                              const float *attn, const void *grad_out, float *grad_value, float *grad_loc,
+                              float *grad_attn, bool det, bool accumulate, void *workspace, cudaStream_t stream);
+
 }  // namespace msda

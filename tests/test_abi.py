@@ -147,3 +147,20 @@ def test_product_path_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f"{f} mentions the oracle"
                 assert "_work/" not in text and "/_work" not in text, f"{f} refers to working files"
+
+
+@pytest.mark.parametrize("shapes,starts,Len_in,expect", [
+    ([2, 3, 4, 1, 2, 2], [0, 24], 28, 0),       # valid: reaches the pointer checks (NULL value)
+    ([2, 3, 4, 1, 2, 2], [0, 24], 29, 1),       # Len_in disagrees with sum D*H*W
+    ([2, 0, 4, 1, 2, 2], [0, 0], 4, 1),         # empty volume
+    ([2, 3, 4, 1, 2, 2], [0, 23], 28, 1),       # level start off by one
+])
+def test_3d_host_checks(msda, shapes, starts, Len_in, expect):
+    p = _problem(msda, Len_in=Len_in, n_levels=2)
+    sh, st = _levels(shapes, starts)
+    lib = msda.lib()
+    rc = lib.msda3d_forward(ctypes.byref(p), None if expect == 0 else FAKE, sh, st, FAKE, FAKE, FAKE, None)
+    assert rc == (1 if expect == 0 else expect), lib.msda_last_error()
+    rc = lib.msda3d_backward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, None if expect == 0 else FAKE,
+                             0, None, 0, None)
+    assert rc == (1 if expect == 0 else expect)

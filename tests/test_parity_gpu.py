@@ -358,3 +358,49 @@ def test_options_dense_merge_path(msda):
     ref = oracle.backward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
                                 p["attention_logits"], p["grad_output"], options=3)
     _check_backward_fused(w, [t.cpu().numpy() for t in got], ref)
+
+
+# ----------------------------------------------------------------- 3-D variant (trilinear)
+def _vol_case(dtype, D, seed, levels=((3, 4, 5), (2, 3, 2), (1, 1, 1), (4, 2, 3)), K=3, Lq=29, N=2, M=3):
+    raw = workloads.draw_volumes(N, M, D, levels, K, Lq, dtype=dtype, loc_range=(-0.15, 1.15), seed=seed)
+    L = len(levels)
+    attn = oracle.softmax(raw["attention_logits"]).astype(np.float32).reshape(N, Lq, M, L, K)
+    value, g = raw["value"], raw["grad_output"]
+    if dtype == "bf16":
+        value, g = H.bf16_round(value), H.bf16_round(g)
+    return raw, value, g, attn
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("D", [8, 32, 64])
+@pytest.mark.parametrize("opt", [0, 2], ids=["half_pixel", "align_corners"])
+def test_3d_forward_backward(msda, dtype, D, opt):
+    raw, value, g, attn = _vol_case(dtype, D, seed=1400 + D + opt)
+    sh, st, loc = raw["spatial_shapes"], raw["level_start_index"], raw["sampling_locations"]
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    v, gd, locd, ad = H.dev(value, dt), H.dev(g, dt), H.dev(loc), H.dev(attn)
+    out = msda.msda3d_forward(v, sh, st, locd, ad, options=opt).float().cpu().numpy()
+    H.assert_fwd(out, oracle.forward3d(value, sh, st, loc, attn, options=opt), dtype, f"3-D {dtype} D={D} output")
+    ref = oracle.backward3d(value, sh, st, loc, attn, g, options=opt)
+    w = workloads.custom(name="volumes", N=2, M=3, D=D, levels=[(1, 1)], K=3, dtype=dtype)
+    _check_backward(w, [t.cpu().numpy() for t in msda.msda3d_backward(v, sh, st, locd, ad, gd, options=opt)], ref)
+    det = [[t.cpu().numpy() for t in msda.msda3d_backward(v, sh, st, locd, ad, gd, flags=msda.MSDA_DETERMINISTIC,
+                                                           options=opt)] for _ in range(2)]
+    _check_backward(w, det[0], ref)
+    for a, b in zip(det[0], det[1]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), "deterministic 3-D backward is not bitwise stable"
+
+
+def test_3d_one_slice_is_2d(msda):
+    """One-slice volumes sampled on their centre plane give the 2-D call's result."""
+    w = workloads.custom(N=1, M=2, D=32, levels=[(6, 7), (3, 4)], K=3, Len_q=19, refs="none", seed=1450)
+    p = H.prepared(w)
+    sh2 = p["spatial_shapes"]
+    sh3 = np.concatenate([np.ones((sh2.shape[0], 1), np.int64), sh2], axis=1)
+    loc3 = np.concatenate([p["sampling_locations"], np.full(p["sampling_locations"].shape[:-1] + (1,), 0.5,
+                                                            np.float32)], axis=-1)
+    out2 = msda.msda_forward(H.dev(p["value"]), sh2, p["level_start_index"], H.dev(p["sampling_locations"]),
+                             H.dev(p["attention_weights"])).cpu().numpy()
+    out3 = msda.msda3d_forward(H.dev(p["value"]), sh3, p["level_start_index"], H.dev(loc3),
+                               H.dev(p["attention_weights"])).cpu().numpy()
+    assert np.abs(out3 - out2).max() <= 1e-5

@@ -141,3 +141,24 @@ def draw(w: Workload, seed=None):
 def custom(name="custom", **kw):
     """A workload with explicit fields (tests of ragged and edge shapes)."""
     return Workload(name=name, **kw)
+
+
+# ----------------------------------------------------------------------------- volumes (3-D variant)
+VIDEO_LEVELS = [(8, 50, 84), (4, 25, 42), (2, 13, 21)]   # (D, H, W): frames x rows x columns
+
+
+def draw_volumes(N, M, D, levels, K, Len_q, dtype="f32", loc_range=(-0.05, 1.05), seed=1239):
+    """Raw draws for the 3-D variant: value [N,Len_in,M,D] ~N(0,1) with
+    Len_in = sum D_l*H_l*W_l, sampling_locations [N,Len_q,M,L,K,3] ~U(loc_range)
+    per coordinate, attention_logits [N,Len_q,M,L*K] and grad_output ~N(0,1)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    sh = np.asarray(levels, dtype=np.int64).reshape(-1, 3)
+    sizes = sh.prod(-1)
+    S = int(sizes.sum())
+    L = sh.shape[0]
+    lo, hi = loc_range
+    return {"spatial_shapes": sh, "level_start_index": np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(np.int64),
+            "value": rng.standard_normal((N, S, M, D), dtype=np.float32),
+            "sampling_locations": rng.uniform(lo, hi, size=(N, Len_q, M, L, K, 3)).astype(np.float32),
+            "attention_logits": rng.standard_normal((N, Len_q, M, L * K), dtype=np.float32),
+            "grad_output": rng.standard_normal((N, Len_q, M * D), dtype=np.float32), "dtype": dtype}
