@@ -445,6 +445,52 @@ def run_sweep(args):
         print(json.dumps({"sweep": True, "workload": name, "dtype": w.dtype, "samples": w.samples, "calls": calls,
                           "oracle_fwd_bwd_points_per_s_1core": pts / el,
                           "oracle_sample": f"{q} of {w.Lq} queries x {w.N} batches"}))
+    run_sweep_volumes(timed, peak)
+
+
+def run_sweep_volumes(timed, peak):
+    """The 3-D variant on a video-like workload: three levels of (frames, rows,
+    columns) = (8, 50, 84), (4, 25, 42), (2, 13, 21), one query per voxel,
+    uniformly drawn locations, fp32."""
+    import torch
+    import scale_deformable_attention_06_b300 as msda
+    import oracle
+    dev = torch.device("cuda", 0)
+    levels = workloads.VIDEO_LEVELS
+    S = sum(d * h * w for d, h, w in levels)
+    N, M, D, K, Lq = 1, 8, 32, 4, S
+    raw = workloads.draw_volumes(N, M, D, levels, K, Lq, seed=1240)
+    L = len(levels)
+    sh, st = raw["spatial_shapes"], raw["level_start_index"]
+    attn_h = torch.softmax(torch.from_numpy(raw["attention_logits"]).double(), -1).float().reshape(N, Lq, M, L, K)
+    value = torch.from_numpy(raw["value"]).to(dev)
+    gout = torch.from_numpy(raw["grad_output"]).to(dev)
+    loc = torch.from_numpy(raw["sampling_locations"]).to(dev)
+    attn = attn_h.contiguous().to(dev)
+    out = torch.empty((N, Lq, M * D), device=dev)
+    gv = torch.empty(value.shape, device=dev)
+    gl, ga = torch.empty_like(loc), torch.empty_like(attn)
+    samples = N * Lq * M * L * K
+    t = {"fwd": timed(lambda: msda.msda3d_forward(value, sh, st, loc, attn, output=out), 20),
+         "bwd": timed(lambda: msda.msda3d_backward(value, sh, st, loc, attn, gout, grad_value=gv,
+                                                   grad_sampling_locations=gl, grad_attention_weights=ga,
+                                                   flags=msda.MSDA_ACCUMULATE_GRAD_VALUE), 20,
+                      pre=lambda: gv.zero_())}
+    nval, nout = N * S * M * D, N * Lq * M * D
+    ab = {"fwd": 4 * (nval + samples * 4 + nout), "bwd": 4 * (nval + samples * 4 + nout + nval + samples * 4)}
+    calls = {k: {"us": ms * 1e3, "points_per_s": samples / (ms / 1e3), "gbs": ab[k] / (ms / 1e3) / 1e9,
+                 "frac_of_measured_hbm_peak": ab[k] / (ms / 1e3) / 1e9 / peak, "algorithmic_bytes": ab[k]}
+             for k, ms in t.items()}
+    q = 64
+    lv = raw["sampling_locations"][:, :q].astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.forward3d(raw["value"].astype(np.float64), sh, st, lv, attn_h.numpy()[:, :q].astype(np.float64))
+    oracle.backward3d(raw["value"].astype(np.float64), sh, st, lv, attn_h.numpy()[:, :q].astype(np.float64),
+                      raw["grad_output"][:, :q].astype(np.float64))
+    el = time.perf_counter() - t0
+    print(json.dumps({"sweep": True, "workload": "video (3-D, trilinear)", "dtype": "f32", "samples": samples,
+                      "calls": calls, "oracle_fwd_bwd_points_per_s_1core": N * q * M * L * K / el,
+                      "oracle_sample": f"{q} of {Lq} queries"}))
 
 
 # ----------------------------------------------------------------------------- oracle timings
