@@ -223,18 +223,19 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 float4 v[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) v[c] = load4_value(vbase + (size_t)u.pix[c] * dm.pix, pol);
-                // partial <g, v_c> over this lane's channels
+                // partial <g, v_c> over this lane's channels (two packed products
+                // per corner); corners outside the map read as zero
                 float t[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    t[c] = __fmaf_rn(g.w, v[c].w, __fmaf_rn(g.z, v[c].z, __fmaf_rn(g.y, v[c].y, g.x * v[c].x)));
-                // partial grad_attn, d/dpx, d/dpy; corners outside the map read as zero
-                const float gy0 = 1.f - u.fy, gx0 = 1.f - u.fx;
+                for (int c = 0; c < 4; ++c) {
+                    float2 pr = __fmul2_rn(make_float2(g.x, g.y), make_float2(v[c].x, v[c].y));
+                    pr = __ffma2_rn(make_float2(g.z, g.w), make_float2(v[c].z, v[c].w), pr);
+                    t[c] = u.in[c] ? pr.x + pr.y : 0.f;
+                }
+                // partial grad_attn, d/dpx, d/dpy
                 const float pga = u.w[0] * t[0] + u.w[1] * t[1] + u.w[2] * t[2] + u.w[3] * t[3];
-                const float pdx = (u.in[1] ? gy0 * t[1] : 0.f) - (u.in[0] ? gy0 * t[0] : 0.f) +
-                                  (u.in[3] ? u.fy * t[3] : 0.f) - (u.in[2] ? u.fy * t[2] : 0.f);
-                const float pdy = (u.in[2] ? gx0 * t[2] : 0.f) - (u.in[0] ? gx0 * t[0] : 0.f) +
-                                  (u.in[3] ? u.fx * t[3] : 0.f) - (u.in[1] ? u.fx * t[1] : 0.f);
+                const float pdx = (1.f - u.fy) * (t[1] - t[0]) + u.fy * (t[3] - t[2]);
+                const float pdy = (1.f - u.fx) * (t[2] - t[0]) + u.fx * (t[3] - t[1]);
                 float tot[2];
                 int first;
                 reduce_scatter4<R>(pga, pdx, pdy, 0.f, ch, tot, first);
@@ -249,8 +250,10 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                         for (int c = 0; c < 4; ++c) {
                             if (!u.in[c]) continue;
                             const float cw = u.A * u.w[c];
-                            scatter4<DET>(a, vhead + (size_t)u.pix[c] * dm.pix,
-                                          make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w), scale);
+                            const float2 lo = __fmul2_rn(make_float2(cw, cw), make_float2(g.x, g.y));
+                            const float2 hi = __fmul2_rn(make_float2(cw, cw), make_float2(g.z, g.w));
+                            scatter4<DET>(a, vhead + (size_t)u.pix[c] * dm.pix, make_float4(lo.x, lo.y, hi.x, hi.y),
+                                          scale);
                         }
                     } else if constexpr (MERGE) {
                         // lanes ch < 4 insert corner c = ch of their query; the valid
