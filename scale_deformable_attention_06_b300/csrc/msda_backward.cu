@@ -586,7 +586,9 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
     a.lv = g.lv;
     for (int s = 0; s < kMaxSamples; ++s) a.level_of[s] = g.level_of[s];
     a.qblocks = (g.d.Len_q + HW - 1) / HW;
-    a.merge_mask = HW == 4 ? merge_levels(g) : 0u;
+    // deterministic mode: a fixed-point reduction is four 64-bit atomics per
+    // lane and corner, so merging pays on every level
+    a.merge_mask = HW == 4 ? (det ? (1u << g.d.L) - 1u : merge_levels(g)) : 0u;
     if (det) {
         unsigned *hdr = static_cast<unsigned *>(workspace);
         unsigned long long *fixed = reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + 256);
