@@ -146,7 +146,11 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
         if (lane == 0) sm.count = 0;
         __syncwarp();
     }
-    if (FUSED && !(OPTS && dm.per_level_softmax)) {
+    // fused, whole-row softmax: statistics in the record phase (short rows) or
+    // in a pass of their own; either way the arithmetic of the fused forward
+    const bool row_softmax = FUSED && !(OPTS && dm.per_level_softmax);
+    const bool seg_stats = SoftmaxChunk<T, D>::in_record_phase && row_softmax && P <= SoftmaxChunk<T, D>::value;
+    if (row_softmax && !seg_stats) {
         // softmax statistics of the warp's queries (the same arithmetic as the
         // fused forward, so A is the same value there and here)
         for (int hh = 0; hh < HW; ++hh) {
@@ -164,6 +168,34 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
         __syncwarp();
     }
     float dotp[2] = {0.f, 0.f};        // fused: this lane's part of sum_s A_s * grad_attn_s, per slot
+
+    // seg_stats: the attention weight of each of this lane's two record slots
+    // (slot it = record lane + 32 it: query (lane + 32 it) / RC, sample its
+    // remainder; a query's samples are RC consecutive lanes)
+    float A_seg[2] = {0.f, 0.f};
+    if constexpr (FUSED) {
+        if (seg_stats) {                                // warp-uniform; the row is one chunk
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int i = lane + 32 * it, j = i % RC, hh = i / RC;
+                const int qq = qb * HW + hh;
+                const bool valid = j < P && qq < dm.Len_q;
+                const float lg = valid ? __ldg(a.logits + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + j)
+                                       : -INFINITY;
+                float mx = lg;
+#pragma unroll
+                for (int o = 1; o < RC && o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float e = valid ? expf(lg - mx) : 0.f;
+                float sum = e;
+#pragma unroll
+                for (int o = 1; o < RC && o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                const float inv = 1.f / sum;
+                A_seg[it] = e * inv;
+                if (j == 0 && qq < dm.Len_q) sm.stat[hh] = make_float2(mx, inv);
+            }
+            __syncwarp();
+        }
+    }
 
     for (int r0 = 0; r0 < P; r0 += RC) {
         const int RJ = min(RC, P - r0);
@@ -194,7 +226,10 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                         pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
                         st = sm.stat[hh];
                     }
-                    A = expf(load_stream1(a.logits + si) - st.x) * st.y;
+                    if (seg_stats)
+                        A = A_seg[(i - lane) >> 5];     // this iteration's slot
+                    else
+                        A = expf(load_stream1(a.logits + si) - st.x) * st.y;
                 } else {
                     const float2 lc = load_stream2(a.loc + 2 * si);
                     pixel_coord(lc.x, a.lv.Sx[l], a.lv.shift, x0, fx);

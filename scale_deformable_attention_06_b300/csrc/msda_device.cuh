@@ -361,6 +361,24 @@ __device__ __forceinline__ int fixed_shift(unsigned bits, int rows) {
     return shift < -60 ? -60 : (shift > 100 ? 100 : shift);
 }
 
+// ---- softmax statistics inside the record phase ----------------------------
+// When all L*K logits of a row fit in one record chunk of both the forward
+// (64 / HW rows-fastest records) and the backward (64 / (128 / D) samples-
+// fastest records), the record phase holds every logit in some lane and the
+// row's max and sum come from shuffles there, with one summation tree in both
+// kernels: pairwise by sample index, zero-padded (so A is bitwise the same in
+// the fused forward and the fused backward).  Longer rows use a separate
+// statistics pass, again the same in both kernels.
+template <typename T, int D>
+struct SoftmaxChunk {
+    static constexpr int fwd = kRecordsPerWarp / Layout<T, D>::HW;
+    static constexpr int bwd = kRecordsPerWarp / (128 / D);
+    static constexpr int value = fwd < bwd ? fwd : bwd;
+    // compiled in only where it serves rows of 16 logits (4 levels x 4
+    // points); elsewhere the extra code measured slower than it saved
+    static constexpr bool in_record_phase = value >= 16;
+};
+
 // acc[0..V) += w * v
 template <typename T, int V>
 __device__ __forceinline__ void fma_row(float (&acc)[V], float w, const Vec<T> &v) {

@@ -56,7 +56,11 @@ msda_forward_kernel(const __grid_constant__ FwdArgs a) {
     if (row0 >= dm.rows) return;
     const int P = dm.P;
 
-    if (FUSED && !(OPTS && a.d.per_level_softmax)) {
+    // fused, whole-row softmax: statistics in the record phase (short rows) or
+    // in a pass of their own (rows longer than SoftmaxChunk)
+    const bool row_softmax = FUSED && !(OPTS && a.d.per_level_softmax);
+    const bool seg_stats = SoftmaxChunk<T, D>::in_record_phase && row_softmax && P <= SoftmaxChunk<T, D>::value;
+    if (row_softmax && !seg_stats) {
         // softmax statistics of each row: max and 1/sum of exp(logit - max)
         for (int h = 0; h < HW; ++h) {
             const int row = row0 + h;
@@ -87,6 +91,36 @@ msda_forward_kernel(const __grid_constant__ FwdArgs a) {
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
 
+    // seg_stats: the attention weight of each of this lane's two record slots
+    // (slot it = record lane + 32 it, one row: HW divides 32)
+    float A_seg[2] = {0.f, 0.f};
+    if constexpr (FUSED) {
+        if (seg_stats) {                                // warp-uniform; the row is one chunk
+            float lg[2];
+            bool valid[2];
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int i = lane + 32 * it, hh = i % HW, j = i / HW;
+                valid[it] = j < P && row0 + hh < dm.rows;
+                lg[it] = valid[it] ? __ldg(a.logits + (size_t)(row0 + hh) * P + j) : -INFINITY;
+            }
+            float mx = fmaxf(lg[0], lg[1]);
+#pragma unroll
+            for (int o = HW; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float e[2], sm[2];
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                e[it] = valid[it] ? expf(lg[it] - mx) : 0.f;
+                sm[it] = e[it];
+#pragma unroll
+                for (int o = HW; o < 32; o <<= 1) sm[it] += __shfl_xor_sync(0xffffffffu, sm[it], o);
+            }
+            const float inv = 1.f / (sm[0] + sm[1]);
+            A_seg[0] = e[0] * inv;
+            A_seg[1] = e[1] * inv;
+        }
+    }
+
     for (int s0 = 0; s0 < P; s0 += JC) {
         const int J = min(JC, P - s0);
         // ---- phase 1: corner records, record i = j * HW + hh
@@ -115,9 +149,12 @@ msda_forward_kernel(const __grid_constant__ FwdArgs a) {
                     } else {
                         pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
                         pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
-                        st = s_stat[warp][hh];
+                        st = seg_stats ? make_float2(0.f, 0.f) : s_stat[warp][hh];
                     }
-                    A = expf(load_stream1(a.logits + si) - st.x) * st.y;
+                    if (seg_stats)
+                        A = A_seg[(i - lane) >> 5];     // this iteration's slot
+                    else
+                        A = expf(load_stream1(a.logits + si) - st.x) * st.y;
                 } else {
                     const float2 lc = load_stream2(a.loc + 2 * si);
                     pixel_coord(lc.x, a.lv.Sx[l], a.lv.shift, x0, fx);
