@@ -168,6 +168,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
         __syncwarp();
     }
     float dotp[2] = {0.f, 0.f};        // fused: this lane's part of sum_s A_s * grad_attn_s, per slot
+    float gA_keep[2] = {0.f, 0.f};     // fused, seg_stats: this lane's grad_A per slot
 
     // seg_stats: the attention weight of each of this lane's two record slots
     // (slot it = record lane + 32 it: query (lane + 32 it) / RC, sample its
@@ -364,7 +365,10 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                                make_float2(res.y * a.lv.Rx[l], res.z * a.lv.Ry[l]));
                     else
                         __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si, make_float2(res.y, res.z));
-                    a.grad_attn[si] = res.x;           // grad of A; read back below by this lane
+                    if (seg_stats)
+                        gA_keep[it] = res.x;           // the row is this one chunk: keep grad of A
+                    else
+                        a.grad_attn[si] = res.x;       // grad of A; read back below by this lane
                     dotp[it] = __fmaf_rn(__uint_as_float(sm.rec[hh][j].w), res.x, dotp[it]);
                 } else {
                     __stcs(a.grad_attn + si, res.x);
@@ -388,6 +392,19 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
 #pragma unroll
             for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
             tot[it] = v;
+        }
+        if (seg_stats) {
+            // one chunk: A and grad_A of every sample are in registers already
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int i = lane + 32 * it;
+                const int j = i % RC, hh = i / RC;
+                const int qq = qb * HW + hh;
+                if (j < P && qq < dm.Len_q)
+                    __stcs(a.grad_attn + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + j,
+                           A_seg[it] * (gA_keep[it] - tot[it]));
+            }
+            return;
         }
         if (OPTS && dm.per_level_softmax) {
             // groups are the levels.  Their K grad_A were written by several
