@@ -164,3 +164,27 @@ def test_3d_host_checks(msda, shapes, starts, Len_in, expect):
     rc = lib.msda3d_backward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, FAKE, FAKE, None if expect == 0 else FAKE,
                              0, None, 0, None)
     assert rc == (1 if expect == 0 else expect)
+
+
+def test_index_limits_rejected_before_launch(msda):
+    """Sizes whose element offsets would not fit the kernels' 32-bit index
+    arithmetic are refused on the host (MSDA_ERR_UNSUPPORTED)."""
+    lib = msda.lib()
+    # a single level of 2^14 x 2^14 pixels: Len_in = 2^28 (corner records hold pixel indices below 2^28)
+    p = _problem(msda, Len_in=1 << 28, n_levels=1, head_dim=8, n_heads=1)
+    sh, st = _levels([1 << 14, 1 << 14], [0])
+    assert lib.msda_forward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, None) == 2
+    assert b"2^28" in lib.msda_last_error()
+    # (Len_in + 2 W + 4) * n_heads * head_dim >= 2^31
+    p = _problem(msda, Len_in=4096 * 4096, n_levels=1, head_dim=64, n_heads=2)
+    sh, st = _levels([4096, 4096], [0])
+    assert lib.msda_forward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, None) == 2
+    assert b"2^31" in lib.msda_last_error()
+    # N * Len_q * n_heads >= 2^31
+    p = _problem(msda, N=1 << 16, Len_q=1 << 12, n_heads=8)
+    sh, st = _levels([8, 8, 4, 4], [0, 64])
+    assert lib.msda_forward(ctypes.byref(p), FAKE, sh, st, FAKE, FAKE, FAKE, None) == 2
+    # the same limits for the 3-D calls
+    p = _problem(msda, Len_in=1 << 28, n_levels=1, head_dim=8, n_heads=1)
+    sh3, st3 = _levels([1 << 4, 1 << 12, 1 << 12], [0])
+    assert lib.msda3d_forward(ctypes.byref(p), FAKE, sh3, st3, FAKE, FAKE, FAKE, None) == 2
