@@ -12,8 +12,10 @@
 // Work decomposition.  A warp owns HW consecutive queries of one (n, head m)
 // ("head-major"), every lane 4 channels of one of them (R = D / 4 lanes per
 // query, HW = 32 / R).  Per chunk of up to RC samples:
-//   phase 1: one 16-byte corner record per (query, sample) into warp-private
-//            shared memory (pack_record), reads contiguous along the samples;
+//   phase 1: one 32-byte corner record per (query, sample) into warp-private
+//            shared memory: the four corners' element offsets (clamped inside
+//            the map, see pack_record), fx, fy, A and the inside-mask; reads
+//            contiguous along the samples;
 //   phase 2: per sample, four gathers of the lane's channels; the lane forms
 //            its partial <g, v_c> and from them its partial grad_attn, d/dpx,
 //            d/dpy (all linear in the dot products), which a reduce-scatter
@@ -79,7 +81,8 @@ constexpr int kMergeSamples = 4;       // samples per merge chunk (4 queries x 4
 
 template <int HW, int RC, bool MERGE>
 struct BwdWarpSmem {
-    uint4 rec[HW][RC + 1];             // corner records (padded rows)
+    int4 roff[HW][RC + 1];             // corner records: element offsets of the 4 corners (padded rows)
+    float4 raux[HW][RC + 1];           //   fx, fy, A, inside-mask bits
     float4 res[HW][RC + 1];            // per sample: grad_attn, A*d/dpx, A*d/dpy
     float2 stat[HW];                   // fused: softmax max and 1 / sum of each query
     float gdot[HW][kMaxLevels];        // fused, per-level softmax: sum_k A_k grad_A_k
@@ -87,7 +90,8 @@ struct BwdWarpSmem {
 
 template <int HW, int RC>
 struct BwdWarpSmem<HW, RC, true> {
-    uint4 rec[HW][RC + 1];
+    int4 roff[HW][RC + 1];
+    float4 raux[HW][RC + 1];
     float4 res[HW][RC + 1];
     float2 stat[HW];
     float gdot[HW][kMaxLevels];
@@ -205,7 +209,8 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
             const int j = i % RC, hh = i / RC;
             if (j >= RJ) continue;
             const int qq = qb * HW + hh;
-            uint4 rc = make_uint4(0u, 0u, 0u, 0u);
+            int4 ro = make_int4(0, 0, 0, 0);                   // outside every map: offset 0, mask 0
+            float4 ra = make_float4(0.f, 0.f, 0.f, 0.f);
             if (qq < dm.Len_q) {
                 const int l = a.level_of[r0 + j];
                 const float Wf = a.lv.Wf[l], Hf = a.lv.Hf[l];
@@ -237,9 +242,18 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                     pixel_coord(lc.y, a.lv.Sy[l], a.lv.shift, y0, fy);
                     A = load_stream1(a.attn + si);
                 }
-                rc = pack_record(x0, fx, y0, fy, A, a.lv.W[l], a.lv.H[l], Wf, Hf, a.lv.start[l]);
+                // four element offsets (relative to this lane group's value head),
+                // always inside the map, and the inside-mask; computed once here
+                // instead of by every lane of the query in phase 2
+                const uint4 pk = pack_record(x0, fx, y0, fy, A, a.lv.W[l], a.lv.H[l], Wf, Hf, a.lv.start[l]);
+                const Unpacked u = unpack_record(pk, a.lv.W[l]);
+                ro = make_int4((int)u.pix[0] * dm.pix, (int)u.pix[1] * dm.pix, (int)u.pix[2] * dm.pix,
+                               (int)u.pix[3] * dm.pix);
+                const unsigned mask = (u.in[0] ? 1u : 0u) | (u.in[1] ? 2u : 0u) | (u.in[2] ? 4u : 0u) | (u.in[3] ? 8u : 0u);
+                ra = make_float4(fx, fy, A, __uint_as_float(mask));
             }
-            sm.rec[hh][j] = rc;
+            sm.roff[hh][j] = ro;
+            sm.raux[hh][j] = ra;
         }
         __syncwarp();
         // ---- phase 2, one level (or merge chunk) at a time
@@ -255,10 +269,18 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
             // 64 that four resident blocks allow, and measured slower
 #pragma unroll 1
             for (int j = s0 - r0; j < s0 - r0 + J; ++j) {
-                const Unpacked u = unpack_record(sm.rec[h][j], W);
+                const int4 ro = sm.roff[h][j];
+                const float4 ra = sm.raux[h][j];
+                const int off[4] = {ro.x, ro.y, ro.z, ro.w};
+                const float fx = ra.x, fy = ra.y, A = ra.z;
+                const unsigned mask = __float_as_uint(ra.w);
+                const bool in[4] = {(mask & 1u) != 0, (mask & 2u) != 0, (mask & 4u) != 0, (mask & 8u) != 0};
+                // bilinear weights; an outside corner's weight is never used (its
+                // dot product is zeroed and it is not scattered)
+                const float w[4] = {(1.f - fx) * (1.f - fy), fx * (1.f - fy), (1.f - fx) * fy, fx * fy};
                 float4 v[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) v[c] = load4_value(vbase + (size_t)u.pix[c] * dm.pix, pol);
+                for (int c = 0; c < 4; ++c) v[c] = load4_value(vbase + off[c], pol);
                 // partial <g, v_c> over this lane's channels (two packed products
                 // per corner); corners outside the map read as zero
                 float t[4];
@@ -266,30 +288,29 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 for (int c = 0; c < 4; ++c) {
                     float2 pr = __fmul2_rn(make_float2(g.x, g.y), make_float2(v[c].x, v[c].y));
                     pr = __ffma2_rn(make_float2(g.z, g.w), make_float2(v[c].z, v[c].w), pr);
-                    t[c] = u.in[c] ? pr.x + pr.y : 0.f;
+                    t[c] = in[c] ? pr.x + pr.y : 0.f;
                 }
                 // partial grad_attn, d/dpx, d/dpy
-                const float pga = u.w[0] * t[0] + u.w[1] * t[1] + u.w[2] * t[2] + u.w[3] * t[3];
-                const float pdx = (1.f - u.fy) * (t[1] - t[0]) + u.fy * (t[3] - t[2]);
-                const float pdy = (1.f - u.fx) * (t[2] - t[0]) + u.fx * (t[3] - t[1]);
+                const float pga = w[0] * t[0] + w[1] * t[1] + w[2] * t[2] + w[3] * t[3];
+                const float pdx = (1.f - fy) * (t[1] - t[0]) + fy * (t[3] - t[2]);
+                const float pdy = (1.f - fx) * (t[2] - t[0]) + fx * (t[3] - t[1]);
                 float tot[2];
                 int first;
                 reduce_scatter4<R>(pga, pdx, pdy, 0.f, ch, tot, first);
                 if (R <= 4 || (ch & (R / 4 - 1)) == 0) {
                     float *rs = reinterpret_cast<float *>(&sm.res[h][j]);
-                    if (first < 3) rs[first] = first == 0 ? tot[0] : u.A * tot[0];
-                    if (R == 2 && first == 0) rs[1] = u.A * tot[1];
+                    if (first < 3) rs[first] = first == 0 ? tot[0] : A * tot[0];
+                    if (R == 2 && first == 0) rs[1] = A * tot[1];
                 }
                 if (row_ok) {
                     if (!merge) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            if (!u.in[c]) continue;
-                            const float cw = u.A * u.w[c];
+                            if (!in[c]) continue;
+                            const float cw = A * w[c];
                             const float2 lo = __fmul2_rn(make_float2(cw, cw), make_float2(g.x, g.y));
                             const float2 hi = __fmul2_rn(make_float2(cw, cw), make_float2(g.z, g.w));
-                            scatter4<DET>(a, vhead + (size_t)u.pix[c] * dm.pix, make_float4(lo.x, lo.y, hi.x, hi.y),
-                                          scale);
+                            scatter4<DET>(a, vhead + off[c], make_float4(lo.x, lo.y, hi.x, hi.y), scale);
                         }
                     } else if constexpr (MERGE) {
                         // lanes ch < 4 insert corner c = ch of their query; the valid
@@ -297,13 +318,16 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                         // one step touch the same (slot, query) coefficient
                         if (ch < 4) {
                             const int c = ch;
-                            const bool inside = c == 0 ? u.in[0] : c == 1 ? u.in[1] : c == 2 ? u.in[2] : u.in[3];
+                            const bool inside = (mask >> c) & 1u;
                             if (inside) {
-                                const unsigned key = c == 0 ? u.pix[0] : c == 1 ? u.pix[1] : c == 2 ? u.pix[2] : u.pix[3];
-                                const float coef = u.A * (c == 0 ? u.w[0] : c == 1 ? u.w[1] : c == 2 ? u.w[2] : u.w[3]);
+                                // the corner's element offset is the key (< 2^31, never kEmptyKey)
+                                const unsigned key = (unsigned)(c == 0 ? off[0] : c == 1 ? off[1] : c == 2 ? off[2] : off[3]);
+                                const float coef = A * (c == 0 ? w[0] : c == 1 ? w[1] : c == 2 ? w[2] : w[3]);
                                 // at most 64 keys per chunk in 128 slots: a free or matching
                                 // slot is always found
-                                unsigned slot = key & (kMergeSlots - 1);
+                                // offsets are multiples of n_heads * head_dim: hash, do not mask
+                                static_assert(kMergeSlots == 128, "the hash below yields 7 bits");
+                                unsigned slot = (key * 2654435761u) >> 25;
                                 for (int probe = 0; probe < kMergeSlots; ++probe) {
                                     const unsigned old = atomicCAS(&sm.key[slot], kEmptyKey, key);
                                     if (old == kEmptyKey) sm.list[atomicAdd(&sm.count, 1)] = (unsigned short)slot;
@@ -333,7 +357,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                             acc = ffma4(al.y, gall[1], acc);
                             acc = ffma4(al.z, gall[2], acc);
                             acc = ffma4(al.w, gall[3], acc);
-                            scatter4<DET>(a, vhead + (size_t)sm.key[slot] * dm.pix, acc, scale);
+                            scatter4<DET>(a, vhead + sm.key[slot], acc, scale);
                         }
                     }
                     __syncwarp();
@@ -369,7 +393,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                         gA_keep[it] = res.x;           // the row is this one chunk: keep grad of A
                     else
                         a.grad_attn[si] = res.x;       // grad of A; read back below by this lane
-                    dotp[it] = __fmaf_rn(__uint_as_float(sm.rec[hh][j].w), res.x, dotp[it]);
+                    dotp[it] = __fmaf_rn(sm.raux[hh][j].z, res.x, dotp[it]);
                 } else {
                     __stcs(a.grad_attn + si, res.x);
                     // d px / d loc = S (W, or W - 1 with align_corners)
