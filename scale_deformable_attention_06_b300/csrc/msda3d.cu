@@ -114,6 +114,35 @@ __device__ __forceinline__ Rec3 record3(const Args3 &a, int r, int s) {
                         a.lv.Dzf[l], a.lv.start[l]);
 }
 
+// ---- expanded records --------------------------------------------------------
+// Phase 1 expands a sample once, for all the lanes of its row: the eight
+// corners' element offsets (relative to the row's value head; always inside
+// the volume) with the corner's inside bit in bit 0 (offsets are multiples of
+// n_heads * head_dim >= 8), and the forward's weights (A folded in) or the
+// backward's fractions and A.
+struct Exp3 {
+    int4 o0, o1;       // offsets | inside bit, corners 0-3 and 4-7
+    float4 a, b;       // forward: A*w_c, corners 0-3 and 4-7; backward: (fx, fy, fz, A), unused
+};
+
+__device__ __forceinline__ Exp3 expand3(const Rec3 &r, int W, int HW, int pix, bool forward) {
+    const Unpacked3 u = unpack_record3(r, W, HW);
+    int o[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) o[c] = (int)u.pix[c] * pix | (u.in[c] ? 1 : 0);
+    Exp3 e;
+    e.o0 = make_int4(o[0], o[1], o[2], o[3]);
+    e.o1 = make_int4(o[4], o[5], o[6], o[7]);
+    if (forward) {
+        e.a = make_float4(u.A * u.w[0], u.A * u.w[1], u.A * u.w[2], u.A * u.w[3]);
+        e.b = make_float4(u.A * u.w[4], u.A * u.w[5], u.A * u.w[6], u.A * u.w[7]);
+    } else {
+        e.a = make_float4(u.f[0], u.f[1], u.f[2], u.A);
+        e.b = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return e;
+}
+
 // ---- forward ------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
@@ -121,7 +150,7 @@ msda3d_forward_kernel(const __grid_constant__ Args3 a) {
     using Lay = Layout<T, D>;
     constexpr int V = Lay::V, R = Lay::R, HW = Lay::HW;
     constexpr int JC = kRecordsPerWarp / HW;
-    __shared__ Rec3 s_rec[kWarpsPerBlock][HW][JC + 1];
+    __shared__ Exp3 s_rec[kWarpsPerBlock][HW][JC + 1];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = (blockIdx.x * kWarpsPerBlock + warp) * HW;
@@ -145,22 +174,28 @@ msda3d_forward_kernel(const __grid_constant__ Args3 a) {
         for (int i = lane; i < HW * JC; i += 32) {
             const int j = i % JC, hh = i / JC;
             if (j >= J) continue;
-            Rec3 rc;
-            rc.a = make_uint4(0u, 0u, 0u, 0u);      // outside every volume: weight 0, row 0
-            rc.b = make_uint4(0u, 0u, 0u, 0u);
-            if (row0 + hh < dm.rows) rc = record3(a, row0 + hh, s0 + j);
-            s_rec[warp][hh][j] = rc;
+            Exp3 e;
+            e.o0 = e.o1 = make_int4(0, 0, 0, 0);      // outside every volume: offset 0, weight 0
+            e.a = e.b = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row0 + hh < dm.rows) {
+                const int l = a.level_of[s0 + j];
+                e = expand3(record3(a, row0 + hh, s0 + j), a.lv.W[l], a.lv.H[l] * a.lv.W[l], dm.pix, true);
+            }
+            s_rec[warp][hh][j] = e;
         }
         __syncwarp();
 #pragma unroll 2
         for (int j = 0; j < J; ++j) {
-            const int l = a.level_of[s0 + j];
-            const Unpacked3 u = unpack_record3(s_rec[warp][h][j], a.lv.W[l], a.lv.H[l] * a.lv.W[l]);
+            const Exp3 &e = s_rec[warp][h][j];
+            const int4 o0 = e.o0, o1 = e.o1;
+            const float4 wa = e.a, wb = e.b;
+            const int o[8] = {o0.x & ~1, o0.y & ~1, o0.z & ~1, o0.w & ~1, o1.x & ~1, o1.y & ~1, o1.z & ~1, o1.w & ~1};
+            const float wt[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
             Vec<T> v[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) v[c] = load_value(vbase + (size_t)u.pix[c] * dm.pix, pol);
+            for (int c = 0; c < 8; ++c) v[c] = load_value(vbase + o[c], pol);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) fma_row<T, V>(acc, u.w[c] * u.A, v[c]);
+            for (int c = 0; c < 8; ++c) fma_row<T, V>(acc, wt[c], v[c]);
         }
         __syncwarp();
     }
@@ -174,7 +209,9 @@ msda3d_backward_kernel(const __grid_constant__ Args3 a) {
     constexpr int R = D / 4, HW = 32 / R;
     constexpr int RC = kRecordsPerWarp / HW;
     static_assert(HW * RC == 64, "phase 1 and 3 give every lane two (query, sample) slots");
-    __shared__ Rec3 s_rec[kWarpsPerBlock][HW][RC + 1];
+    __shared__ int4 s_o0[kWarpsPerBlock][HW][RC + 1];      // corner offsets | inside bit, corners 0-3
+    __shared__ int4 s_o1[kWarpsPerBlock][HW][RC + 1];      // corners 4-7
+    __shared__ float4 s_f[kWarpsPerBlock][HW][RC + 1];     // fx, fy, fz, A
     __shared__ float4 s_res[kWarpsPerBlock][HW][RC + 1];   // grad_attn, A*d/dpx, A*d/dpy, A*d/dpz
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -204,53 +241,66 @@ msda3d_backward_kernel(const __grid_constant__ Args3 a) {
             const int j = i % RC, hh = i / RC;
             if (j >= RJ) continue;
             const int qq = qb * HW + hh;
-            Rec3 rc;
-            rc.a = make_uint4(0u, 0u, 0u, 0u);
-            rc.b = make_uint4(0u, 0u, 0u, 0u);
-            if (qq < dm.Len_q) rc = record3(a, (n * dm.Len_q + qq) * dm.M + m, r0 + j);
-            s_rec[warp][hh][j] = rc;
+            Exp3 e;
+            e.o0 = e.o1 = make_int4(0, 0, 0, 0);
+            e.a = e.b = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (qq < dm.Len_q) {
+                const int l = a.level_of[r0 + j];
+                e = expand3(record3(a, (n * dm.Len_q + qq) * dm.M + m, r0 + j), a.lv.W[l], a.lv.H[l] * a.lv.W[l],
+                            dm.pix, false);
+            }
+            s_o0[warp][hh][j] = e.o0;
+            s_o1[warp][hh][j] = e.o1;
+            s_f[warp][hh][j] = e.a;
         }
         __syncwarp();
         // ---- phase 2: gather, partial sums, reduce-scatter, grad_value
 #pragma unroll 1
         for (int j = 0; j < RJ; ++j) {
-            const int l = a.level_of[r0 + j];
-            const Unpacked3 u = unpack_record3(s_rec[warp][h][j], a.lv.W[l], a.lv.H[l] * a.lv.W[l]);
+            const int4 o0 = s_o0[warp][h][j], o1 = s_o1[warp][h][j];
+            const float4 fr = s_f[warp][h][j];
+            const int oc[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+            const float f[3] = {fr.x, fr.y, fr.z};
+            const float A = fr.w;
             float t[8];
+            bool in[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const float4 v = load4_value(vbase + (size_t)u.pix[c] * dm.pix, pol);
-                t[c] = __fmaf_rn(g.w, v.w, __fmaf_rn(g.z, v.z, __fmaf_rn(g.y, v.y, g.x * v.x)));
+                in[c] = (oc[c] & 1) != 0;
+                const float4 v = load4_value(vbase + (oc[c] & ~1), pol);
+                float2 pr = __fmul2_rn(make_float2(g.x, g.y), make_float2(v.x, v.y));
+                pr = __ffma2_rn(make_float2(g.z, g.w), make_float2(v.z, v.w), pr);
+                t[c] = in[c] ? pr.x + pr.y : 0.f;     // outside corners read as zero
             }
-            // partial grad_attn and d/dp along each axis; outside corners read as zero
+            // partial grad_attn and d/dp along each axis (unmasked factors: outside
+            // corners have t = 0 and are not scattered)
             float pga = 0.f, pd[3] = {0.f, 0.f, 0.f};
+            float w[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const int i = c & 1, jj = (c >> 1) & 1, k = (c >> 2) & 1;
-                const float tc = u.in[c] ? t[c] : 0.f;
-                pga = __fmaf_rn(u.w[c], tc, pga);
-                // d w_c / d f_x = (i ? 1 : -1) u_y(j) u_z(k), unmasked along x
-                const float wyz = (jj ? u.f[1] : 1.f - u.f[1]) * (k ? u.f[2] : 1.f - u.f[2]);
-                const float wxz = (i ? u.f[0] : 1.f - u.f[0]) * (k ? u.f[2] : 1.f - u.f[2]);
-                const float wxy = (i ? u.f[0] : 1.f - u.f[0]) * (jj ? u.f[1] : 1.f - u.f[1]);
-                pd[0] = __fmaf_rn(i ? wyz : -wyz, tc, pd[0]);
-                pd[1] = __fmaf_rn(jj ? wxz : -wxz, tc, pd[1]);
-                pd[2] = __fmaf_rn(k ? wxy : -wxy, tc, pd[2]);
+                const float ux = i ? f[0] : 1.f - f[0], uy = jj ? f[1] : 1.f - f[1], uz = k ? f[2] : 1.f - f[2];
+                w[c] = ux * uy * uz;
+                pga = __fmaf_rn(w[c], t[c], pga);
+                // d w_c / d f_x = (i ? 1 : -1) u_y(j) u_z(k), and likewise
+                pd[0] = __fmaf_rn(i ? uy * uz : -(uy * uz), t[c], pd[0]);
+                pd[1] = __fmaf_rn(jj ? ux * uz : -(ux * uz), t[c], pd[1]);
+                pd[2] = __fmaf_rn(k ? ux * uy : -(ux * uy), t[c], pd[2]);
             }
             float tot[2];
             int first;
             reduce_scatter4<R>(pga, pd[0], pd[1], pd[2], ch, tot, first);
             if (R <= 4 || (ch & (R / 4 - 1)) == 0) {
                 float *rs = reinterpret_cast<float *>(&s_res[warp][h][j]);
-                rs[first] = first == 0 ? tot[0] : u.A * tot[0];
-                if (R == 2) rs[first + 1] = u.A * tot[1];
+                rs[first] = first == 0 ? tot[0] : A * tot[0];
+                if (R == 2) rs[first + 1] = A * tot[1];
             }
             if (row_ok) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    if (!u.in[c]) continue;
-                    const float cw = u.A * u.w[c];
-                    const size_t dst = vhead + (size_t)u.pix[c] * dm.pix;
+                    if (!in[c]) continue;
+                    const float cw = A * w[c];
+                    const size_t dst = vhead + (oc[c] & ~1);
                     if constexpr (DET) {
                         unsigned long long *p = a.fixed + dst;
                         red_add_u64(p + 0, __float2ll_rn(cw * g.x * scale));
