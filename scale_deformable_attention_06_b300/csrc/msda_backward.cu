@@ -150,25 +150,14 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
         if (lane == 0) sm.count = 0;
         __syncwarp();
     }
-    // fused, whole-row softmax: statistics in the record phase (short rows) or
-    // in a pass of their own; either way the arithmetic of the fused forward
+    // fused, whole-row softmax: statistics in the record phase when the row is
+    // one record chunk (compiled in where a chunk holds 16 logits), else in a
+    // pass of their own; the same summation tree as the fused forward either way
     const bool row_softmax = FUSED && !(OPTS && dm.per_level_softmax);
-    const bool seg_stats = SoftmaxChunk<T, D>::in_record_phase && row_softmax && P <= SoftmaxChunk<T, D>::value;
+    const bool seg_stats = (RC >= 16) && row_softmax && P <= RC;
     if (row_softmax && !seg_stats) {
-        // softmax statistics of the warp's queries (the same arithmetic as the
-        // fused forward, so A is the same value there and here)
-        for (int hh = 0; hh < HW; ++hh) {
-            const int qq = qb * HW + hh;
-            if (qq >= dm.Len_q) break;                  // warp-uniform
-            const float *lg = a.logits + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P;
-            float mx = -INFINITY;
-            for (int s = lane; s < P; s += 32) mx = fmaxf(mx, __ldg(lg + s));
-            mx = warp_max(mx);
-            float sum = 0.f;
-            for (int s = lane; s < P; s += 32) sum += expf(__ldg(lg + s) - mx);
-            sum = warp_sum(sum);
-            if (lane == 0) sm.stat[hh] = make_float2(mx, 1.f / sum);
-        }
+        row_softmax_stats(a.logits + ((size_t)(n * dm.Len_q + qb * HW) * dm.M + m) * P, (size_t)dm.M * P, P,
+                          min(HW, dm.Len_q - qb * HW), lane, sm.stat);
         __syncwarp();
     }
     float dotp[2] = {0.f, 0.f};        // fused: this lane's part of sum_s A_s * grad_attn_s, per slot

@@ -361,23 +361,58 @@ __device__ __forceinline__ int fixed_shift(unsigned bits, int rows) {
     return shift < -60 ? -60 : (shift > 100 ? 100 : shift);
 }
 
-// ---- softmax statistics inside the record phase ----------------------------
-// When all L*K logits of a row fit in one record chunk of both the forward
-// (64 / HW rows-fastest records) and the backward (64 / (128 / D) samples-
-// fastest records), the record phase holds every logit in some lane and the
-// row's max and sum come from shuffles there, with one summation tree in both
-// kernels: pairwise by sample index, zero-padded (so A is bitwise the same in
-// the fused forward and the fused backward).  Longer rows use a separate
-// statistics pass, again the same in both kernels.
-template <typename T, int D>
-struct SoftmaxChunk {
-    static constexpr int fwd = kRecordsPerWarp / Layout<T, D>::HW;
-    static constexpr int bwd = kRecordsPerWarp / (128 / D);
-    static constexpr int value = fwd < bwd ? fwd : bwd;
-    // compiled in only where it serves rows of 16 logits (4 levels x 4
-    // points); elsewhere the extra code measured slower than it saved
-    static constexpr bool in_record_phase = value >= 16;
-};
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---- softmax statistics of whole rows -----------------------------------------
+// For rows of at most 32 logits every kernel sums exp(logit - max) in one tree,
+// pairwise by sample index and zero padded to the next power of two, whichever
+// lane layout holds the logits: the record phase of the fused forward (rows
+// fastest), that of the fused backward (samples fastest), or the separate pass
+// below.  So A is bitwise the same in the fused forward and the fused backward
+// whichever path each takes.  Longer rows use a strided warp reduction, the
+// same code in both kernels.
+
+// stats[hh] = (max, 1 / sum of exp(logit - max)) of the P logits of row hh,
+// rows lg0 + hh * stride for hh < nvalid (warp-uniform arguments; all lanes).
+__device__ __forceinline__ void row_softmax_stats(const float *lg0, size_t stride, int P, int nvalid, int lane,
+                                                  float2 *stats) {
+    if (P <= 32) {
+        int P2 = 1;
+        while (P2 < P) P2 <<= 1;
+        const int per_pass = 32 / P2;
+        for (int r0 = 0; r0 < nvalid; r0 += per_pass) {
+            const int hh = r0 + lane / P2, j = lane % P2;
+            const bool valid = hh < nvalid && j < P;
+            const float x = valid ? __ldg(lg0 + hh * stride + j) : -INFINITY;
+            float mx = x;
+            for (int o = 1; o < P2; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float e = valid ? expf(x - mx) : 0.f;
+            float sum = e;
+            for (int o = 1; o < P2; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (j == 0 && hh < nvalid) stats[hh] = make_float2(mx, 1.f / sum);
+        }
+    } else {
+        for (int hh = 0; hh < nvalid; ++hh) {
+            const float *lg = lg0 + hh * stride;
+            float mx = -INFINITY;
+            for (int s = lane; s < P; s += 32) mx = fmaxf(mx, __ldg(lg + s));
+            mx = warp_max(mx);
+            float sum = 0.f;
+            for (int s = lane; s < P; s += 32) sum += expf(__ldg(lg + s) - mx);
+            sum = warp_sum(sum);
+            if (lane == 0) stats[hh] = make_float2(mx, 1.f / sum);
+        }
+    }
+}
 
 // acc[0..V) += w * v
 template <typename T, int V>
@@ -396,17 +431,6 @@ __device__ __forceinline__ void fma_row(float (&acc)[V], float w, const Vec<T> &
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] = __fmaf_rn(w, v.get(i), acc[i]);
     }
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
 }
 
 }  // namespace msda

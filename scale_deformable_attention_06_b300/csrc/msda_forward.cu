@@ -56,24 +56,13 @@ msda_forward_kernel(const __grid_constant__ FwdArgs a) {
     if (row0 >= dm.rows) return;
     const int P = dm.P;
 
-    // fused, whole-row softmax: statistics in the record phase (short rows) or
-    // in a pass of their own (rows longer than SoftmaxChunk)
+    // fused, whole-row softmax: statistics in the record phase when the row is
+    // one record chunk (compiled in where a chunk holds 16 logits), else in a
+    // pass of their own; the same summation tree either way
     const bool row_softmax = FUSED && !(OPTS && a.d.per_level_softmax);
-    const bool seg_stats = SoftmaxChunk<T, D>::in_record_phase && row_softmax && P <= SoftmaxChunk<T, D>::value;
+    const bool seg_stats = (JC >= 16) && row_softmax && P <= JC;
     if (row_softmax && !seg_stats) {
-        // softmax statistics of each row: max and 1/sum of exp(logit - max)
-        for (int h = 0; h < HW; ++h) {
-            const int row = row0 + h;
-            if (row >= dm.rows) break;                  // warp-uniform
-            const float *lg = a.logits + (size_t)row * P;
-            float mx = -INFINITY;
-            for (int s = lane; s < P; s += 32) mx = fmaxf(mx, __ldg(lg + s));
-            mx = warp_max(mx);
-            float sum = 0.f;
-            for (int s = lane; s < P; s += 32) sum += expf(__ldg(lg + s) - mx);
-            sum = warp_sum(sum);
-            if (lane == 0) s_stat[warp][h] = make_float2(mx, 1.f / sum);
-        }
+        row_softmax_stats(a.logits + (size_t)row0 * P, (size_t)P, P, min(HW, dm.rows - row0), lane, s_stat[warp]);
         __syncwarp();
     }
 
