@@ -253,7 +253,6 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
             if (merge && J > kMergeSamples) J = kMergeSamples;
             for (int jj = 1; jj < J; ++jj)
                 if (a.level_of[s0 + jj] != l) { J = jj; break; }
-            const int W = a.lv.W[l];
             // one sample at a time: unrolling raises the register count past the
             // 64 that four resident blocks allow, and measured slower
 #pragma unroll 1
