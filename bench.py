@@ -353,8 +353,30 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         return t0.elapsed_time(t1)
 
+    def copies_only(iters):
+        """The same uploads and downloads, concurrent on their two streams,
+        with no compute: the host link's floor for the pipelined step."""
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        s_out.wait_event(t0)
+        for i in range(iters):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                for h, d in zip(h_in, sets[b][0]):
+                    d.copy_(h, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                for h, d in zip(h_outs[b], sets[1 - b][1]):
+                    h.copy_(d, non_blocking=True)
+        s_in.wait_stream(s_out)
+        t1.record(s_in)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1)
+
     pipelined(4)
     e2e_s = max_over_ranks(pipelined(e2e_iters) / 1e3 / e2e_iters, dist if world > 1 else None)
+    copies_only(2)
+    link_floor_ms = copies_only(e2e_iters) / e2e_iters
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
 
@@ -398,7 +420,10 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
                 "pipeline": "double-buffered: upload of step i+1 and download of step i-1 on their own streams "
                             "while step i computes",
-                "serial_ms_per_step": e2e_serial_ms},
+                "serial_ms_per_step": e2e_serial_ms,
+                "copies_only_ms_per_step": link_floor_ms,
+                "copies_only": "the same uploads and downloads run concurrently with no compute: the host link's "
+                               "floor for the pipelined step"},
         # per step: forward 1; backward: grad_value zeroing + backward kernel
         # (+ reference-point reduction in the fused step)
         "gpu_launches": (4 if args.step == "fused" else 3) * args.steps,
