@@ -302,11 +302,7 @@ msda3d_backward_kernel(const __grid_constant__ Args3 a) {
                     const float cw = A * w[c];
                     const size_t dst = vhead + (oc[c] & ~1);
                     if constexpr (DET) {
-                        unsigned long long *p = a.fixed + dst;
-                        red_add_u64(p + 0, __float2ll_rn(cw * g.x * scale));
-                        red_add_u64(p + 1, __float2ll_rn(cw * g.y * scale));
-                        red_add_u64(p + 2, __float2ll_rn(cw * g.z * scale));
-                        red_add_u64(p + 3, __float2ll_rn(cw * g.w * scale));
+                        red_fixed4<R>(a.fixed, dst, ch, make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w), scale);
                     } else {
                         red_add_v4(a.grad_value + dst, make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w));
                     }

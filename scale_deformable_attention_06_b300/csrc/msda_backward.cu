@@ -61,15 +61,11 @@ struct BwdArgs {
     unsigned merge_mask;           // bit l: merge grad_value contributions on level l
 };
 
-// grad_value[dst .. dst + 4) += v (fp32 reduction, or fixed point)
-template <bool DET>
-__device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, float4 v, float scale) {
+// grad_value[dst .. dst + 4) += v, lane ch of R (fp32 reduction, or fixed point)
+template <bool DET, int R>
+__device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, int ch, float4 v, float scale) {
     if constexpr (DET) {
-        unsigned long long *p = a.fixed + dst;
-        red_add_u64(p + 0, __float2ll_rn(v.x * scale));
-        red_add_u64(p + 1, __float2ll_rn(v.y * scale));
-        red_add_u64(p + 2, __float2ll_rn(v.z * scale));
-        red_add_u64(p + 3, __float2ll_rn(v.w * scale));
+        red_fixed4<R>(a.fixed, dst, ch, v, scale);
     } else {
         red_add_v4(a.grad_value + dst, v);
     }
@@ -298,7 +294,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                             const float cw = A * w[c];
                             const float2 lo = __fmul2_rn(make_float2(cw, cw), make_float2(g.x, g.y));
                             const float2 hi = __fmul2_rn(make_float2(cw, cw), make_float2(g.z, g.w));
-                            scatter4<DET>(a, vhead + off[c], make_float4(lo.x, lo.y, hi.x, hi.y), scale);
+                            scatter4<DET, R>(a, vhead + off[c], ch, make_float4(lo.x, lo.y, hi.x, hi.y), scale);
                         }
                     } else if constexpr (MERGE) {
                         // lanes ch < 4 insert corner c = ch of their query; the valid
@@ -345,7 +341,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                             acc = ffma4(al.y, gall[1], acc);
                             acc = ffma4(al.z, gall[2], acc);
                             acc = ffma4(al.w, gall[3], acc);
-                            scatter4<DET>(a, vhead + sm.key[slot], acc, scale);
+                            scatter4<DET, R>(a, vhead + sm.key[slot], ch, acc, scale);
                         }
                     }
                     __syncwarp();
@@ -521,11 +517,18 @@ __global__ void row_bound_kernel(const float *attn, const T *grad_out, int rows,
     if ((threadIdx.x & 31) == 0) atomicMax(bound_bits, __float_as_uint(best));
 }
 
+// grad_value = fixed * 2^-shift, undoing the channel permutation of each
+// block of D = 4R words (red_fixed4).  The sums are below 2^62 and shift lies
+// in [-60, 100], so the scaled value is a normal float: one rounding, in the
+// int64 -> fp32 conversion; the power-of-two scaling is exact.
 __global__ void fixed_to_f32_kernel(const unsigned long long *fixed, const unsigned *bound_bits, int rows,
-                                    float *grad_value, size_t n, int accumulate) {
+                                    float *grad_value, size_t n, int D, int accumulate) {
     const int shift = fixed_shift(*bound_bits, rows);
+    const size_t R = (size_t)(D >> 2);
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const float v = (float)ldexp((double)(long long)fixed[i], -shift);
+        const size_t d = i & (size_t)(D - 1);
+        const size_t word = i - d + (d & 3) * R + (d >> 2);
+        const float v = ldexpf(__ll2float_rn((long long)fixed[word]), -shift);
         grad_value[i] = accumulate ? grad_value[i] + v : v;
     }
 }
@@ -598,7 +601,7 @@ cudaError_t backward_finish(const LaunchGeometry &g, int D, float *grad_value, b
                             const unsigned long long *fixed, const unsigned *bound, cudaStream_t stream) {
     const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
     if (det && nval > 0)
-        fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(fixed, bound, g.d.rows, grad_value, nval,
+        fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(fixed, bound, g.d.rows, grad_value, nval, D,
                                                                       accumulate ? 1 : 0);
     return cudaGetLastError();
 }
@@ -683,7 +686,7 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
     }
     if (det && nval > 0)
         fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(a.fixed, a.bound_bits, g.d.rows, io.grad_value,
-                                                                      nval, accumulate ? 1 : 0);
+                                                                      nval, D, accumulate ? 1 : 0);
     return cudaGetLastError();
 }
 

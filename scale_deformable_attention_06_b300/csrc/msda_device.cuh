@@ -350,6 +350,21 @@ __device__ __forceinline__ void red_add_u64(unsigned long long *p, long long v) 
     asm volatile("red.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Fixed-point accumulators of the deterministic backward.  Within each
+// (pixel, head) block of D = 4R words the channels are permuted: channel
+// 4*ch + i, the i-th of lane ch's four, sits at word i*R + ch.  Each of a
+// lane's four 64-bit reductions then covers, over the R lanes of one query,
+// R consecutive words, not R words 32 bytes apart (a quarter of the sectors).
+// dst: element offset of channel 4*ch of the block, as for the fp32 buffer.
+template <int R>
+__device__ __forceinline__ void red_fixed4(unsigned long long *fixed, size_t dst, int ch, float4 v, float scale) {
+    unsigned long long *p = fixed + (dst - 3 * (size_t)ch);
+    red_add_u64(p, __float2ll_rn(v.x * scale));
+    red_add_u64(p + R, __float2ll_rn(v.y * scale));
+    red_add_u64(p + 2 * R, __float2ll_rn(v.z * scale));
+    red_add_u64(p + 3 * R, __float2ll_rn(v.w * scale));
+}
+
 // Power-of-two scale of the fixed-point sums: every partial sum is at most
 // rows * max_row_bound < 2^62 after scaling.
 __device__ __forceinline__ int fixed_shift(unsigned bits, int rows) {
