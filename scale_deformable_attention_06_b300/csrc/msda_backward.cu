@@ -82,6 +82,7 @@ struct BwdWarpSmem {
     float4 res[HW][RC + 1];            // per sample: grad_attn, A*d/dpx, A*d/dpy
     float2 stat[HW];                   // fused: softmax max and 1 / sum of each query
     float gdot[HW][kMaxLevels];        // fused, per-level softmax: sum_k A_k grad_A_k
+    float dotp[64];                    // fused: per (query, sample) slot, sum of A * grad_A
 };
 
 template <int HW, int RC>
@@ -91,6 +92,7 @@ struct BwdWarpSmem<HW, RC, true> {
     float4 res[HW][RC + 1];
     float2 stat[HW];
     float gdot[HW][kMaxLevels];
+    float dotp[64];
     unsigned key[kMergeSlots];         // corner pixel of the slot, kEmptyKey if free
     float4 alpha[kMergeSlots];         // per query of the warp: summed A * w_c (HW == 4)
     unsigned short list[kMergeSlots];  // occupied slots in order of first use
@@ -156,42 +158,36 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                           min(HW, dm.Len_q - qb * HW), lane, sm.stat);
         __syncwarp();
     }
-    float dotp[2] = {0.f, 0.f};        // fused: this lane's part of sum_s A_s * grad_attn_s, per slot
-    float gA_keep[2] = {0.f, 0.f};     // fused, seg_stats: this lane's grad_A per slot
-
-    // seg_stats: the attention weight of each of this lane's two record slots
-    // (slot it = record lane + 32 it: query (lane + 32 it) / RC, sample its
-    // remainder; a query's samples are RC consecutive lanes)
-    float A_seg[2] = {0.f, 0.f};
+    // fused: slot it of lane i is query (lane + 32 it) / RC, sample its
+    // remainder (a query's samples are RC consecutive slots); each lane alone
+    // reads and writes its two slots' partial sums of A * grad_A
     if constexpr (FUSED) {
-        if (seg_stats) {                                // warp-uniform; the row is one chunk
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int i = lane + 32 * it, j = i % RC, hh = i / RC;
-                const int qq = qb * HW + hh;
-                const bool valid = j < P && qq < dm.Len_q;
-                const float lg = valid ? __ldg(a.logits + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + j)
-                                       : -INFINITY;
-                float mx = lg;
-#pragma unroll
-                for (int o = 1; o < RC && o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                const float e = valid ? expf(lg - mx) : 0.f;
-                float sum = e;
-#pragma unroll
-                for (int o = 1; o < RC && o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                const float inv = 1.f / sum;
-                A_seg[it] = e * inv;
-                if (j == 0 && qq < dm.Len_q) sm.stat[hh] = make_float2(mx, inv);
-            }
-            __syncwarp();
-        }
+        sm.dotp[lane] = 0.f;
+        sm.dotp[lane + 32] = 0.f;
     }
 
     for (int r0 = 0; r0 < P; r0 += RC) {
         const int RJ = min(RC, P - r0);
         // ---- phase 1: corner records of samples r0 .. r0 + RJ
-        for (int i = lane; i < HW * RC; i += 32) {
+        for (int i = lane; i < HW * RC; i += 32) {    // two iterations on every lane
             const int j = i % RC, hh = i / RC;
+            float A_slot = 0.f;
+            if constexpr (FUSED) {
+                if (seg_stats) {    // warp-uniform: the row is this one chunk; its softmax, a slot per lane
+                    const int qq = qb * HW + hh;
+                    const bool valid = j < P && qq < dm.Len_q;
+                    const float lg = valid ? __ldg(a.logits + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + j)
+                                           : -INFINITY;
+                    float mx = lg;
+#pragma unroll
+                    for (int o = 1; o < RC && o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    const float e = valid ? expf(lg - mx) : 0.f;
+                    float sum = e;
+#pragma unroll
+                    for (int o = 1; o < RC && o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                    A_slot = e * (1.f / sum);
+                }
+            }
             if (j >= RJ) continue;
             const int qq = qb * HW + hh;
             int4 ro = make_int4(0, 0, 0, 0);                   // outside every map: offset 0, mask 0
@@ -204,23 +200,23 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 if constexpr (FUSED) {
                     const float2 rf = __ldg(reinterpret_cast<const float2 *>(a.ref) + (size_t)(n * dm.Len_q + qq) * dm.L + l);
                     const float2 of = load_stream2(a.off + 2 * si);
-                    float2 st;
                     if constexpr (OPTS) {
                         pixel_coord_fused(rf.x, of.x, a.lv.Sx[l], a.lv.Rx[l], a.lv.shift, x0, fx);
                         pixel_coord_fused(rf.y, of.y, a.lv.Sy[l], a.lv.Ry[l], a.lv.shift, y0, fy);
-                        if (dm.per_level_softmax)
-                            group_softmax_stats(a.logits + (si - (r0 + j)) + l * dm.K, dm.K, st.x, st.y);
-                        else
-                            st = sm.stat[hh];
                     } else {
                         pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
                         pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
-                        st = sm.stat[hh];
                     }
-                    if (seg_stats)
-                        A = A_seg[(i - lane) >> 5];     // this iteration's slot
-                    else
+                    if (seg_stats) {
+                        A = A_slot;
+                    } else {
+                        float2 st;
+                        if (OPTS && dm.per_level_softmax)
+                            group_softmax_stats(a.logits + (si - (r0 + j)) + l * dm.K, dm.K, st.x, st.y);
+                        else
+                            st = sm.stat[hh];
                         A = expf(load_stream1(a.logits + si) - st.x) * st.y;
+                    }
                 } else {
                     const float2 lc = load_stream2(a.loc + 2 * si);
                     pixel_coord(lc.x, a.lv.Sx[l], a.lv.shift, x0, fx);
@@ -373,11 +369,13 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                                make_float2(res.y * a.lv.Rx[l], res.z * a.lv.Ry[l]));
                     else
                         __stcs(reinterpret_cast<float2 *>(a.grad_loc) + si, make_float2(res.y, res.z));
-                    if (seg_stats)
-                        gA_keep[it] = res.x;           // the row is this one chunk: keep grad of A
-                    else
-                        a.grad_attn[si] = res.x;       // grad of A; read back below by this lane
-                    dotp[it] = __fmaf_rn(sm.raux[hh][j].z, res.x, dotp[it]);
+                    // one chunk (seg_stats): A and grad_A stay in raux and res for the
+                    // closing pass; else grad_A goes to grad_attn, read back below by
+                    // this lane, and the slot's A * grad_A to its partial sum
+                    if (!seg_stats) {
+                        a.grad_attn[si] = res.x;
+                        sm.dotp[i] = __fmaf_rn(sm.raux[hh][j].z, res.x, sm.dotp[i]);
+                    }
                 } else {
                     __stcs(a.grad_attn + si, res.x);
                     // d px / d loc = S (W, or W - 1 with align_corners)
@@ -393,26 +391,30 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
         // Slot it of lane i covers query (lane + 32 it) / RC; the lanes of one
         // query form an aligned group of min(RC, 32), summed in a fixed order.
         constexpr int G = RC < 32 ? RC : 32;
-        float tot[2];
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            float v = dotp[it];
-#pragma unroll
-            for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            tot[it] = v;
-        }
         if (seg_stats) {
-            // one chunk: A and grad_A of every sample are in registers already
+            // one chunk: A and grad_A of every sample are still in raux and res
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
                 const int i = lane + 32 * it;
                 const int j = i % RC, hh = i / RC;
                 const int qq = qb * HW + hh;
-                if (j < P && qq < dm.Len_q)
-                    __stcs(a.grad_attn + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + j,
-                           A_seg[it] * (gA_keep[it] - tot[it]));
+                const bool ok = j < P && qq < dm.Len_q;
+                const float A = ok ? sm.raux[hh][j].z : 0.f, gA = ok ? sm.res[hh][j].x : 0.f;
+                float v = __fmaf_rn(A, gA, 0.f);
+#pragma unroll
+                for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (ok)
+                    __stcs(a.grad_attn + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * P + j, A * (gA - v));
             }
             return;
+        }
+        float tot[2];
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            float v = sm.dotp[lane + 32 * it];
+#pragma unroll
+            for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            tot[it] = v;
         }
         if (OPTS && dm.per_level_softmax) {
             // groups are the levels.  Their K grad_A were written by several
