@@ -520,18 +520,27 @@ __global__ void row_bound_kernel(const float *attn, const T *grad_out, int rows,
 }
 
 // grad_value = fixed * 2^-shift, undoing the channel permutation of each
-// block of D = 4R words (red_fixed4).  The sums are below 2^62 and shift lies
-// in [-60, 100], so the scaled value is a normal float: one rounding, in the
+// block of D = 4R words (red_fixed4): thread t writes the 4 channels of lane
+// ch = t mod R of its block, words ch, R + ch, 2R + ch, 3R + ch (consecutive
+// threads read consecutive words).  The sums are below 2^62 and shift lies in
+// [-60, 100], so the scaled value is a normal float: one rounding, in the
 // int64 -> fp32 conversion; the power-of-two scaling is exact.
 __global__ void fixed_to_f32_kernel(const unsigned long long *fixed, const unsigned *bound_bits, int rows,
-                                    float *grad_value, size_t n, int D, int accumulate) {
+                                    float4 *grad_value, size_t n4, int D, int accumulate) {
     const int shift = fixed_shift(*bound_bits, rows);
     const size_t R = (size_t)(D >> 2);
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const size_t d = i & (size_t)(D - 1);
-        const size_t word = i - d + (d & 3) * R + (d >> 2);
-        const float v = ldexpf(__ll2float_rn((long long)fixed[word]), -shift);
-        grad_value[i] = accumulate ? grad_value[i] + v : v;
+    for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n4; t += (size_t)gridDim.x * blockDim.x) {
+        const size_t ch = t & (R - 1);
+        const unsigned long long *w = fixed + (t - ch) * 4 + ch;
+        float4 v = make_float4(ldexpf(__ll2float_rn((long long)__ldcs(w)), -shift),
+                               ldexpf(__ll2float_rn((long long)__ldcs(w + R)), -shift),
+                               ldexpf(__ll2float_rn((long long)__ldcs(w + 2 * R)), -shift),
+                               ldexpf(__ll2float_rn((long long)__ldcs(w + 3 * R)), -shift));
+        if (accumulate) {
+            const float4 o = grad_value[t];
+            v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+        }
+        grad_value[t] = v;
     }
 }
 
@@ -603,8 +612,8 @@ cudaError_t backward_finish(const LaunchGeometry &g, int D, float *grad_value, b
                             const unsigned long long *fixed, const unsigned *bound, cudaStream_t stream) {
     const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
     if (det && nval > 0)
-        fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(fixed, bound, g.d.rows, grad_value, nval, D,
-                                                                      accumulate ? 1 : 0);
+        fixed_to_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(
+            fixed, bound, g.d.rows, reinterpret_cast<float4 *>(grad_value), nval / 4, D, accumulate ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -687,8 +696,9 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
         }
     }
     if (det && nval > 0)
-        fixed_to_f32_kernel<<<grid_for(nval, 256), 256, 0, stream>>>(a.fixed, a.bound_bits, g.d.rows, io.grad_value,
-                                                                      nval, D, accumulate ? 1 : 0);
+        fixed_to_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(
+            a.fixed, a.bound_bits, g.d.rows, reinterpret_cast<float4 *>(io.grad_value), nval / 4, D,
+            accumulate ? 1 : 0);
     return cudaGetLastError();
 }
 
