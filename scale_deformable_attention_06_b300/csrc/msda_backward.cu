@@ -154,7 +154,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     const bool row_softmax = FUSED && !(OPTS && dm.per_level_softmax);
     const bool seg_stats = (RC >= 16) && row_softmax && P <= RC;
     if (row_softmax && !seg_stats) {
-        row_softmax_stats(a.logits + ((size_t)(n * dm.Len_q + qb * HW) * dm.M + m) * P, (size_t)dm.M * P, P,
+        row_softmax_stats<HW>(a.logits + ((size_t)(n * dm.Len_q + qb * HW) * dm.M + m) * P, (size_t)dm.M * P, P,
                           min(HW, dm.Len_q - qb * HW), lane, sm.stat);
         __syncwarp();
     }

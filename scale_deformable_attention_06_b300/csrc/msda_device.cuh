@@ -397,23 +397,39 @@ __device__ __forceinline__ float warp_sum(float v) {
 // same code in both kernels.
 
 // stats[hh] = (max, 1 / sum of exp(logit - max)) of the P logits of row hh,
-// rows lg0 + hh * stride for hh < nvalid (warp-uniform arguments; all lanes).
+// rows lg0 + hh * stride for hh < nvalid <= NR (warp-uniform arguments; all
+// lanes).  P <= 32: a row takes P2 (P rounded up to a power of two) lanes, a
+// pass 32 / P2 rows, and the max and the sum are xor trees over the row's
+// lanes.  The logits of up to four passes are loaded before their trees, so a
+// warp waits for one round of loads per four passes, not one per pass.
+template <int NR>
 __device__ __forceinline__ void row_softmax_stats(const float *lg0, size_t stride, int P, int nvalid, int lane,
                                                   float2 *stats) {
     if (P <= 32) {
+        constexpr int G = NR < 4 ? NR : 4;
         int P2 = 1;
         while (P2 < P) P2 <<= 1;
         const int per_pass = 32 / P2;
-        for (int r0 = 0; r0 < nvalid; r0 += per_pass) {
-            const int hh = r0 + lane / P2, j = lane % P2;
-            const bool valid = hh < nvalid && j < P;
-            const float x = valid ? __ldg(lg0 + hh * stride + j) : -INFINITY;
-            float mx = x;
-            for (int o = 1; o < P2; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float e = valid ? expf(x - mx) : 0.f;
-            float sum = e;
-            for (int o = 1; o < P2; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            if (j == 0 && hh < nvalid) stats[hh] = make_float2(mx, 1.f / sum);
+        const int j = lane % P2, hl = lane / P2;
+        for (int p0 = 0; p0 * per_pass < nvalid; p0 += G) {
+            float x[G];                 // pass p0 + u: row (p0 + u) * per_pass + hl
+#pragma unroll
+            for (int u = 0; u < G; ++u) {
+                const int hh = (p0 + u) * per_pass + hl;
+                x[u] = (hh < nvalid && j < P) ? __ldg(lg0 + hh * stride + j) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < G; ++u) {
+                if ((p0 + u) * per_pass >= nvalid) break;   // warp-uniform
+                const int hh = (p0 + u) * per_pass + hl;
+                const bool valid = hh < nvalid && j < P;
+                float mx = x[u];
+                for (int o = 1; o < P2; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float e = valid ? expf(x[u] - mx) : 0.f;
+                float sum = e;
+                for (int o = 1; o < P2; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                if (j == 0 && hh < nvalid) stats[hh] = make_float2(mx, 1.f / sum);
+            }
         }
     } else {
         for (int hh = 0; hh < nvalid; ++hh) {

@@ -37,11 +37,16 @@ struct FwdArgs {
     int opts;                              // any option bit set
 };
 
-// OPTS: the problem sets option bits (fused calls); without them the kernel
-// carries none of the option code.
+// Resident blocks per SM the fp32 kernels are compiled for (at most 48
+// registers a thread): faster on the fp32 gathers than the compiler's own
+// choice.  The bf16 kernels keep the compiler's choice, which measured faster
+// for them.
+constexpr int kFwdMinBlocksF32 = 5;
+
+// The kernel body.  OPTS: the problem sets option bits (fused calls); without
+// them the kernel carries none of the option code.
 template <typename T, int D, bool FUSED, bool OPTS>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-msda_forward_kernel(const __grid_constant__ FwdArgs a) {
+__device__ __forceinline__ void forward_body(const FwdArgs &a) {
     using Lay = Layout<T, D>;
     constexpr int V = Lay::V, R = Lay::R, HW = Lay::HW;
     constexpr int JC = kRecordsPerWarp / HW;     // samples of each row per chunk
@@ -62,7 +67,7 @@ msda_forward_kernel(const __grid_constant__ FwdArgs a) {
     const bool row_softmax = FUSED && !(OPTS && a.d.per_level_softmax);
     const bool seg_stats = (JC >= 16) && row_softmax && P <= JC;
     if (row_softmax && !seg_stats) {
-        row_softmax_stats(a.logits + (size_t)row0 * P, (size_t)P, P, min(HW, dm.rows - row0), lane, s_stat[warp]);
+        row_softmax_stats<HW>(a.logits + (size_t)row0 * P, (size_t)P, P, min(HW, dm.rows - row0), lane, s_stat[warp]);
         __syncwarp();
     }
 
@@ -177,15 +182,35 @@ msda_forward_kernel(const __grid_constant__ FwdArgs a) {
     if (row_ok) store_row<T, V>(static_cast<T *>(a.out) + (size_t)row * D + ch * V, acc);
 }
 
+template <typename T, int D, bool FUSED, bool OPTS>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kFwdMinBlocksF32)
+msda_forward_kernel(const __grid_constant__ FwdArgs a) {       // fp32 value
+    forward_body<T, D, FUSED, OPTS>(a);
+}
+
+template <typename T, int D, bool FUSED, bool OPTS>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+msda_forward_kernel_bf16(const __grid_constant__ FwdArgs a) {  // bf16 value
+    forward_body<T, D, FUSED, OPTS>(a);
+}
+
 template <typename T, int D, bool FUSED>
 static cudaError_t launch_fwd(const FwdArgs &args, cudaStream_t stream) {
     constexpr int HW = Layout<T, D>::HW;
     const long long warps = ((long long)args.d.rows + HW - 1) / HW;
     const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (FUSED && args.opts)
-        msda_forward_kernel<T, D, FUSED, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
-    else
-        msda_forward_kernel<T, D, FUSED, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    const bool opts = FUSED && args.opts;
+    if constexpr (sizeof(T) == 4) {
+        if (opts)
+            msda_forward_kernel<T, D, FUSED, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+        else
+            msda_forward_kernel<T, D, FUSED, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    } else {
+        if (opts)
+            msda_forward_kernel_bf16<T, D, FUSED, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+        else
+            msda_forward_kernel_bf16<T, D, FUSED, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    }
     return cudaGetLastError();
 }
 
