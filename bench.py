@@ -86,9 +86,21 @@ def algorithmic_bytes(w):
     return {"fwd": fwd, "bwd": bwd, "fused_fwd": fused, "fused_bwd": fused_bwd}
 
 
-def kernel_source_hash():
+# The source files each profiled kernel is built from (its translation unit
+# and the headers it includes).
+KERNEL_SOURCES = {
+    "msda_forward_kernel": ("msda_forward.cu", "msda_device.cuh", "msda_launch.h"),
+    "msda_backward_kernel": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
+    "msda_backward_kernel_fused": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
+    "ref_grad_kernel": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
+}
+
+
+def kernel_source_hash(kernel=None):
+    """Hash of the sources of `kernel` (of every kernel source when None)."""
+    files = KERNEL_SOURCES[kernel] if kernel else sorted(os.listdir(CSRC))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
+    for f in files:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -96,15 +108,16 @@ def kernel_source_hash():
 
 def profiled_traffic(kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when the kernels changed since it was captured."""
+    None when the kernel's sources changed since it was captured."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    k = rec.get("kernels", {}).get(kernel, {})
+    if not k or k.get("source_hash") != kernel_source_hash(kernel):
         return None
-    return rec.get("kernels", {}).get(kernel, {}).get("dram_bytes_per_launch")
+    return k.get("dram_bytes_per_launch")
 
 
 def measured_peak():
