@@ -404,3 +404,83 @@ def test_3d_one_slice_is_2d(msda):
     out3 = msda.msda3d_forward(H.dev(p["value"]), sh3, p["level_start_index"], H.dev(loc3),
                                H.dev(p["attention_weights"])).cpu().numpy()
     assert np.abs(out3 - out2).max() <= 1e-5
+
+
+# ----------------------------------------------------------------- the top of the index range
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_element_offsets_near_2_31(msda, dtype):
+    """Element offsets (pixel * n_heads * head_dim) within 0.4% of 2^31, the
+    largest the host checks accept: a 2048 x 2040 level, then a 4 x 4 level
+    whose rows start at element 2.139e9 (8.6 GB of fp32 value).  The first
+    level's samples lie far outside it (all four corners padded) and, in the
+    fused calls, its logits are -1e4, whose weights are exactly 0 in fp32 and
+    fp64.  Every result on the small level then equals the oracle's on the
+    1-level problem made of that level's data alone, and everything on the
+    large level is exactly zero."""
+    M, D, Lq, K = 8, 64, 64, 2
+    big, small = (2048, 2040), (4, 4)
+    start1 = big[0] * big[1]
+    Len_in = start1 + small[0] * small[1]
+    assert (Len_in + 2 * big[1] + 4) * M * D < 2 ** 31 <= (Len_in + 2 * big[1] + 4) * M * D * 1.01
+    rng = np.random.Generator(np.random.PCG64(2031))
+    value_s = rng.standard_normal((1, 16, M, D)).astype(np.float32)
+    g = rng.standard_normal((1, Lq, M * D)).astype(np.float32)
+    if dtype == "bf16":
+        value_s, g = H.bf16_round(value_s), H.bf16_round(g)
+    loc_s = rng.uniform(-0.15, 1.15, (1, Lq, M, 1, K, 2)).astype(np.float32)     # some corners padded
+    attn_s = rng.uniform(0.1, 1.0, (1, Lq, M, 1, K)).astype(np.float32)
+    ref_s = rng.uniform(0.1, 0.9, (1, Lq, 1, 2)).astype(np.float32)
+    off_s = rng.normal(0.0, 1.0, (1, Lq, M, 1, K, 2)).astype(np.float32)         # pixels of the 4 x 4 level
+    logit_s = rng.standard_normal((1, Lq, M, K)).astype(np.float32)
+    sh_s, st_s = np.array([small], np.int64), np.array([0], np.int64)
+    sh = np.array([big, small], np.int64)
+    st = np.array([0, start1], np.int64)
+
+    # the two-level problem on the device: zeros on the large level
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    value = torch.zeros((1, Len_in, M, D), dtype=dt, device="cuda")
+    value[0, start1:] = torch.from_numpy(value_s[0]).to(device="cuda", dtype=dt)
+    loc = np.concatenate([np.full((1, Lq, M, 1, K, 2), -3.0, np.float32), loc_s], axis=3)
+    attn = np.concatenate([np.full((1, Lq, M, 1, K), 0.3, np.float32), attn_s], axis=3)
+    ref = np.concatenate([np.full((1, Lq, 1, 2), -3.0, np.float32), ref_s], axis=2)
+    off = np.concatenate([np.zeros((1, Lq, M, 1, K, 2), np.float32), off_s], axis=3)
+    logit = np.concatenate([np.full((1, Lq, M, K), -1e4, np.float32), logit_s], axis=3)
+    gd = H.dev(g, dt)
+
+    def small_level(x):            # [N, Len_in, M, D] -> the small level's rows, and the rest's largest |x|
+        lo, hi = torch.aminmax(x[0, :start1])
+        rest = max(-float(lo), float(hi))
+        return x[:, start1:].cpu().numpy(), rest
+
+    # unfused
+    out = msda.msda_forward(value, sh, st, H.dev(loc), H.dev(attn)).float().cpu().numpy()
+    H.assert_fwd(out, oracle.forward(value_s, sh_s, st_s, loc_s, attn_s), dtype, "forward near 2^31")
+    gv_r, gl_r, ga_r = oracle.backward(value_s, sh_s, st_s, loc_s, attn_s, g)
+    for flags in (0, msda.MSDA_DETERMINISTIC):
+        gv, gl, ga = msda.msda_backward(value, sh, st, H.dev(loc), H.dev(attn), gd, flags=flags)
+        gv_small, gv_rest = small_level(gv)
+        assert gv_rest == 0.0, f"grad_value on the outside level: {gv_rest}"
+        gl, ga = gl.cpu().numpy(), ga.cpu().numpy()
+        assert not gl[:, :, :, 0].any() and not ga[:, :, :, 0].any()
+        H.assert_bwd(gv_small, gv_r, "f32", f"grad_value near 2^31 (flags {flags})")
+        H.assert_bwd(gl[:, :, :, 1:], gl_r, "f32", f"grad_loc near 2^31 (flags {flags})")
+        H.assert_bwd(ga[:, :, :, 1:], ga_r, "f32", f"grad_attn near 2^31 (flags {flags})")
+        del gv
+    # fused
+    fo = msda.msda_forward_fused(value, sh, st, H.dev(ref), H.dev(off), H.dev(logit.reshape(1, Lq, M, 2 * K)))
+    H.assert_fwd(fo.float().cpu().numpy(), oracle.forward_fused(value_s, sh_s, st_s, ref_s, off_s, logit_s), dtype,
+                 "fused forward near 2^31")
+    fr = oracle.backward_fused(value_s, sh_s, st_s, ref_s, off_s, logit_s, g)
+    for flags in (0, msda.MSDA_DETERMINISTIC):
+        gv, gref, goff, glog = msda.msda_backward_fused(value, sh, st, H.dev(ref), H.dev(off),
+                                                        H.dev(logit.reshape(1, Lq, M, 2 * K)), gd, flags=flags)
+        gv_small, gv_rest = small_level(gv)
+        assert gv_rest == 0.0, f"fused grad_value on the outside level: {gv_rest}"
+        gref, goff = gref.cpu().numpy(), goff.cpu().numpy()
+        glog = glog.cpu().numpy().reshape(1, Lq, M, 2, K)
+        assert not gref[:, :, 0].any() and not goff[:, :, :, 0].any() and not glog[:, :, :, 0].any()
+        H.assert_bwd(gv_small, fr[0], "f32", f"fused grad_value near 2^31 (flags {flags})")
+        H.assert_bwd(gref[:, :, 1:], fr[1], "f32", f"fused grad_ref near 2^31 (flags {flags})")
+        H.assert_bwd(goff[:, :, :, 1:], fr[2], "f32", f"fused grad_off near 2^31 (flags {flags})")
+        H.assert_bwd(glog[:, :, :, 1], fr[3].reshape(1, Lq, M, K), "f32", f"fused grad_logit near 2^31 (flags {flags})")
+        del gv
