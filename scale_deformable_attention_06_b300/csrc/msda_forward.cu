@@ -61,15 +61,17 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     if (row0 >= dm.rows) return;
     const int P = dm.P;
 
-    // fused, whole-row softmax: statistics in the record phase when the row is
-    // one record chunk (compiled in where a chunk holds 16 logits), else in a
-    // pass of their own; the same summation tree either way
+    // fused, whole-row softmax.  A row that is one record chunk (compiled in
+    // where a chunk holds 16 logits) gets its statistics in the record phase
+    // and normalised weights.  A row of several chunks is summed online: each
+    // chunk's record phase updates the row's running max and sum and keeps the
+    // weights relative to that max, the gather phase first rescales the
+    // accumulator by exp(old max - new max), and the output is divided by the
+    // sum at the end, so no pass over the logits precedes the gathers.
     const bool row_softmax = FUSED && !(OPTS && a.d.per_level_softmax);
     const bool seg_stats = (JC >= 16) && row_softmax && P <= JC;
-    if (row_softmax && !seg_stats) {
-        row_softmax_stats<HW>(a.logits + (size_t)row0 * P, (size_t)P, P, min(HW, dm.rows - row0), lane, s_stat[warp]);
-        __syncwarp();
-    }
+    const bool online = row_softmax && !seg_stats;
+    float run_max = -INFINITY, run_sum = 0.f;      // online: of row lane % HW (phase-1 role)
 
     // phase-2 lane role
     const int h = lane / R, ch = lane % R;
@@ -117,6 +119,35 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
 
     for (int s0 = 0; s0 < P; s0 += JC) {
         const int J = min(JC, P - s0);
+        // online softmax: exp(logit - running max) of this lane's two record
+        // slots (slot it = record lane + 32 it, row lane % HW, sample its / HW);
+        // the row's lanes are those with the same lane % HW
+        float e_slot[2] = {0.f, 0.f};
+        if constexpr (FUSED) {
+            if (online) {                                   // warp-uniform
+                const int r = row0 + lane % HW;
+                float lg[2];
+#pragma unroll
+                for (int it = 0; it < 2; ++it) {
+                    const int j = (lane + 32 * it) / HW;
+                    lg[it] = (j < J && r < dm.rows) ? __ldg(a.logits + (size_t)r * P + s0 + j) : -INFINITY;
+                }
+                float cm = fmaxf(lg[0], lg[1]);
+#pragma unroll
+                for (int o = HW; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+                const float m_new = fmaxf(run_max, cm);
+                // first chunk: exp(-inf) = 0; a row outside the problem keeps scale 1
+                const float scale = m_new == -INFINITY ? 1.f : expf(run_max - m_new);
+#pragma unroll
+                for (int it = 0; it < 2; ++it) e_slot[it] = lg[it] == -INFINITY ? 0.f : expf(lg[it] - m_new);
+                float cs = e_slot[0] + e_slot[1];
+#pragma unroll
+                for (int o = HW; o < 32; o <<= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
+                run_sum = __fmaf_rn(run_sum, scale, cs);
+                run_max = m_new;
+                if (lane < HW) s_stat[warp][lane] = make_float2(scale, run_sum);
+            }
+        }
         // ---- phase 1: corner records, record i = j * HW + hh
         for (int i = lane; i < HW * J; i += 32) {
             const int hh = i % HW, j = i / HW;
@@ -132,23 +163,22 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
                     const int nq = r / dm.M;            // (n, q) of this row
                     const float2 rf = __ldg(reinterpret_cast<const float2 *>(a.ref) + (size_t)nq * dm.L + l);
                     const float2 of = load_stream2(a.off + 2 * si);
-                    float2 st;
+                    float2 st = make_float2(0.f, 1.f);      // per-level groups only
                     if constexpr (OPTS) {
                         pixel_coord_fused(rf.x, of.x, a.lv.Sx[l], a.lv.Rx[l], a.lv.shift, x0, fx);
                         pixel_coord_fused(rf.y, of.y, a.lv.Sy[l], a.lv.Ry[l], a.lv.shift, y0, fy);
                         if (dm.per_level_softmax)       // the level's K logits are this sample's group
                             group_softmax_stats(a.logits + (size_t)r * P + l * dm.K, dm.K, st.x, st.y);
-                        else
-                            st = s_stat[warp][hh];
                     } else {
                         pixel_coord_fused(rf.x, of.x, Wf, x0, fx);
                         pixel_coord_fused(rf.y, of.y, Hf, y0, fy);
-                        st = seg_stats ? make_float2(0.f, 0.f) : s_stat[warp][hh];
                     }
-                    if (seg_stats)
+                    if (!row_softmax)                   // per-level groups
+                        A = expf(load_stream1(a.logits + si) - st.x) * st.y;
+                    else if (seg_stats)
                         A = A_seg[(i - lane) >> 5];     // this iteration's slot
                     else
-                        A = expf(load_stream1(a.logits + si) - st.x) * st.y;
+                        A = e_slot[(i - lane) >> 5];    // relative to the running max
                 } else {
                     const float2 lc = load_stream2(a.loc + 2 * si);
                     pixel_coord(lc.x, a.lv.Sx[l], a.lv.shift, x0, fx);
@@ -164,6 +194,13 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         }
         __syncwarp();
         // ---- phase 2: gathers of this lane's row
+        if constexpr (FUSED) {
+            if (online) {                                   // rescale to the row's new running max
+                const float sc = s_stat[warp][h].x;
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[v] *= sc;
+            }
+        }
 #pragma unroll 2
         for (int j = 0; j < J; ++j) {
             const int4 o = s_off[warp][j * HW + h];
@@ -178,6 +215,13 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
             fma_row<T, V>(acc, w.w, v3);
         }
         __syncwarp();
+    }
+    if constexpr (FUSED) {
+        if (online) {                                       // divide by the row's sum
+            const float inv = 1.f / s_stat[warp][h].y;
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] *= inv;
+        }
     }
     if (row_ok) store_row<T, V>(static_cast<T *>(a.out) + (size_t)row * D + ch * V, acc);
 }

@@ -307,6 +307,33 @@ def test_fused_backward_dense_merge_and_accumulate(msda):
         H.assert_bwd(gv.cpu().numpy(), gv0 + ref[0], "f32", "fused accumulated grad_value")
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 8), ("f32", 16), ("bf16", 32), ("f32", 64)])
+@pytest.mark.parametrize("trend", ["rising", "falling", "spike"])
+def test_fused_forward_rows_of_many_chunks(msda, dtype, D, trend):
+    """Rows of L*K = 48 logits spread over up to 24 record chunks (the forward
+    sums the softmax online, rescaling at every new maximum): logits rising
+    along the row (a new maximum in every chunk), falling (none after the
+    first), and one spike 30 above the rest in the last chunk."""
+    levels = [(5, 6), (3, 4), (2, 2), (1, 3)]
+    w = workloads.custom(N=2, M=3, D=D, levels=levels, K=12, Len_q=19, dtype=dtype, refs="uniform",
+                         ref_range=(0.0, 1.0), offset_sigma=0.3, seed=1600 + D)
+    p = dict(H.prepared(w))
+    P = 4 * 12
+    base = p["attention_logits"].reshape(-1, P).astype(np.float32)
+    ramp = np.linspace(-6.0, 6.0, P, dtype=np.float32)
+    if trend == "rising":
+        lg = base * 0.1 + ramp
+    elif trend == "falling":
+        lg = base * 0.1 - ramp
+    else:
+        lg = base.copy()
+        lg[:, -1] += 30.0
+    p["attention_logits"] = lg.reshape(p["attention_logits"].shape)
+    ref = oracle.forward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
+                               p["sampling_offsets"], p["attention_logits"])
+    H.assert_fwd(_run_fused(msda, w, p), ref, dtype, f"fused forward, {trend} logits")
+
+
 # ----------------------------------------------------------------- options (per-level softmax, align_corners)
 OPT_CASES = [("per_level", 1), ("align", 2), ("both", 3)]
 
