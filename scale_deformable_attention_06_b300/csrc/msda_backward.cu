@@ -150,7 +150,8 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     }
     // fused, whole-row softmax: statistics in the record phase when the row is
     // one record chunk (compiled in where a chunk holds 16 logits), else in a
-    // pass of their own; the same summation tree as the fused forward either way
+    // pass of their own before the records, since every sample's gradient
+    // needs its normalised weight
     const bool row_softmax = FUSED && !(OPTS && dm.per_level_softmax);
     const bool seg_stats = (RC >= 16) && row_softmax && P <= RC;
     if (row_softmax && !seg_stats) {
