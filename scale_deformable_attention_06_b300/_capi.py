@@ -6,7 +6,9 @@ MSDAError when the library returns a non-OK status.  No step of the method
 runs in Python; there is no CPU fallback.  If libmsda.so has not been built,
 importing the package raises ImportError.
 """
+import contextvars
 import ctypes
+import functools
 import os
 
 import torch
@@ -89,11 +91,37 @@ def _dtype_code(t):
     raise TypeError(f"value dtype {t.dtype} is not float32 or bfloat16")
 
 
+# the device of the call being marshalled (that of its value tensor)
+_CALL_DEVICE = contextvars.ContextVar("msda_call_device", default=None)
+
+
+def _on_value_device(fn):
+    """Runs a call with its value tensor's device current (the library
+    launches on the current device); every tensor the call passes must live
+    on that device."""
+    @functools.wraps(fn)
+    def call(value, *args, **kwargs):
+        if not isinstance(value, torch.Tensor):
+            raise TypeError("value must be a torch.Tensor")
+        if not value.is_cuda:
+            raise ValueError("value must be on a CUDA device (there is no CPU path)")
+        token = _CALL_DEVICE.set(value.device)
+        try:
+            with torch.cuda.device(value.device):
+                return fn(value, *args, **kwargs)
+        finally:
+            _CALL_DEVICE.reset(token)
+    return call
+
+
 def _dev(t, name, dtype=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device (there is no CPU path)")
+    device = _CALL_DEVICE.get()
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, value on {device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -126,6 +154,7 @@ def problem(value, Len_q, n_levels, n_points, options=0):
     return msda_problem(N, S, M, D, Len_q, n_levels, n_points, _dtype_code(value), options)
 
 
+@_on_value_device
 def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
                  output=None, stream=None, options=0):
     """out[N, Len_q, M*D] from value [N,Len_in,M,D] (f32|bf16), sampling_locations
@@ -151,6 +180,7 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
     return output
 
 
+@_on_value_device
 def msda_forward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
                        attention_logits, output=None, stream=None, options=0):
     """out[N, Len_q, M*D] from reference_points [N,Len_q,L,2], sampling_offsets
@@ -182,6 +212,7 @@ def msda_backward_workspace_size(value, Len_q, n_levels, n_points, flags=0):
     return int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
 
 
+@_on_value_device
 def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, grad_output,
                   grad_value=None, grad_sampling_locations=None, grad_attention_weights=None, flags=0,
                   workspace=None, stream=None, options=0):
@@ -216,6 +247,7 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, 
     return grad_value, grad_sampling_locations, grad_attention_weights
 
 
+@_on_value_device
 def msda_backward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
                         attention_logits, grad_output, grad_value=None, grad_reference_points=None,
                         grad_sampling_offsets=None, grad_attention_logits=None, flags=0, workspace=None,
@@ -263,6 +295,7 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
     return grad_value, grad_reference_points, grad_sampling_offsets, grad_attention_logits
 
 
+@_on_value_device
 def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
                           grad_output, grad_value, grad_sampling_locations, grad_attention_weights, flags=0,
                           stream=None, options=0):
@@ -295,6 +328,7 @@ class _HostVolumes:
         self.stp = ctypes.cast(st.data_ptr(), ctypes.POINTER(ctypes.c_int64))
 
 
+@_on_value_device
 def msda3d_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, output=None,
                    stream=None, options=0):
     """3-D variant: out[N, Len_q, M*D] from value [N,Len_in,M,D], spatial_shapes [L,3] (D,H,W),
@@ -316,6 +350,7 @@ def msda3d_forward(value, spatial_shapes, level_start_index, sampling_locations,
     return output
 
 
+@_on_value_device
 def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, grad_output,
                     grad_value=None, grad_sampling_locations=None, grad_attention_weights=None, flags=0,
                     workspace=None, stream=None, options=0):

@@ -188,3 +188,14 @@ def test_index_limits_rejected_before_launch(msda):
     p = _problem(msda, Len_in=1 << 28, n_levels=1, head_dim=8, n_heads=1)
     sh3, st3 = _levels([1 << 4, 1 << 12, 1 << 12], [0])
     assert lib.msda3d_forward(ctypes.byref(p), FAKE, sh3, st3, FAKE, FAKE, FAKE, None) == 2
+
+
+@pytest.mark.parametrize("call", ["msda_forward", "msda_backward", "msda3d_forward"])
+def test_binding_refuses_host_tensors(msda, call):
+    """The binding refuses tensors that are not on a CUDA device before any
+    C call: there is no CPU path."""
+    import torch
+    v = torch.zeros((1, 4, 1, 8))
+    with pytest.raises(ValueError, match="CUDA device"):
+        getattr(msda, call)(v, [[2, 2]], [0], torch.zeros((1, 2, 1, 1, 1, 2)), torch.ones((1, 2, 1, 1, 1)),
+                            *([torch.zeros((1, 2, 8))] if call == "msda_backward" else []))
