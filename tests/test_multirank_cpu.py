@@ -61,3 +61,23 @@ def test_algorithmic_bytes_of_the_encoder_step():
     # value 45.5 MB, locations 45.5 MB, weights 22.8 MB, output 45.5 MB
     assert ab["fwd"] == pytest.approx(159.3e6, rel=2e-3)
     assert ab["bwd"] == pytest.approx(273.1e6, rel=2e-3)
+
+
+def test_touched_value_bytes():
+    """Byte accounting of sparse queries: whole 32-byte sectors of the rows
+    the in-map corners reach, each counted once."""
+    import numpy as np
+    import workloads
+    # 4 x 4 map, two heads of 16-byte bf16 rows (two rows per sector)
+    w = workloads.custom(N=1, M=2, D=8, levels=[(4, 4)], K=1, Len_q=1, dtype="bf16")
+    loc = np.array([0.5, 0.5, 0.1, 0.1], np.float32).reshape(1, 1, 2, 1, 1, 2)
+    # head 0: px = py = 1.5, pixels 5, 6, 9, 10 -> rows 10, 12, 18, 20 -> sectors 5, 6, 9, 10;
+    # head 1: px = py = -0.1, only pixel 0 inside -> row 1 -> sector 0
+    assert bench.touched_value_bytes(w, loc) == 5 * 32
+    # fp32 rows of 128 bytes: every query samples the centre of pixel (3, 2), so
+    # px = 3, py = 2 exactly; its four corners (3..4, 2..3) are all in the map
+    # (two with weight 0, loaded all the same): 4 rows per (batch, head)
+    w = workloads.custom(N=2, M=3, D=32, levels=[(5, 7)], K=2, Len_q=4)
+    loc = np.full((2, 4, 3, 1, 2, 2), 0.0, np.float32)
+    loc[..., 0], loc[..., 1] = 3.5 / 7, 2.5 / 5
+    assert bench.touched_value_bytes(w, loc) == 2 * 3 * 4 * 128
