@@ -121,6 +121,8 @@ KERNEL_SOURCES = {
     "msda_backward_kernel": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
     "msda_backward_kernel_fused": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
     "ref_grad_kernel": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
+    "msda3d_forward_kernel": ("msda3d.cu", "msda_device.cuh", "msda_launch.h"),
+    "msda3d_backward_kernel": ("msda3d.cu", "msda_device.cuh", "msda_launch.h"),
 }
 
 
@@ -519,7 +521,10 @@ def run_sweep(args):
         torch.cuda.synchronize(dev)
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
+    chosen = args.sweep_only.split(",") if args.sweep_only else None
     for name in ("tiny", "encoder", "decoder", "encoder_train", "large"):
+        if chosen is not None and name not in chosen:
+            continue
         w = workloads.WORKLOADS[name]
         raw = workloads.draw(w)
         sh, starts = torch.from_numpy(raw["spatial_shapes"]), raw["level_start_index"]
@@ -589,7 +594,8 @@ def run_sweep(args):
                           "value_bytes": vbytes, "value_bytes_touched": touched, "calls": calls,
                           "oracle_fwd_bwd_points_per_s_1core": pts / el,
                           "oracle_sample": f"{q} of {w.Lq} queries x {w.N} batches"}))
-    run_sweep_volumes(timed, peak)
+    if chosen is None or "video" in chosen:
+        run_sweep_volumes(timed, peak)
 
 
 def run_sweep_volumes(timed, peak):
@@ -623,7 +629,8 @@ def run_sweep_volumes(timed, peak):
     nval, nout = N * S * M * D, N * Lq * M * D
     ab = {"fwd": 4 * (nval + samples * 4 + nout), "bwd": 4 * (nval + samples * 4 + nout + nval + samples * 4)}
     calls = {k: {"us": ms * 1e3, "points_per_s": samples / (ms / 1e3), "gbs": ab[k] / (ms / 1e3) / 1e9,
-                 "frac_of_measured_hbm_peak": ab[k] / (ms / 1e3) / 1e9 / peak, "algorithmic_bytes": ab[k]}
+                 "frac_of_measured_hbm_peak": ab[k] / (ms / 1e3) / 1e9 / peak,
+                 "frac_of_nominal_8tbs": ab[k] / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, "algorithmic_bytes": ab[k]}
              for k, ms in t.items()}
     q = 64
     lv = raw["sampling_locations"][:, :q].astype(np.float64)
@@ -710,6 +717,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-step", action="store_true", help="time the step only (for profiler runs)")
     ap.add_argument("--sweep", action="store_true", help="per-call times on every workload (one JSON line each)")
+    ap.add_argument("--sweep-only", default="",
+                    help="comma list of sweep workloads (tiny, encoder, decoder, encoder_train, large, video)")
     ap.add_argument("--step", choices=["unfused", "fused"], default="unfused",
                     help="unfused: msda_forward + msda_backward on locations and weights; fused: msda_forward_fused + "
                          "msda_backward_fused on reference points, offsets and logits")
