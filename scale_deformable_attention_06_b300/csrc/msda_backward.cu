@@ -132,15 +132,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     float scale = 1.f;
     if constexpr (DET) scale = ldexpf(1.f, fixed_shift(*a.bound_bits, dm.rows));
 
-    float4 gall[MERGE ? HW : 1];       // merge flush: this lane's channels of every query of the warp
     if constexpr (MERGE) {
-#pragma unroll
-        for (int hh = 0; hh < HW; ++hh) {
-            gall[hh].x = __shfl_sync(0xffffffffu, g.x, hh * R + ch);
-            gall[hh].y = __shfl_sync(0xffffffffu, g.y, hh * R + ch);
-            gall[hh].z = __shfl_sync(0xffffffffu, g.z, hh * R + ch);
-            gall[hh].w = __shfl_sync(0xffffffffu, g.w, hh * R + ch);
-        }
         for (int i = lane; i < kMergeSlots; i += 32) {
             sm.key[i] = kEmptyKey;
             sm.alpha[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -328,16 +320,28 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 if (merge) {
                     // one reduction per distinct corner pixel and lane: sum_h alpha_h * g_h
                     const int U = sm.count;
+                    // this lane's channels of grad_output of each of the warp's queries,
+                    // reloaded here rather than held in registers through the sample loop
+                    float4 gq[HW];
+#pragma unroll
+                    for (int hh = 0; hh < HW; ++hh) {
+                        const int qq = qb * HW + hh;
+                        gq[hh] = qq < dm.Len_q
+                                     ? load4_value<T>(static_cast<const T *>(a.grad_out) +
+                                                          ((size_t)(n * dm.Len_q + qq) * dm.M + m) * D + ch * 4,
+                                                      pol)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                     for (int u0 = 0; u0 < U; u0 += HW) {
                         const int ui = u0 + h;
                         if (ui < U) {
                             const int slot = sm.list[ui];
                             const float4 al = sm.alpha[slot];
                             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                            acc = ffma4(al.x, gall[0], acc);
-                            acc = ffma4(al.y, gall[1], acc);
-                            acc = ffma4(al.z, gall[2], acc);
-                            acc = ffma4(al.w, gall[3], acc);
+                            acc = ffma4(al.x, gq[0], acc);
+                            acc = ffma4(al.y, gq[1], acc);
+                            acc = ffma4(al.z, gq[2], acc);
+                            acc = ffma4(al.w, gq[3], acc);
                             scatter4<DET, R>(a, vhead + sm.key[slot], ch, acc, scale);
                         }
                     }
