@@ -88,6 +88,16 @@ def algorithmic_bytes(w):
     return {"fwd": fwd, "bwd": bwd, "fused_fwd": fused, "fused_bwd": fused_bwd}
 
 
+def workload_config(args, w, world):
+    """The config keys both arms report: the workload, the step, the batch."""
+    return {"workload": "Deformable DETR encoder fwd+bwd: N=2, M=8, D=32, L=4 levels 100x167, 50x84, "
+                        "25x42, 13x21 (Len_in=22223), Len_q=Len_in, K=4, fp32"
+                        if args.workload == WORKLOAD else args.workload,
+            "step": "forward + backward (fused calls)" if args.step == "fused" else "forward + backward",
+            "per_rank_batch": w.N, "sampled_points_per_step_per_rank": w.samples,
+            "parallelism": f"dp{world} (independent batches per rank)"}
+
+
 def touched_value_bytes(w, loc):
     """Byte accounting for workloads whose queries are sparse: the bytes of
     the distinct 32-byte sectors of value that the in-map corners of all
@@ -446,14 +456,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16-storage/f32",
         "data": "synthetic (seeded PCG64 draws with the encoder workload's shapes and distributions)",
-        "config": {"workload": "Deformable DETR encoder fwd+bwd: N=2, M=8, D=32, L=4 levels 100x167, 50x84, "
-                               "25x42, 13x21 (Len_in=22223), Len_q=Len_in, K=4, fp32"
-                               if args.workload == WORKLOAD else args.workload,
-                   "step": ("msda_forward_fused + msda_backward_fused" if args.step == "fused" else
-                            "msda_forward + msda_backward") + " (atomic grad_value)", "per_rank_batch": w.N,
-                   "sampled_points_per_step_per_rank": pts,
-                   "l2": "flushed before every step (256 MB write); per-step events exclude the flush",
-                   "parallelism": f"dp{world} (independent batches per rank)"},
+        "config": dict(workload_config(args, w, world),
+                       calls=("msda_forward_fused + msda_backward_fused" if args.step == "fused" else
+                              "msda_forward + msda_backward") + " (atomic grad_value)",
+                       l2="flushed before every step (256 MB write); per-step events exclude the flush"),
         "fwd": {"ms": fwd_ms, "points_per_s": pts / (fwd_ms / 1e3), "gbs": ab["fwd"] / (fwd_ms / 1e3) / 1e9,
                 "frac_of_peak": ab["fwd"] / (fwd_ms / 1e3) / 1e9 / peak,
                 "frac_of_nominal_8tbs": ab["fwd"] / (fwd_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
@@ -700,8 +706,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "Deformable DETR encoder fwd+bwd (oracle on a query sample per step)",
-                       "step": "oracle forward + backward"},
+            "config": dict(workload_config(args, w, world),
+                           calls="oracle forward + backward (fp64, one host core) on a bounded query sample per step"),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))

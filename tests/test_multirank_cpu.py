@@ -81,3 +81,24 @@ def test_touched_value_bytes():
     loc = np.full((2, 4, 3, 1, 2, 2), 0.0, np.float32)
     loc[..., 0], loc[..., 1] = 3.5 / 7, 2.5 / 5
     assert bench.touched_value_bytes(w, loc) == 2 * 3 * 4 * 128
+
+
+def test_reference_arm_line():
+    """`bench.py --impl reference` runs the oracle on the host (no GPU) and
+    prints the contract's line: the same metric and config as our arm, the
+    oracle as its cpu_baseline, an e2e with no copies."""
+    import json
+    import subprocess
+    import sys
+    import types
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=bench.ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    args = types.SimpleNamespace(workload=bench.WORKLOAD, step="unfused")
+    expect = bench.workload_config(args, bench.workloads.WORKLOADS[bench.WORKLOAD], 1)
+    assert {k: line["config"][k] for k in expect} == expect
