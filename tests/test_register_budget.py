@@ -1,0 +1,64 @@
+"""Register budgets of the hot kernels, from ptxas's own report (-Xptxas -v),
+without a GPU.  The backward runs four resident blocks (64 registers a
+thread) and measured 7-12% slower whenever a change made it spill; the fp32
+forward is compiled for five blocks (48 registers)."""
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "scale_deformable_attention_06_b300", "csrc")
+ENTRY = re.compile(r"Compiling entry function '(\w+)' for 'sm_103a'\s*\n.*?(\d+) bytes spill stores, (\d+) bytes "
+                   r"spill loads\s*\n.*?Used (\d+) registers", re.S)
+
+
+def _nvcc():
+    for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", shutil.which("nvcc")):
+        if cand and os.path.exists(cand):
+            return cand
+    return None
+
+
+@pytest.fixture(scope="module")
+def ptxas_report(tmp_path_factory):
+    nvcc = _nvcc()
+    if nvcc is None:
+        pytest.skip("nvcc not available")
+    out = tmp_path_factory.mktemp("ptxas")
+    procs = {}
+    for src in ("msda_backward.cu", "msda_forward.cu"):
+        cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-I",
+               os.path.join(ROOT, "include"), "-I", CSRC, "--expt-relaxed-constexpr", "-Xptxas", "-v", "-c",
+               "-o", str(out / (src + ".o")), os.path.join(CSRC, src)]
+        procs[src] = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+    report = {}
+    for src, p in procs.items():
+        text = p.communicate(timeout=900)[0]
+        assert p.returncode == 0, text[-2000:]
+        for name, st, ld, regs in ENTRY.findall(text):
+            report[name] = (int(st), int(ld), int(regs))
+    return report
+
+
+def test_backward_kernels_do_not_spill(ptxas_report):
+    bwd = {k: v for k, v in ptxas_report.items() if "msda_backward_kernel" in k}
+    assert len(bwd) >= 64, "every (dtype, D, det, merge, fused, opts) instantiation is reported"
+    bad = {k: v for k, v in bwd.items() if v[0] or v[1] or v[2] > 64}
+    assert not bad, f"spills or more than 64 registers: {bad}"
+
+
+def test_fp32_forward_within_48_registers(ptxas_report):
+    fwd = {k: v for k, v in ptxas_report.items() if "msda_forward_kernelIf" in k}
+    assert len(fwd) == 16
+    bad = {k: v for k, v in fwd.items() if v[0] or v[1] or v[2] > 48}
+    assert not bad, f"spills or more than 48 registers: {bad}"
+
+
+def test_bf16_forward_spills_at_most_a_word(ptxas_report):
+    fwd = {k: v for k, v in ptxas_report.items() if "msda_forward_kernel_bf16" in k}
+    assert len(fwd) == 16
+    bad = {k: v for k, v in fwd.items() if v[0] > 4 or v[1] > 4}
+    assert not bad, f"spills above 4 bytes: {bad}"
