@@ -186,8 +186,12 @@ MSDA_API size_t msda_backward_workspace_size(const msda_problem *problem, unsign
  * Default mode sums grad_value with fp32 atomics, so its low bits vary from
  * run to run.  MSDA_DETERMINISTIC sums in 64-bit fixed point, scaled from a
  * bound on the total so that no sum can overflow, then converts to fp32: the
- * result is bitwise identical from run to run.  grad_sampling_locations and
- * grad_attention_weights are bitwise reproducible in both modes.
+ * result is bitwise identical from run to run.  The scale is chosen per batch
+ * element from that element's rows alone, so a batch element's grad_value does
+ * not depend on the other batch elements of the call: splitting a batch over
+ * several calls (or GPUs) gives bitwise the same result.
+ * grad_sampling_locations and grad_attention_weights are bitwise reproducible
+ * in both modes, and depend only on their own (query, head) row.
  */
 MSDA_API msda_status msda_backward(const msda_problem *problem, const void *value,
                           const int64_t *spatial_shapes, const int64_t *level_start_index,
@@ -239,11 +243,12 @@ MSDA_API msda_status msda_backward_fused(const msda_problem *problem, const void
  * start-up because cudaMalloc/cudaFree can synchronize the device.
  *
  * The scratch lives in the library: one 64 MiB device array (fixed-point
- * accumulators plus a 256-byte header), which every GPU that loads the
- * library holds until the process exits.  Problems with
- * N * Len_in * n_heads * head_dim above 8,388,576 elements do not fit and are
- * rejected with MSDA_ERR_UNSUPPORTED before anything is launched; use
- * msda_backward with a workspace for them.
+ * accumulators, 8 bytes per grad_value element, after a header of 4 bytes per
+ * batch element rounded up to 256), which every GPU that loads the library
+ * holds until the process exits.  A problem that needs more (for N <= 64: one
+ * with N * Len_in * n_heads * head_dim above 8,388,576 elements) is rejected
+ * with MSDA_ERR_UNSUPPORTED before anything is launched; use msda_backward
+ * with a workspace for it.
  *
  * Same arguments, results and checks as msda_backward with
  * flags = MSDA_DETERMINISTIC, except that there is no workspace and `flags`
@@ -252,7 +257,11 @@ MSDA_API msda_status msda_backward_fused(const msda_problem *problem, const void
  *
  * The first call on a device looks up the device address of the scratch
  * array (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Every call clears the part of the scratch it
+ * before any stream capture.  That address is cached per device for the life
+ * of the process and is not looked up again: cudaDeviceReset destroys the
+ * context that holds the array, so after a reset of a device this entry point
+ * must not be called on it again in the same process (msda_backward with a
+ * workspace has no such limit).  Every call clears the part of the scratch it
  * uses before summing into it.  All calls on one device share the one
  * array, so calls whose kernels overlap on the GPU (on different streams, or
  * from different threads) race on it and give wrong results: order them on

@@ -1,7 +1,6 @@
 """Build the fp64 CPU oracle (test infrastructure) into oracle/libmsda_oracle.so.
 
-Plain gcc, no fast-math, no FMA contraction: the fp32 floor decisions in
-msda_oracle.c must round once per operation, as written.
+Plain gcc -O2, no fast-math: every step of msda_oracle.c is double precision.
 """
 import os
 import subprocess
@@ -15,7 +14,7 @@ LIB = os.path.join(HERE, "libmsda_oracle.so")
 def build(force: bool = False) -> str:
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
         return LIB
-    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
            "-Wall", "-Wextra", "-o", LIB + ".tmp", SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(LIB + ".tmp", LIB)

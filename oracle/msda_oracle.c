@@ -37,12 +37,14 @@
  *     ([MSDA-tut] §3.2 code: view(..., n_levels*n_points), softmax(dim=-1)).
  *   - fused offsets are in pixels of their level: loc = ref + off / (W_l, H_l)
  *     ([DDETR-tut] §6: reference_points + sampling_offsets / scale_factors).
- *   - where floating point decides an integer (which pixel is the lower-left
- *     corner), the decision is taken in the fp32 arithmetic the CUDA kernels
- *     use, written out below in decide_floor_*; every weight, value and sum
- *     after that decision is fp64.  Near an exact integer the two precisions
- *     may pick neighbouring cells; bilinear interpolation is continuous there,
- *     so only the (one-sided) location gradient depends on the choice.
+ *   - the lower-left corner is x0 = floor(px), y0 = floor(py), taken on the
+ *     fp64 pixel coordinate like every other step; at an exact integer px the
+ *     corner x0 + 1 gets weight 0 and the location gradient is the one-sided
+ *     derivative of the cell floor() selects.  Bilinear interpolation is
+ *     continuous across cell edges, so a sample within rounding of an edge
+ *     has the same output whichever cell is taken; only its location gradient
+ *     jumps, and a comparison against this oracle has to allow either side
+ *     there.
  *
  * Options (the last argument of the forward and backward entry points; bits):
  *   1  per-level softmax: the fused calls normalise the n_points logits of each
@@ -62,49 +64,6 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
-
-/* ------------------------------------------------------------------------- */
-/* Floor decisions in fp32 (the kernels' precision).                          */
-/* Compiled with -ffp-contract=off so that each float operation rounds once.  */
-/* ------------------------------------------------------------------------- */
-
-/* Unfused path: the corner is floor(RN(RN(loc * size) - 0.5)), or with
- * align_corners floor(RN(loc * (size - 1))). */
-static int64_t decide_floor_unfused(double loc, int64_t size, int align)
-{
-    float lf = (float)loc;
-    if (align) {
-        float sf = (float)(size - 1);
-        float p = lf * sf;
-        return (int64_t)floorf(p);
-    }
-    float sf = (float)size;
-    float p = lf * sf;
-    float ph = p - 0.5f;
-    return (int64_t)floorf(ph);
-}
-
-/* Fused path: the corner is floor(RN(RN(ref * size) + RN(off - 0.5))), or with
- * align_corners floor(RN(RN(ref * (size - 1)) + RN(off * r))), r the fp32
- * quotient (size - 1) / size (the offset is in pixels of size). */
-static int64_t decide_floor_fused(double ref, double off, int64_t size, int align)
-{
-    float rf = (float)ref;
-    float of = (float)off;
-    if (align) {
-        float sm1 = (float)(size - 1);
-        float r = sm1 / (float)size;
-        float p = rf * sm1;
-        float t = of * r;
-        float s = p + t;
-        return (int64_t)floorf(s);
-    }
-    float sf = (float)size;
-    float p = rf * sf;
-    float t = of - 0.5f;
-    float s = p + t;
-    return (int64_t)floorf(s);
-}
 
 /* ------------------------------------------------------------------------- */
 /* Step a1: sampling location = reference point + offset / (W_l, H_l).        */
@@ -181,26 +140,42 @@ static void make_corners(int64_t x0, int64_t y0, double fx, double fy, int64_t H
         }
 }
 
+/* Lower corner index floor(p) of a pixel coordinate p on an axis of `size`
+ * pixels.  An index below -2 or above size + 1 is clamped there before the
+ * conversion to an integer: both neighbours of such a sample lie outside the
+ * map either way, so the clamp changes no result. */
+static int64_t lower_corner(double p, int64_t size)
+{
+    double f = floor(p);
+    if (f < -2.0) f = -2.0;
+    if (f > (double)size + 1.0) f = (double)size + 1.0;
+    return (int64_t)f;
+}
+
+/* Step a3 from the pixel coordinate (px, py): the cell and the fractions. */
+static void cell_of(double px, double py, int64_t H, int64_t W, int64_t start, corners_t *c)
+{
+    int64_t x0 = lower_corner(px, W);
+    int64_t y0 = lower_corner(py, H);
+    make_corners(x0, y0, px - (double)x0, py - (double)y0, H, W, start, c);
+}
+
 static void corners_unfused(double lx, double ly, int64_t H, int64_t W, int64_t start, int align,
                             corners_t *c)
 {
-    int64_t x0 = decide_floor_unfused(lx, W, align);
-    int64_t y0 = decide_floor_unfused(ly, H, align);
-    double px = align ? lx * (double)(W - 1) : lx * (double)W - 0.5;
+    double px = align ? lx * (double)(W - 1) : lx * (double)W - 0.5;   /* step a3 */
     double py = align ? ly * (double)(H - 1) : ly * (double)H - 0.5;
-    make_corners(x0, y0, px - (double)x0, py - (double)y0, H, W, start, c);
+    cell_of(px, py, H, W, start, c);
 }
 
 static void corners_fused(double rx, double ry, double ox, double oy, int64_t H, int64_t W,
                           int64_t start, int align, corners_t *c)
 {
-    int64_t x0 = decide_floor_fused(rx, ox, W, align);
-    int64_t y0 = decide_floor_fused(ry, oy, H, align);
     double lx = rx + ox / (double)W;    /* step a1 */
     double ly = ry + oy / (double)H;
     double px = align ? lx * (double)(W - 1) : lx * (double)W - 0.5;   /* step a3 */
     double py = align ? ly * (double)(H - 1) : ly * (double)H - 0.5;
-    make_corners(x0, y0, px - (double)x0, py - (double)y0, H, W, start, c);
+    cell_of(px, py, H, W, start, c);
 }
 
 static int check_levels(int64_t Len_in, int64_t n_levels, const int64_t *shapes, const int64_t *starts)
@@ -479,8 +454,8 @@ static void corners3(const double *loc, int64_t Dd, int64_t H, int64_t W, int64_
     int64_t i0[3];
     double p[3];
     for (int a = 0; a < 3; ++a) {
-        i0[a] = decide_floor_unfused(loc[a], size[a], align);
         p[a] = align ? loc[a] * (double)(size[a] - 1) : loc[a] * (double)size[a] - 0.5;
+        i0[a] = lower_corner(p[a], size[a]);
         c->f[a] = p[a] - (double)i0[a];
     }
     for (int k = 0; k < 2; ++k)

@@ -149,6 +149,50 @@ def _stream(stream, device):
     return ctypes.c_void_p(int(stream))
 
 
+
+
+def _check_out(t, name, shape, dtype):
+    """A caller-passed output tensor must have exactly this shape and dtype."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+def _check_backward_args(value, n_levels, sampling_locations, attention_weights, grad_output, grad_value=None,
+                         grad_sampling_locations=None, grad_attention_weights=None, coords=2):
+    """Shapes and dtypes of a backward call, checked before anything reaches
+    the library (a wrong size there would be read or written out of bounds).
+    value [N,Len_in,M,D]; sampling_locations [N,Len_q,M,L,K,coords];
+    attention_weights [N,Len_q,M,L,K]; grad_output [N,Len_q,M*D] with the
+    dtype of value; the optional outputs grad_value [N,Len_in,M,D],
+    grad_sampling_locations and grad_attention_weights (shaped like the
+    locations and weights), all float32.  Returns (Len_q, L, K)."""
+    if value.dim() != 4:
+        raise ValueError("value must be [N, Len_in, M, D]")
+    N, S, M, D = value.shape
+    if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != coords:
+        raise ValueError(f"sampling_locations must be [N, Len_q, M, L, K, {coords}]")
+    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
+    if tuple(sampling_locations.shape[:5]) != (N, Lq, M, L, K):
+        raise ValueError("sampling_locations disagrees with value (N or M)")
+    if tuple(attention_weights.shape) != (N, Lq, M, L, K):
+        raise ValueError("attention_weights must be [N, Len_q, M, L, K]")
+    if tuple(grad_output.shape) != (N, Lq, M * D):
+        raise ValueError("grad_output must be [N, Len_q, M*D]")
+    if grad_output.dtype != value.dtype:
+        raise TypeError("grad_output must have the dtype of value")
+    if L != n_levels:
+        raise ValueError("n_levels of sampling_locations and spatial_shapes disagree")
+    for t, name in ((sampling_locations, "sampling_locations"), (attention_weights, "attention_weights")):
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be torch.float32, got {t.dtype}")
+    _check_out(grad_value, "grad_value", (N, S, M, D), torch.float32)
+    _check_out(grad_sampling_locations, "grad_sampling_locations", sampling_locations.shape, torch.float32)
+    _check_out(grad_attention_weights, "grad_attention_weights", (N, Lq, M, L, K), torch.float32)
+    return Lq, L, K
+
 def problem(value, Len_q, n_levels, n_points, options=0):
     N, S, M, D = value.shape
     return msda_problem(N, S, M, D, Len_q, n_levels, n_points, _dtype_code(value), options)
@@ -196,6 +240,7 @@ def msda_forward_fused(value, spatial_shapes, level_start_index, reference_point
         raise ValueError("attention_logits must hold N*Len_q*M*L*K values")
     if L != lv.L:
         raise ValueError("n_levels of sampling_offsets and spatial_shapes disagree")
+    _check_out(output, "output", (N, Lq, M * D), value.dtype)
     if output is None:
         output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
     prob = problem(value, Lq, L, K, options)
@@ -219,11 +264,8 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, 
     """Returns (grad_value f32 [N,Len_in,M,D], grad_sampling_locations, grad_attention_weights)."""
     lv = _HostLevels(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
-    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
-    if tuple(attention_weights.shape) != (N, Lq, M, L, K) or tuple(grad_output.shape) != (N, Lq, M * D):
-        raise ValueError("attention_weights / grad_output shapes disagree with value")
-    if grad_output.dtype != value.dtype:
-        raise TypeError("grad_output must have the dtype of value")
+    Lq, L, K = _check_backward_args(value, lv.L, sampling_locations, attention_weights, grad_output, grad_value,
+                                    grad_sampling_locations, grad_attention_weights)
     dev = value.device
     if grad_value is None:
         grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)
@@ -268,6 +310,10 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
         raise TypeError("grad_output must have the dtype of value")
     if L != lv.L:
         raise ValueError("n_levels of sampling_offsets and spatial_shapes disagree")
+    _check_out(grad_value, "grad_value", (N, S, M, D), torch.float32)
+    _check_out(grad_reference_points, "grad_reference_points", reference_points.shape, torch.float32)
+    _check_out(grad_sampling_offsets, "grad_sampling_offsets", sampling_offsets.shape, torch.float32)
+    _check_out(grad_attention_logits, "grad_attention_logits", attention_logits.shape, torch.float32)
     dev = value.device
     if grad_value is None:
         grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)
@@ -304,7 +350,12 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
     For callers that may not allocate device memory; see include/msda.h for
     the size limit and for why overlapping calls race."""
     lv = _HostLevels(spatial_shapes, level_start_index)
-    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
+    for t, name in ((grad_value, "grad_value"), (grad_sampling_locations, "grad_sampling_locations"),
+                    (grad_attention_weights, "grad_attention_weights")):
+        if t is None:
+            raise ValueError(f"{name} must be passed: this call allocates nothing, its outputs included")
+    Lq, L, K = _check_backward_args(value, lv.L, sampling_locations, attention_weights, grad_output, grad_value,
+                                    grad_sampling_locations, grad_attention_weights)
     prob = problem(value, Lq, L, K, options)
     _check(_lib.msda_backward_noalloc(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
                                       _dev(sampling_locations, "sampling_locations", torch.float32),
@@ -340,6 +391,7 @@ def msda3d_forward(value, spatial_shapes, level_start_index, sampling_locations,
     Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
     if tuple(attention_weights.shape) != (N, Lq, M, L, K) or L != lv.L:
         raise ValueError("attention_weights / spatial_shapes disagree with sampling_locations")
+    _check_out(output, "output", (N, Lq, M * D), value.dtype)
     if output is None:
         output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
     prob = problem(value, Lq, L, K, options)
@@ -357,9 +409,8 @@ def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations
     """3-D variant of msda_backward.  Returns (grad_value, grad_sampling_locations [..,3], grad_attention_weights)."""
     lv = _HostVolumes(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
-    Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
-    if tuple(grad_output.shape) != (N, Lq, M * D) or grad_output.dtype != value.dtype:
-        raise ValueError("grad_output must be [N, Len_q, M*D] with the dtype of value")
+    Lq, L, K = _check_backward_args(value, lv.L, sampling_locations, attention_weights, grad_output, grad_value,
+                                    grad_sampling_locations, grad_attention_weights, coords=3)
     dev = value.device
     if grad_value is None:
         grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)

@@ -232,7 +232,7 @@ msda3d_backward_kernel(const __grid_constant__ Args3 a) {
     float4 g = load4_stream<T>(static_cast<const T *>(a.grad_out) + (size_t)row * D + ch * 4);
     if (!row_ok) g = make_float4(0.f, 0.f, 0.f, 0.f);
     float scale = 1.f;
-    if constexpr (DET) scale = ldexpf(1.f, fixed_shift(*a.bound_bits, dm.rows));
+    if constexpr (DET) scale = ldexpf(1.f, fixed_shift(a.bound_bits[n], dm.qm));   // this batch element's scale
 
     for (int r0 = 0; r0 < P; r0 += RC) {
         const int RJ = min(RC, P - r0);
@@ -398,8 +398,8 @@ cudaError_t launch_backward3d(const LaunchGeometry3 &g, int dtype, int D, const 
     a.grad_attn = grad_attn;
     unsigned long long *fixed = nullptr;
     const unsigned *bound = nullptr;
-    cudaError_t e = backward_prepare(g.g, dtype, D, attn, grad_out, grad_value, det, accumulate, workspace, &fixed,
-                                     &bound, stream);
+    cudaError_t e = backward_prepare(g.g, dtype, D, attn, 1.f, grad_out, grad_value, det, accumulate, workspace,
+                                     &fixed, &bound, stream);
     if (e != cudaSuccess) return e;
     a.fixed = fixed;
     a.bound_bits = bound;

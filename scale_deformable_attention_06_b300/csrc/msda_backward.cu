@@ -53,7 +53,7 @@ struct BwdArgs {
     const float *off;              // fused: sampling offsets (pixels of the level)
     const float *logits;           // fused: attention logits [N][Len_q][M][L*K]
     unsigned long long *fixed;     // deterministic: [N*Len_in*M*D] accumulators
-    const unsigned *bound_bits;    // deterministic: bits of max row bound (a float)
+    const unsigned *bound_bits;    // deterministic: per batch element, bits of its max row bound (a float)
     Dims d;
     LevelTable lv;
     unsigned char level_of[kMaxSamples];
@@ -130,7 +130,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     float4 g = load4_stream<T>(static_cast<const T *>(a.grad_out) + (size_t)row * D + ch * 4);
     if (!row_ok) g = make_float4(0.f, 0.f, 0.f, 0.f);
     float scale = 1.f;
-    if constexpr (DET) scale = ldexpf(1.f, fixed_shift(*a.bound_bits, dm.rows));
+    if constexpr (DET) scale = ldexpf(1.f, fixed_shift(a.bound_bits[n], dm.qm));   // this batch element's scale
 
     if constexpr (MERGE) {
         for (int i = lane; i < kMergeSlots; i += 32) {
@@ -502,50 +502,74 @@ __global__ void zero_u64_kernel(ulonglong2 *p, size_t n2) {
         p[i] = make_ulonglong2(0ull, 0ull);
 }
 
-// max over rows of (sum_s |A_s|) * (max_d |g_d|), as float bits (non-negative
+// Bound of batch element n's fixed-point sums: max over its rows of
+// (sum_s |A_s|) * (max_d |g_d|), as float bits in bound_bits[n] (non-negative
 // floats order like their bit patterns, so an integer max is exact and
-// independent of the order of the atomics).
+// independent of the order of the atomics).  Every grad_value element of batch
+// element n sums at most rows_per_batch such row totals (bilinear weights lie in
+// [0, 1] and sum to at most 1).  attn == nullptr (fused calls): the weights of
+// a row are softmax outputs summing to row_sum (1, or n_levels with the
+// per-level softmax).  Blocks (x, y): y walks the batch elements.
 template <typename T, int D>
-__global__ void row_bound_kernel(const float *attn, const T *grad_out, int rows, int P, unsigned *bound_bits) {
-    float best = 0.f;
-    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
-        float sa = 1.001f;             // softmax weights (fused call): they sum to 1
-        if (attn) {
-            sa = 0.f;
-            for (int s = 0; s < P; ++s) sa += fabsf(attn[(size_t)r * P + s]);
+__global__ void row_bound_kernel(const float *attn, const T *grad_out, int N, int rows_per_batch, int P,
+                                 float row_sum, unsigned *bound_bits) {
+    __shared__ float s_max[32];
+    for (int n = blockIdx.y; n < N; n += gridDim.y) {
+        float best = 0.f;
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < rows_per_batch; i += gridDim.x * blockDim.x) {
+            const size_t r = (size_t)n * rows_per_batch + i;
+            float sa = row_sum * 1.001f;
+            if (attn) {
+                sa = 0.f;
+                for (int s = 0; s < P; ++s) sa += fabsf(attn[r * P + s]);
+            }
+            float gm = 0.f;
+            const T *g = grad_out + r * D;
+            for (int d = 0; d < D; ++d) gm = fmaxf(gm, fabsf((float)g[d]));
+            // round the product up a little so the bound stays an upper bound
+            best = fmaxf(best, sa * gm * 1.0001f);
         }
-        float gm = 0.f;
-        const T *g = grad_out + (size_t)r * D;
-        for (int d = 0; d < D; ++d) gm = fmaxf(gm, fabsf((float)g[d]));
-        // round the product up a little so the bound stays an upper bound
-        best = fmaxf(best, sa * gm * 1.0001f);
+        best = warp_max(best);
+        if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = best;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            float v = threadIdx.x < (blockDim.x >> 5) ? s_max[threadIdx.x] : 0.f;
+            v = warp_max(v);
+            if (threadIdx.x == 0) atomicMax(bound_bits + n, __float_as_uint(v));
+        }
+        __syncthreads();
     }
-    best = warp_max(best);
-    if ((threadIdx.x & 31) == 0) atomicMax(bound_bits, __float_as_uint(best));
 }
 
-// grad_value = fixed * 2^-shift, undoing the channel permutation of each
-// block of D = 4R words (red_fixed4): thread t writes the 4 channels of lane
-// ch = t mod R of its block, words ch, R + ch, 2R + ch, 3R + ch (consecutive
-// threads read consecutive words).  The sums are below 2^62 and shift lies in
-// [-60, 100], so the scaled value is a normal float: one rounding, in the
-// int64 -> fp32 conversion; the power-of-two scaling is exact.
-__global__ void fixed_to_f32_kernel(const unsigned long long *fixed, const unsigned *bound_bits, int rows,
-                                    float4 *grad_value, size_t n4, int D, int accumulate) {
-    const int shift = fixed_shift(*bound_bits, rows);
+// grad_value = fixed * 2^-shift_n, batch element n's own scale, undoing the
+// channel permutation of each block of D = 4R words (red_fixed4): thread t
+// writes the 4 channels of lane ch = t mod R of its block, words ch, R + ch,
+// 2R + ch, 3R + ch (consecutive threads read consecutive words).  The sums are
+// below 2^62 and shift lies in [-60, 100], so the scaled value is a normal
+// float: one rounding, in the int64 -> fp32 conversion; the power-of-two
+// scaling is exact.  Blocks (x, y): y walks the batch elements.
+__global__ void fixed_to_f32_kernel(const unsigned long long *fixed, const unsigned *bound_bits, int N,
+                                    int rows_per_batch, float4 *grad_value, size_t n4_per_batch, int D,
+                                    int accumulate) {
     const size_t R = (size_t)(D >> 2);
-    for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n4; t += (size_t)gridDim.x * blockDim.x) {
-        const size_t ch = t & (R - 1);
-        const unsigned long long *w = fixed + (t - ch) * 4 + ch;
-        float4 v = make_float4(ldexpf(__ll2float_rn((long long)__ldcs(w)), -shift),
-                               ldexpf(__ll2float_rn((long long)__ldcs(w + R)), -shift),
-                               ldexpf(__ll2float_rn((long long)__ldcs(w + 2 * R)), -shift),
-                               ldexpf(__ll2float_rn((long long)__ldcs(w + 3 * R)), -shift));
-        if (accumulate) {
-            const float4 o = grad_value[t];
-            v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+    for (int n = blockIdx.y; n < N; n += gridDim.y) {
+        const int shift = fixed_shift(bound_bits[n], rows_per_batch);
+        const unsigned long long *fx = fixed + (size_t)n * n4_per_batch * 4;
+        float4 *gv = grad_value + (size_t)n * n4_per_batch;
+        for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n4_per_batch;
+             t += (size_t)gridDim.x * blockDim.x) {
+            const size_t ch = t & (R - 1);
+            const unsigned long long *w = fx + (t - ch) * 4 + ch;
+            float4 v = make_float4(ldexpf(__ll2float_rn((long long)__ldcs(w)), -shift),
+                                   ldexpf(__ll2float_rn((long long)__ldcs(w + R)), -shift),
+                                   ldexpf(__ll2float_rn((long long)__ldcs(w + 2 * R)), -shift),
+                                   ldexpf(__ll2float_rn((long long)__ldcs(w + 3 * R)), -shift));
+            if (accumulate) {
+                const float4 o = gv[t];
+                v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+            }
+            gv[t] = v;
         }
-        grad_value[t] = v;
     }
 }
 
@@ -555,11 +579,18 @@ static unsigned grid_for(size_t work, int threads) {
     return (unsigned)(b ? b : 1);
 }
 
+// Deterministic workspace: a header of one 32-bit bound per batch element,
+// padded to a multiple of 256 bytes, then the fixed-point accumulators.
+static size_t workspace_header_bytes(int N) { return ((size_t)(N > 0 ? N : 1) * 4 + 255) / 256 * 256; }
+
 size_t backward_workspace_bytes(const LaunchGeometry &g, int D, bool deterministic) {
     if (!deterministic) return 0;
     const size_t n = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
-    return 256 + n * sizeof(unsigned long long);
+    return workspace_header_bytes(g.d.N) + n * sizeof(unsigned long long);
 }
+
+// grid.y of the per-batch helper kernels
+static unsigned batch_grid(int N) { return (unsigned)(N < 1 ? 1 : (N > 65535 ? 65535 : N)); }
 
 // Levels whose samples are dense enough that neighbouring queries' corners
 // often coincide: Len_q * n_points samples on H*W pixels, at least 32 per pixel.
@@ -574,22 +605,26 @@ static unsigned merge_levels(const LaunchGeometry &g) {
 
 // grad_value preparation and completion, shared by the 2-D and 3-D
 // backward: zeroing (fp32 mode) or the fixed-point accumulators and their
-// scale bound (deterministic mode); then the conversion back to fp32.
-cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const float *attn, const void *grad_out,
-                             float *grad_value, bool det, bool accumulate, void *workspace,
+// per-batch scale bounds (deterministic mode); then the conversion back to
+// fp32.  attn == nullptr: fused call, whose rows' weights sum to row_sum.
+cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const float *attn, float row_sum,
+                             const void *grad_out, float *grad_value, bool det, bool accumulate, void *workspace,
                              unsigned long long **fixed, const unsigned **bound, cudaStream_t stream) {
     const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
     *fixed = nullptr;
     *bound = nullptr;
     if (det) {
+        const size_t hdr_bytes = workspace_header_bytes(g.d.N);
         unsigned *hdr = static_cast<unsigned *>(workspace);
-        *fixed = reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + 256);
+        *fixed = reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + hdr_bytes);
         *bound = hdr;
-        zero_u64_kernel<<<grid_for((nval * 8 + 256) / 16, 256), 256, 0, stream>>>(
-            static_cast<ulonglong2 *>(workspace), (nval * 8 + 256) / 16);
+        // header and accumulators are contiguous: zero both
+        zero_u64_kernel<<<grid_for((nval * 8 + hdr_bytes) / 16, 256), 256, 0, stream>>>(
+            static_cast<ulonglong2 *>(workspace), (nval * 8 + hdr_bytes) / 16);
         if (g.d.rows > 0) {
-#define MSDA_BOUND(T, DD) row_bound_kernel<T, DD><<<grid_for(g.d.rows, 256), 256, 0, stream>>>( \
-        attn, static_cast<const T *>(grad_out), g.d.rows, g.d.P, hdr)
+            const dim3 grid(grid_for(g.d.qm, 256) / batch_grid(g.d.N) + 1, batch_grid(g.d.N));
+#define MSDA_BOUND(T, DD) row_bound_kernel<T, DD><<<grid, 256, 0, stream>>>( \
+        attn, static_cast<const T *>(grad_out), g.d.N, g.d.qm, g.d.P, row_sum, hdr)
             if (dtype == 0) {
                 switch (D) {
                     case 8: MSDA_BOUND(float, 8); break;
@@ -615,10 +650,13 @@ cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const fl
 
 cudaError_t backward_finish(const LaunchGeometry &g, int D, float *grad_value, bool det, bool accumulate,
                             const unsigned long long *fixed, const unsigned *bound, cudaStream_t stream) {
-    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
-    if (det && nval > 0)
-        fixed_to_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(
-            fixed, bound, g.d.rows, reinterpret_cast<float4 *>(grad_value), nval / 4, D, accumulate ? 1 : 0);
+    const size_t per_batch = (size_t)g.d.Len_in * g.d.M * D / 4;
+    if (det && per_batch > 0 && g.d.N > 0) {
+        const dim3 grid(grid_for(per_batch, 256) / batch_grid(g.d.N) + 1, batch_grid(g.d.N));
+        fixed_to_f32_kernel<<<grid, 256, 0, stream>>>(fixed, bound, g.d.N, g.d.qm,
+                                                      reinterpret_cast<float4 *>(grad_value), per_batch, D,
+                                                      accumulate ? 1 : 0);
+    }
     return cudaGetLastError();
 }
 
@@ -653,7 +691,6 @@ template <typename T, int D, bool FUSED>
 static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool det, bool accumulate, void *workspace,
                                 cudaStream_t stream) {
     constexpr int HW = 32 / (D / 4);
-    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * D;
     BwdArgs a{};
     a.value = io.value;
     a.loc = io.loc;
@@ -672,21 +709,16 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
     // deterministic mode: a fixed-point reduction is four 64-bit atomics per
     // lane and corner, so merging pays on every level
     a.merge_mask = HW == 4 ? (det ? (1u << g.d.L) - 1u : merge_levels(g)) : 0u;
-    if (det) {
-        unsigned *hdr = static_cast<unsigned *>(workspace);
-        unsigned long long *fixed = reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + 256);
-        a.fixed = fixed;
-        a.bound_bits = hdr;
-        // header (256 bytes) and accumulators are contiguous: zero both
-        zero_u64_kernel<<<grid_for((nval * 8 + 256) / 16, 256), 256, 0, stream>>>(
-            static_cast<ulonglong2 *>(workspace), (nval * 8 + 256) / 16);
-        if (g.d.rows > 0)
-            row_bound_kernel<T, D><<<grid_for(g.d.rows, 256), 256, 0, stream>>>(
-                FUSED ? nullptr : io.attn, static_cast<const T *>(io.grad_out), g.d.rows, g.d.P, hdr);
-    } else if (!accumulate && nval > 0) {
-        zero_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(reinterpret_cast<float4 *>(io.grad_value),
-                                                                      nval / 4);
-    }
+    // fused: a row's weights are softmax outputs, summing to 1 (n_levels with
+    // the per-level softmax)
+    const float row_sum = g.d.per_level_softmax ? (float)g.d.L : 1.f;
+    unsigned long long *fixed = nullptr;
+    const unsigned *bound = nullptr;
+    cudaError_t e = backward_prepare(g, sizeof(T) == 4 ? 0 : 1, D, FUSED ? nullptr : io.attn, row_sum, io.grad_out,
+                                     io.grad_value, det, accumulate, workspace, &fixed, &bound, stream);
+    if (e != cudaSuccess) return e;
+    a.fixed = fixed;
+    a.bound_bits = bound;
     if (g.d.rows > 0) {
         const long long tasks = (long long)g.d.N * a.qblocks * g.d.M;
         const unsigned blocks = (unsigned)((tasks + kWarpsPerBlock - 1) / kWarpsPerBlock);
@@ -699,12 +731,10 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
             ref_grad_kernel<<<grid_for(nql, 256), 256, 0, stream>>>(io.grad_loc, io.grad_ref, nql, g.d.M, g.d.L,
                                                                    g.d.K, g.lv);
         }
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
-    if (det && nval > 0)
-        fixed_to_f32_kernel<<<grid_for(nval / 4, 256), 256, 0, stream>>>(
-            a.fixed, a.bound_bits, g.d.rows, reinterpret_cast<float4 *>(io.grad_value), nval / 4, D,
-            accumulate ? 1 : 0);
-    return cudaGetLastError();
+    return backward_finish(g, D, io.grad_value, det, accumulate, fixed, bound, stream);
 }
 
 template <bool FUSED>

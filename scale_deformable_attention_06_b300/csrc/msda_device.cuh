@@ -137,54 +137,63 @@ __device__ __forceinline__ void load_row_f32(const T *p, float (&g)[V]) {
 }
 
 // ---- pixel coordinates ------------------------------------------------------
-// Unfused: px = x * S - shift (S = W, shift = 0.5; with align_corners S = W - 1,
-// shift = 0).  The floor is taken of RN(RN(x*S) - shift); the fraction adds
-// back the exact rounding error of the product (fma), so it is accurate to
-// about 1e-7 px instead of half an ulp of px.
-__device__ __forceinline__ void pixel_coord(float x, float S, float shift, float &fl, float &frac) {
-    float p = __fmul_rn(x, S);
-    float e = __fmaf_rn(x, S, -p);             // x*S = p + e exactly
-    float ph = __fsub_rn(p, shift);
-    fl = floorf(ph);
-    frac = __fadd_rn(__fsub_rn(ph, fl), e);
-}
-
-// Fused: px = ref * S + off * Rr - shift, the same point as (ref + off / W) * S
-// - shift with Rr = S / W (1 without align_corners).  The floor is taken of
-// RN(RN(ref*S) + RN(RN(off*Rr) - shift)); the fraction carries the rounding
-// errors of every operation (fma and two-sum).
+// The pixel coordinate is carried as an unevaluated sum hi + lo of two floats
+// (lo holds the exact rounding errors of the operations that formed hi), and
+// the corner is floor() of that exact sum, as the method defines it (x0 =
+// floor(px)), not floor() of the rounded hi: a coordinate a rounding below an
+// integer stays in the lower cell with a fraction near 1.
 __device__ __forceinline__ float two_sum_err(float a, float b, float s) {
     float bb = __fsub_rn(s, a);
     return __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-// Default convention (S = size, Rr = 1, shift = 0.5): RN(RN(ref*size) + RN(off - 0.5)),
-// three roundings.
+// fl = floor(hi + lo), frac = hi + lo - fl in [0, 1] (rounded once).
+__device__ __forceinline__ void floor_frac(float hi, float lo, float &fl, float &frac) {
+    const float f0 = floorf(hi);
+    const float t = __fsub_rn(hi, f0);             // hi - floor(hi), exact for |hi| >= 1
+    // -1: the exact sum lies below f0; +1: at or above f0 + 1
+    const float c = lo < -t ? -1.f : (lo >= __fsub_rn(1.f, t) ? 1.f : 0.f);
+    fl = __fadd_rn(f0, c);
+    frac = __fadd_rn(__fsub_rn(t, c), lo);
+}
+
+// Unfused: px = x * S - shift (S = W, shift = 0.5; with align_corners S = W - 1,
+// shift = 0), with the exact errors of the product (fma) and the subtraction.
+__device__ __forceinline__ void pixel_coord(float x, float S, float shift, float &fl, float &frac) {
+    const float p = __fmul_rn(x, S);
+    const float e1 = __fmaf_rn(x, S, -p);          // x*S = p + e1 exactly
+    const float ph = __fsub_rn(p, shift);
+    const float e2 = two_sum_err(p, -shift, ph);   // p - shift = ph + e2 exactly
+    floor_frac(ph, __fadd_rn(e1, e2), fl, frac);
+}
+
+// Fused: px = ref * S + off * Rr - shift, the same point as (ref + off / W) * S
+// - shift with Rr = S / W (1 without align_corners), formed without the
+// division, with the errors of every operation (fma and two-sum).
+// Default convention (S = size, Rr = 1, shift = 0.5).
 __device__ __forceinline__ void pixel_coord_fused(float ref, float off, float size, float &fl, float &frac) {
-    float p = __fmul_rn(ref, size);
-    float e1 = __fmaf_rn(ref, size, -p);
-    float t = __fsub_rn(off, 0.5f);
-    float e2 = two_sum_err(off, -0.5f, t);
-    float s = __fadd_rn(p, t);
-    float e3 = two_sum_err(p, t, s);
-    fl = floorf(s);
-    frac = __fadd_rn(__fsub_rn(s, fl), __fadd_rn(e1, __fadd_rn(e2, e3)));
+    const float p = __fmul_rn(ref, size);
+    const float e1 = __fmaf_rn(ref, size, -p);
+    const float t = __fsub_rn(off, 0.5f);
+    const float e2 = two_sum_err(off, -0.5f, t);
+    const float s = __fadd_rn(p, t);
+    const float e3 = two_sum_err(p, t, s);
+    floor_frac(s, __fadd_rn(e1, __fadd_rn(e2, e3)), fl, frac);
 }
 
 // Any convention; for the default one it gives the same floor and fraction as
 // the function above (off * 1 and its error term 0 are exact).
 __device__ __forceinline__ void pixel_coord_fused(float ref, float off, float S, float Rr, float shift, float &fl,
                                                   float &frac) {
-    float p = __fmul_rn(ref, S);
-    float e1 = __fmaf_rn(ref, S, -p);
-    float t0 = __fmul_rn(off, Rr);
-    float ea = __fmaf_rn(off, Rr, -t0);
-    float t = __fsub_rn(t0, shift);
-    float eb = two_sum_err(t0, -shift, t);
-    float s = __fadd_rn(p, t);
-    float e3 = two_sum_err(p, t, s);
-    fl = floorf(s);
-    frac = __fadd_rn(__fsub_rn(s, fl), __fadd_rn(e1, __fadd_rn(ea, __fadd_rn(eb, e3))));
+    const float p = __fmul_rn(ref, S);
+    const float e1 = __fmaf_rn(ref, S, -p);
+    const float t0 = __fmul_rn(off, Rr);
+    const float ea = __fmaf_rn(off, Rr, -t0);
+    const float t = __fsub_rn(t0, shift);
+    const float eb = two_sum_err(t0, -shift, t);
+    const float s = __fadd_rn(p, t);
+    const float e3 = two_sum_err(p, t, s);
+    floor_frac(s, __fadd_rn(e1, __fadd_rn(ea, __fadd_rn(eb, e3))), fl, frac);
 }
 
 // Attention weight of sample k of a softmax group of n logits at lg (max
@@ -366,7 +375,8 @@ __device__ __forceinline__ void red_fixed4(unsigned long long *fixed, size_t dst
 }
 
 // Power-of-two scale of the fixed-point sums: every partial sum is at most
-// rows * max_row_bound < 2^62 after scaling.
+// rows * max_row_bound < 2^62 after scaling (rows: those that can add into one
+// accumulator, the rows of one batch element).
 __device__ __forceinline__ int fixed_shift(unsigned bits, int rows) {
     const double bound = (double)__uint_as_float(bits) * (double)rows;
     if (!(bound > 0.0)) return 0;

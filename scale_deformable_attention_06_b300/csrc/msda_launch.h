@@ -22,8 +22,9 @@ cudaError_t launch_forward(const LaunchGeometry &g, int dtype, int D, const void
 cudaError_t launch_forward_fused(const LaunchGeometry &g, int dtype, int D, const void *value, const float *ref,
                                  const float *off, const float *logits, void *out, cudaStream_t stream);
 
-// Bytes of workspace for the deterministic backward: fixed-point accumulators
-// plus a 256-byte header.
+// Bytes of workspace for the deterministic backward: a header of one 32-bit
+// scale bound per batch element (padded to 256 bytes), then the fixed-point
+// accumulators.
 size_t backward_workspace_bytes(const LaunchGeometry &g, int D, bool deterministic);
 
 cudaError_t launch_backward(const LaunchGeometry &g, int dtype, int D, const void *value, const float *loc,
@@ -38,10 +39,12 @@ cudaError_t launch_backward_fused(const LaunchGeometry &g, int dtype, int D, con
                                   float *grad_ref, float *grad_off, float *grad_logits, bool det, bool accumulate,
                                   void *workspace, cudaStream_t stream);
 
-// grad_value preparation (zeroing, or deterministic accumulators and bound)
-// and completion (fixed point to fp32), shared by the 2-D and 3-D backward.
-cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const float *attn, const void *grad_out,
-                             float *grad_value, bool det, bool accumulate, void *workspace,
+// grad_value preparation (zeroing, or deterministic accumulators and one scale
+// bound per batch element) and completion (fixed point to fp32), shared by the
+// 2-D and 3-D backward.  attn == nullptr: the weights are softmax outputs whose
+// rows sum to row_sum.
+cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const float *attn, float row_sum,
+                             const void *grad_out, float *grad_value, bool det, bool accumulate, void *workspace,
                              unsigned long long **fixed, const unsigned **bound, cudaStream_t stream);
 cudaError_t backward_finish(const LaunchGeometry &g, int D, float *grad_value, bool det, bool accumulate,
                             const unsigned long long *fixed, const unsigned *bound, cudaStream_t stream);

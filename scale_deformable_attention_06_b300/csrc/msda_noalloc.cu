@@ -65,9 +65,10 @@ extern "C" msda_status msda_backward_noalloc(const msda_problem *problem, const 
     if (need > kNoallocScratchBytes) {
         char msg[400];
         snprintf(msg, sizeof(msg),
-                 "msda_backward_noalloc: this problem needs %zu bytes of scratch, above the built-in %zu "
-                 "(N * Len_in * n_heads * head_dim must stay at or below %zu); use msda_backward with a workspace",
-                 need, kNoallocScratchBytes, (kNoallocScratchBytes - 256) / 8);
+                 "msda_backward_noalloc: this problem needs %zu bytes of scratch (8 per grad_value element plus "
+                 "4 per batch element, rounded up to 256), above the built-in %zu; use msda_backward with a "
+                 "workspace",
+                 need, kNoallocScratchBytes);
         return msda::noalloc_fail(MSDA_ERR_UNSUPPORTED, msg);
     }
     st = msda::noalloc_check_pointers(problem, g, value, sampling_locations, attention_weights, grad_output, grad_value,

@@ -4,6 +4,17 @@ seeded raw draws, the oracle's answers, and the tolerance checks.
 The oracle turns the raw draws into the inputs of the unfused calls
 (locations from reference points and offsets, weights from logits); those
 fp32 inputs then go to both sides unchanged.
+
+Cell edges.  The oracle takes x0 = floor(px) on the fp64 pixel coordinate,
+the kernels on a two-float representation of it; where px lies within
+rounding of an integer the two may take neighbouring cells.  The output,
+grad_attention_weights and grad_value are continuous across the edge, but the
+location gradient is one-sided there and jumps: either side's derivative is
+right.  The *_reference helpers flag every coordinate within EDGE_REL of an
+integer, evaluate the oracle with those coordinates moved NUDGE_PX to either
+side, keep per coordinate the side whose location gradient the GPU result
+is closer to, and return the oracle's answer on that choice (all outputs of
+one consistent oracle call).  Every other coordinate keeps its exact value.
 """
 import numpy as np
 import torch
@@ -16,6 +27,119 @@ FWD_F32_ABS = 1e-5
 FWD_F32_REL = 1e-5
 BWD_F32_REL = 1e-4
 BF16_REL = 2e-2
+
+
+# a coordinate is "at a cell edge" when |px - round(px)| <= EDGE_REL * (sum of
+# the magnitudes of the terms that form px + 1): a few fp32 roundings of the
+# error terms the kernels carry, far below one fp32 ulp of px
+EDGE_REL = 2.0 ** -26
+NUDGE_PX = 1e-6
+
+
+def _axis_scales(spatial_shapes, options):
+    """Per level and coordinate (x, y[, z]): the pixel scale S (size, or
+    size - 1 with align_corners), the size, and the half-pixel shift."""
+    sizes = np.asarray(spatial_shapes, dtype=np.float64)[:, ::-1]      # (W, H) or (W, H, D)
+    align = bool(options & oracle.ALIGN_CORNERS)
+    return (sizes - 1.0 if align else sizes), sizes, (0.0 if align else 0.5)
+
+
+def edges_unfused(loc, spatial_shapes, options=0):
+    """(mask, below, above) for sampling_locations [..., L, K, c]: mask marks the
+    coordinates at a cell edge; below / above are float64 copies of loc with
+    those coordinates moved NUDGE_PX pixels under / over the edge."""
+    S, _, shift = _axis_scales(spatial_shapes, options)
+    Sb = S[:, None, :]
+    x = np.asarray(loc, dtype=np.float64)
+    px = x * Sb - shift
+    B = np.rint(px)
+    mask = (np.abs(px - B) <= EDGE_REL * (np.abs(x * Sb) + 1.0)) & (Sb > 0)
+    Sd = np.where(Sb > 0, Sb, 1.0)
+    return mask, np.where(mask, (B - NUDGE_PX + shift) / Sd, x), np.where(mask, (B + NUDGE_PX + shift) / Sd, x)
+
+
+def edges_fused(reference_points, sampling_offsets, spatial_shapes, options=0):
+    """The same for the fused calls, on the offsets: px = ref * S + off * S / size
+    - shift.  With align_corners the kernels scale the offset by S / size
+    rounded to fp32, which widens the window by a relative 2^-23 of |off|."""
+    S, sizes, shift = _axis_scales(spatial_shapes, options)
+    Sb, Rb = S[:, None, :], (S / sizes)[:, None, :]
+    r = np.asarray(reference_points, dtype=np.float64)[:, :, None, :, None, :]
+    o = np.asarray(sampling_offsets, dtype=np.float64)
+    px = r * Sb + o * Rb - shift
+    B = np.rint(px)
+    win = EDGE_REL * (np.abs(r * Sb) + np.abs(o * Rb) + 1.0)
+    if options & oracle.ALIGN_CORNERS:
+        win = win + 2.0 ** -23 * np.abs(o)
+    mask = (np.abs(px - B) <= win) & (Sb > 0)
+    Rd = np.where(Rb > 0, Rb, 1.0)
+    return mask, np.where(mask, o + (B - NUDGE_PX - px) / Rd, o), np.where(mask, o + (B + NUDGE_PX - px) / Rd, o)
+
+
+class BackwardReference:
+    """Oracle reference for the outputs of one backward problem.  `call(x)`
+    runs the oracle with the location-like input x (locations, or offsets for
+    the fused call); output `which` of it is the location gradient that picks
+    the side at each cell edge.  Oracle runs are cached, so several GPU results
+    (atomic and deterministic mode, repeated calls) cost one run each side."""
+
+    def __init__(self, call, x, edges, which):
+        self.call, self.x, self.which = call, np.asarray(x, dtype=np.float64), which
+        self.mask, self.below, self.above = edges
+        self.edge_count = int(self.mask.sum())
+        self._sides = None
+        self._cache = {}
+
+    def for_gpu(self, gpu):
+        """The oracle's outputs for the GPU's outputs `gpu` (a sequence ordered
+        like the oracle's)."""
+        if not self.edge_count:
+            key, x = b"", self.x
+        else:
+            if self._sides is None:
+                self._sides = (self.call(self.below), self.call(self.above))
+            lo, hi = self._sides
+            g = np.asarray(gpu[self.which], dtype=np.float64).reshape(lo[self.which].shape)
+            take_lo = self.mask & (np.abs(g - lo[self.which]) <= np.abs(g - hi[self.which]))
+            key = take_lo[self.mask].tobytes()
+            x = np.where(take_lo, self.below, np.where(self.mask, self.above, self.x))
+        if key not in self._cache:
+            self._cache[key] = self.call(x)
+        return self._cache[key]
+
+
+def backward_reference(p, options=0):
+    """msda_backward: (grad_value, grad_sampling_locations, grad_attention_weights)."""
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+
+    def call(loc):
+        return oracle.backward(p["value"], sh, st, loc, p["attention_weights"], p["grad_output"], options=options)
+
+    return BackwardReference(call, p["sampling_locations"], edges_unfused(p["sampling_locations"], sh, options), 1)
+
+
+def backward3d_reference(p, options=0):
+    """msda3d_backward (spatial_shapes [L,3], locations (x, y, z))."""
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+
+    def call(loc):
+        return oracle.backward3d(p["value"], sh, st, loc, p["attention_weights"], p["grad_output"], options=options)
+
+    return BackwardReference(call, p["sampling_locations"], edges_unfused(p["sampling_locations"], sh, options), 1)
+
+
+def backward_fused_reference(p, options=0):
+    """msda_backward_fused: (grad_value, grad_reference_points,
+    grad_sampling_offsets, grad_attention_logits); edges are resolved on the
+    offsets, so the reference-point gradient sums the chosen sides."""
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+
+    def call(off):
+        return oracle.backward_fused(p["value"], sh, st, p["reference_points"], off, p["attention_logits"],
+                                     p["grad_output"], options=options)
+
+    edges = edges_fused(p["reference_points"], p["sampling_offsets"], sh, options)
+    return BackwardReference(call, p["sampling_offsets"], edges, 2)
 
 
 def bf16_round(a):
@@ -35,13 +159,14 @@ def unfused_inputs(w, raw):
     return loc, attn
 
 
-def prepared(w, raw=None):
+def prepared(w, raw=None, round_bf16=True):
     """All host inputs of workload `w` as float32 (value and grad_output already
-    rounded to bf16 when the workload stores bf16)."""
+    rounded to bf16 when the workload stores bf16, unless round_bf16 is False:
+    the unrounded draws measure the storage error itself)."""
     raw = workloads.draw(w) if raw is None else raw
     loc, attn = unfused_inputs(w, raw)
     value, g = raw["value"], raw["grad_output"]
-    if w.dtype == "bf16":
+    if w.dtype == "bf16" and round_bf16:
         value, g = bf16_round(value), bf16_round(g)
     out = dict(raw)
     out.update(value=value, grad_output=g, sampling_locations=loc, attention_weights=attn)

@@ -199,3 +199,53 @@ def test_binding_refuses_host_tensors(msda, call):
     with pytest.raises(ValueError, match="CUDA device"):
         getattr(msda, call)(v, [[2, 2]], [0], torch.zeros((1, 2, 1, 1, 1, 2)), torch.ones((1, 2, 1, 1, 1)),
                             *([torch.zeros((1, 2, 8))] if call == "msda_backward" else []))
+
+
+def test_backward_argument_checks_in_the_binding(msda):
+    """The binding refuses mismatched backward tensors (and caller-passed
+    outputs of the wrong size or dtype) before it calls the library: a wrong
+    size there would be read or written out of bounds on the device.  Only
+    shapes and dtypes are looked at, so CPU tensors stand in here."""
+    import torch
+    from scale_deformable_attention_06_b300 import _capi
+    N, S, M, D, Lq, L, K = 2, 80, 2, 8, 5, 2, 2
+    bf16 = torch.bfloat16
+    ok = dict(value=torch.zeros(N, S, M, D), sampling_locations=torch.zeros(N, Lq, M, L, K, 2),
+              attention_weights=torch.zeros(N, Lq, M, L, K), grad_output=torch.zeros(N, Lq, M * D),
+              grad_value=torch.zeros(N, S, M, D), grad_sampling_locations=torch.zeros(N, Lq, M, L, K, 2),
+              grad_attention_weights=torch.zeros(N, Lq, M, L, K))
+
+    def call(**over):
+        a = dict(ok)
+        a.update(over)
+        return _capi._check_backward_args(a["value"], L, a["sampling_locations"], a["attention_weights"],
+                                          a["grad_output"], a["grad_value"], a["grad_sampling_locations"],
+                                          a["grad_attention_weights"])
+
+    assert call() == (Lq, L, K)
+    bad = [
+        (ValueError, dict(attention_weights=torch.zeros(N, Lq, M, L, K + 1))),
+        (ValueError, dict(attention_weights=torch.zeros(N, Lq + 1, M, L, K))),
+        (ValueError, dict(grad_output=torch.zeros(N, Lq, M * D - 1))),
+        (TypeError, dict(grad_output=torch.zeros(N, Lq, M * D, dtype=bf16))),
+        (ValueError, dict(sampling_locations=torch.zeros(N, Lq, M + 1, L, K, 2))),
+        (ValueError, dict(sampling_locations=torch.zeros(N, Lq, M, L, K, 3))),
+        (TypeError, dict(sampling_locations=torch.zeros(N, Lq, M, L, K, 2, dtype=torch.float64))),
+        (ValueError, dict(sampling_locations=torch.zeros(N, Lq, M, L + 1, K, 2),
+                          attention_weights=torch.zeros(N, Lq, M, L + 1, K),
+                          grad_sampling_locations=torch.zeros(N, Lq, M, L + 1, K, 2),
+                          grad_attention_weights=torch.zeros(N, Lq, M, L + 1, K))),      # L vs spatial_shapes
+        (ValueError, dict(grad_value=torch.zeros(N, S - 1, M, D))),
+        (TypeError, dict(grad_value=torch.zeros(N, S, M, D, dtype=bf16))),
+        (ValueError, dict(grad_sampling_locations=torch.zeros(N, Lq, M, L, K, 1))),
+        (TypeError, dict(grad_sampling_locations=torch.zeros(N, Lq, M, L, K, 2, dtype=bf16))),
+        (ValueError, dict(grad_attention_weights=torch.zeros(N, Lq, M, L, K - 1))),
+    ]
+    for exc, over in bad:
+        with pytest.raises(exc):
+            call(**over)
+    # a bf16 problem: grad_output must be bf16 too, the gradients stay float32
+    assert call(value=torch.zeros(N, S, M, D, dtype=bf16), grad_output=torch.zeros(N, Lq, M * D, dtype=bf16)) \
+        == (Lq, L, K)
+    with pytest.raises(TypeError):
+        call(value=torch.zeros(N, S, M, D, dtype=bf16))

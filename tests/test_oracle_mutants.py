@@ -59,7 +59,7 @@ def _build_mutant(tmp, find, repl):
     so_path = os.path.join(tmp, "mutant.so")
     with open(c_path, "w") as f:
         f.write(mutated)
-    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off", "-w",
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-w",
                     "-o", so_path, c_path, "-lm"], check=True)
     return so_path
 

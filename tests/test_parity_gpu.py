@@ -56,14 +56,14 @@ def _run_backward_fused(msda, w, p, flags=0):
     return tuple(o.cpu().numpy() for o in outs)
 
 
-def _oracle_backward_fused(p):
-    return oracle.backward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
-                                 p["sampling_offsets"], p["attention_logits"], p["grad_output"])
+def _oracle_backward_fused(p, options=0):
+    """Edge-aware oracle reference of the fused backward (see harness)."""
+    return H.backward_fused_reference(p, options)
 
 
 def _check_backward_fused(w, got, ref):
     names = ("grad_value", "grad_reference_points", "grad_sampling_offsets", "grad_attention_logits")
-    for name, g, r in zip(names, got, ref):
+    for name, g, r in zip(names, got, ref.for_gpu(got)):
         H.assert_bwd(g.reshape(r.shape), r, "f32", f"{w.name} fused {name}")
 
 
@@ -72,14 +72,15 @@ def _oracle_forward(p):
                           p["attention_weights"])
 
 
-def _oracle_backward(p):
-    return oracle.backward(p["value"], p["spatial_shapes"], p["level_start_index"], p["sampling_locations"],
-                           p["attention_weights"], p["grad_output"])
+def _oracle_backward(p, options=0):
+    """Edge-aware oracle reference of the backward (see harness)."""
+    return H.backward_reference(p, options)
 
 
 def _check_backward(w, got, ref):
     dtype = "f32"   # gradients are fp32 outputs of identical (rounded) inputs
-    for name, g, r in zip(("grad_value", "grad_sampling_locations", "grad_attention_weights"), got, ref):
+    for name, g, r in zip(("grad_value", "grad_sampling_locations", "grad_attention_weights"), got,
+                          ref.for_gpu(got)):
         H.assert_bwd(g, r, dtype, f"{w.name} {name}")
 
 
@@ -112,9 +113,21 @@ def test_decoder_fused_bf16(msda):
     p = H.prepared(w)
     ref = oracle.forward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
                                p["sampling_offsets"], p["attention_logits"])
-    H.assert_fwd(_run_fused(msda, w, p), ref, w.dtype, "decoder fused output")
+    fused = _run_fused(msda, w, p)
+    H.assert_fwd(fused, ref, w.dtype, "decoder fused output")
     # the unfused call on the locations the oracle forms agrees as well
     H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), w.dtype, "decoder output")
+    # the storage error itself: against the oracle on the unrounded fp32 draws
+    u = H.prepared(w, round_bf16=False)
+    ref_u = oracle.forward_fused(u["value"], u["spatial_shapes"], u["level_start_index"], u["reference_points"],
+                                 u["sampling_offsets"], u["attention_logits"])
+    _, rel = H.errors(fused, ref_u)
+    assert rel <= H.BF16_REL, f"decoder fused output against unrounded fp32 inputs: rel {rel:.3e}"
+    fb = _run_backward_fused(msda, w, p)
+    for name, g, r in zip(("grad_value", "grad_reference_points", "grad_sampling_offsets", "grad_attention_logits"),
+                          fb, _oracle_backward_fused(u).for_gpu(fb)):
+        _, rel = H.errors(g.reshape(r.shape), r)
+        assert rel <= H.BF16_REL, f"decoder fused {name} against unrounded fp32 inputs: rel {rel:.3e}"
 
 
 def test_encoder_train_backward(msda):
@@ -133,8 +146,18 @@ def test_encoder_train_backward(msda):
 def test_large_bf16_forward_backward(msda):
     w = workloads.WORKLOADS["large"]
     p = H.prepared(w)
-    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), w.dtype, "large output")
-    _check_backward(w, _run_backward(msda, w, p), _oracle_backward(p))
+    out = _run_forward(msda, w, p)
+    H.assert_fwd(out, _oracle_forward(p), w.dtype, "large output")
+    got = _run_backward(msda, w, p)
+    _check_backward(w, got, _oracle_backward(p))
+    # the storage error itself: against the oracle on the unrounded fp32 value and grad_output
+    u = H.prepared(w, round_bf16=False)
+    _, rel = H.errors(out, _oracle_forward(u))
+    assert rel <= H.BF16_REL, f"large output against unrounded fp32 inputs: rel {rel:.3e}"
+    for name, g, r in zip(("grad_value", "grad_sampling_locations", "grad_attention_weights"), got,
+                          _oracle_backward(u).for_gpu(got)):
+        _, rel = H.errors(g, r)
+        assert rel <= H.BF16_REL, f"large {name} against unrounded fp32 inputs: rel {rel:.3e}"
 
 
 # ----------------------------------------------------------------- shapes and edges
@@ -238,7 +261,9 @@ def test_accumulate_grad_value(msda):
     w = workloads.WORKLOADS["tiny"]
     p = H.prepared(w)
     gv0 = np.random.Generator(np.random.PCG64(4)).standard_normal(p["value"].shape).astype(np.float32)
-    ref_gv, _, _ = _oracle_backward(p)
+    # grad_value is continuous in the locations: the plain oracle call is its reference
+    ref_gv = oracle.backward(p["value"], p["spatial_shapes"], p["level_start_index"], p["sampling_locations"],
+                             p["attention_weights"], p["grad_output"])[0]
     for flags in (msda.MSDA_ACCUMULATE_GRAD_VALUE, msda.MSDA_ACCUMULATE_GRAD_VALUE | msda.MSDA_DETERMINISTIC):
         gv = H.dev(gv0)
         msda.msda_backward(H.dev(p["value"]), p["spatial_shapes"], p["level_start_index"], H.dev(p["sampling_locations"]),
@@ -297,14 +322,16 @@ def test_fused_backward_dense_merge_and_accumulate(msda):
                          ref_range=(0.0, 1.0), offset_sigma=0.15, seed=808)
     p = H.prepared(w)
     ref = _oracle_backward_fused(p)
-    _check_backward_fused(w, _run_backward_fused(msda, w, p), ref)
+    got = _run_backward_fused(msda, w, p)
+    _check_backward_fused(w, got, ref)
+    ref_gv = ref.for_gpu(got)[0]
     gv0 = np.random.Generator(np.random.PCG64(9)).standard_normal(p["value"].shape).astype(np.float32)
     for flags in (msda.MSDA_ACCUMULATE_GRAD_VALUE, msda.MSDA_ACCUMULATE_GRAD_VALUE | msda.MSDA_DETERMINISTIC):
         gv = H.dev(gv0)
         msda.msda_backward_fused(H.dev(p["value"]), p["spatial_shapes"], p["level_start_index"],
                                  H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]),
                                  H.dev(p["attention_logits"]), H.dev(p["grad_output"]), grad_value=gv, flags=flags)
-        H.assert_bwd(gv.cpu().numpy(), gv0 + ref[0], "f32", "fused accumulated grad_value")
+        H.assert_bwd(gv.cpu().numpy(), gv0 + ref_gv, "f32", "fused accumulated grad_value")
 
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 8), ("f32", 16), ("bf16", 32), ("f32", 64)])
@@ -357,8 +384,7 @@ def test_options_all_calls(msda, dtype, D, oname, opt):
     out = msda.msda_forward(v, sh, st, loc, attn, options=opt).float().cpu().numpy()
     H.assert_fwd(out, oracle.forward(p["value"], sh, st, p["sampling_locations"], p["attention_weights"],
                                      options=opt), dtype, f"{oname} forward")
-    ref_b = oracle.backward(p["value"], sh, st, p["sampling_locations"], p["attention_weights"], p["grad_output"],
-                            options=opt)
+    ref_b = _oracle_backward(p, opt)
     for flags in (0, msda.MSDA_DETERMINISTIC):
         got = msda.msda_backward(v, sh, st, loc, attn, g, flags=flags, options=opt)
         _check_backward(w, [t.cpu().numpy() for t in got], ref_b)
@@ -366,8 +392,7 @@ def test_options_all_calls(msda, dtype, D, oname, opt):
     fo = msda.msda_forward_fused(v, sh, st, ref, off, lg, options=opt).float().cpu().numpy()
     H.assert_fwd(fo, oracle.forward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
                                           p["attention_logits"], options=opt), dtype, f"{oname} fused forward")
-    ref_fb = oracle.backward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
-                                   p["attention_logits"], p["grad_output"], options=opt)
+    ref_fb = _oracle_backward_fused(p, opt)
     for flags in (0, msda.MSDA_DETERMINISTIC):
         got = msda.msda_backward_fused(v, sh, st, ref, off, lg, g, flags=flags, options=opt)
         _check_backward_fused(w, [t.cpu().numpy() for t in got], ref_fb)
@@ -382,9 +407,7 @@ def test_options_dense_merge_path(msda):
     got = msda.msda_backward_fused(H.dev(p["value"]), sh, st, H.dev(p["reference_points"]),
                                    H.dev(p["sampling_offsets"]), H.dev(p["attention_logits"]),
                                    H.dev(p["grad_output"]), options=3)
-    ref = oracle.backward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
-                                p["attention_logits"], p["grad_output"], options=3)
-    _check_backward_fused(w, [t.cpu().numpy() for t in got], ref)
+    _check_backward_fused(w, [t.cpu().numpy() for t in got], _oracle_backward_fused(p, 3))
 
 
 # ----------------------------------------------------------------- 3-D variant (trilinear)
@@ -408,7 +431,8 @@ def test_3d_forward_backward(msda, dtype, D, opt):
     v, gd, locd, ad = H.dev(value, dt), H.dev(g, dt), H.dev(loc), H.dev(attn)
     out = msda.msda3d_forward(v, sh, st, locd, ad, options=opt).float().cpu().numpy()
     H.assert_fwd(out, oracle.forward3d(value, sh, st, loc, attn, options=opt), dtype, f"3-D {dtype} D={D} output")
-    ref = oracle.backward3d(value, sh, st, loc, attn, g, options=opt)
+    ref = H.backward3d_reference(dict(value=value, spatial_shapes=sh, level_start_index=st, sampling_locations=loc,
+                                      attention_weights=attn, grad_output=g), opt)
     w = workloads.custom(name="volumes", N=2, M=3, D=D, levels=[(1, 1)], K=3, dtype=dtype)
     _check_backward(w, [t.cpu().numpy() for t in msda.msda3d_backward(v, sh, st, locd, ad, gd, options=opt)], ref)
     det = [[t.cpu().numpy() for t in msda.msda3d_backward(v, sh, st, locd, ad, gd, flags=msda.MSDA_DETERMINISTIC,
@@ -482,13 +506,15 @@ def test_element_offsets_near_2_31(msda, dtype):
     # unfused
     out = msda.msda_forward(value, sh, st, H.dev(loc), H.dev(attn)).float().cpu().numpy()
     H.assert_fwd(out, oracle.forward(value_s, sh_s, st_s, loc_s, attn_s), dtype, "forward near 2^31")
-    gv_r, gl_r, ga_r = oracle.backward(value_s, sh_s, st_s, loc_s, attn_s, g)
+    ref_s = H.backward_reference(dict(value=value_s, spatial_shapes=sh_s, level_start_index=st_s,
+                                      sampling_locations=loc_s, attention_weights=attn_s, grad_output=g))
     for flags in (0, msda.MSDA_DETERMINISTIC):
         gv, gl, ga = msda.msda_backward(value, sh, st, H.dev(loc), H.dev(attn), gd, flags=flags)
         gv_small, gv_rest = small_level(gv)
         assert gv_rest == 0.0, f"grad_value on the outside level: {gv_rest}"
         gl, ga = gl.cpu().numpy(), ga.cpu().numpy()
         assert not gl[:, :, :, 0].any() and not ga[:, :, :, 0].any()
+        gv_r, gl_r, ga_r = ref_s.for_gpu((gv_small, gl[:, :, :, 1:], ga[:, :, :, 1:]))
         H.assert_bwd(gv_small, gv_r, "f32", f"grad_value near 2^31 (flags {flags})")
         H.assert_bwd(gl[:, :, :, 1:], gl_r, "f32", f"grad_loc near 2^31 (flags {flags})")
         H.assert_bwd(ga[:, :, :, 1:], ga_r, "f32", f"grad_attn near 2^31 (flags {flags})")
@@ -497,7 +523,9 @@ def test_element_offsets_near_2_31(msda, dtype):
     fo = msda.msda_forward_fused(value, sh, st, H.dev(ref), H.dev(off), H.dev(logit.reshape(1, Lq, M, 2 * K)))
     H.assert_fwd(fo.float().cpu().numpy(), oracle.forward_fused(value_s, sh_s, st_s, ref_s, off_s, logit_s), dtype,
                  "fused forward near 2^31")
-    fr = oracle.backward_fused(value_s, sh_s, st_s, ref_s, off_s, logit_s, g)
+    fref = H.backward_fused_reference(dict(value=value_s, spatial_shapes=sh_s, level_start_index=st_s,
+                                           reference_points=ref_s, sampling_offsets=off_s, attention_logits=logit_s,
+                                           grad_output=g))
     for flags in (0, msda.MSDA_DETERMINISTIC):
         gv, gref, goff, glog = msda.msda_backward_fused(value, sh, st, H.dev(ref), H.dev(off),
                                                         H.dev(logit.reshape(1, Lq, M, 2 * K)), gd, flags=flags)
@@ -506,8 +534,81 @@ def test_element_offsets_near_2_31(msda, dtype):
         gref, goff = gref.cpu().numpy(), goff.cpu().numpy()
         glog = glog.cpu().numpy().reshape(1, Lq, M, 2, K)
         assert not gref[:, :, 0].any() and not goff[:, :, :, 0].any() and not glog[:, :, :, 0].any()
+        fr = fref.for_gpu((gv_small, gref[:, :, 1:], goff[:, :, :, 1:], glog[:, :, :, 1]))
         H.assert_bwd(gv_small, fr[0], "f32", f"fused grad_value near 2^31 (flags {flags})")
         H.assert_bwd(gref[:, :, 1:], fr[1], "f32", f"fused grad_ref near 2^31 (flags {flags})")
         H.assert_bwd(goff[:, :, :, 1:], fr[2], "f32", f"fused grad_off near 2^31 (flags {flags})")
         H.assert_bwd(glog[:, :, :, 1], fr[3].reshape(1, Lq, M, K), "f32", f"fused grad_logit near 2^31 (flags {flags})")
         del gv
+
+
+# ----------------------------------------------------------------- the data-parallel split
+def _slice(p, keys, sl):
+    return {k: (np.ascontiguousarray(v[sl]) if k in keys else v) for k, v in p.items()}
+
+
+BATCHED = ("value", "sampling_locations", "attention_weights", "grad_output", "reference_points",
+           "sampling_offsets", "attention_logits")
+
+
+def _bitwise(a, b, what):
+    a, b = np.ascontiguousarray(a, np.float32), np.ascontiguousarray(b, np.float32)
+    assert a.shape == b.shape and np.array_equal(a.view(np.uint32), b.view(np.uint32)), f"{what} differs"
+
+
+def test_batch_split_matches_one_call(msda):
+    """Ranks that take whole batch elements (the split bench.py makes under
+    torchrun) compute exactly what one call on the whole batch computes: the
+    encoder training problem as one N=2 call and as two N=1 calls gives
+    bitwise the same forward, fused forward and per-sample gradients, and, in
+    deterministic mode, the same grad_value (each batch element's fixed-point
+    scale comes from its own rows alone)."""
+    w = workloads.WORKLOADS["encoder_train"]
+    p = H.prepared(w)
+    halves = [_slice(p, BATCHED, slice(n, n + 1)) for n in range(w.N)]
+    whole = {"fwd": _run_forward(msda, w, p), "fused": _run_fused(msda, w, p),
+             "bwd": _run_backward(msda, w, p, msda.MSDA_DETERMINISTIC),
+             "bwd_atomic": _run_backward(msda, w, p),
+             "fbwd": _run_backward_fused(msda, w, p, msda.MSDA_DETERMINISTIC)}
+    parts = [{"fwd": _run_forward(msda, w, h), "fused": _run_fused(msda, w, h),
+              "bwd": _run_backward(msda, w, h, msda.MSDA_DETERMINISTIC),
+              "bwd_atomic": _run_backward(msda, w, h),
+              "fbwd": _run_backward_fused(msda, w, h, msda.MSDA_DETERMINISTIC)} for h in halves]
+    for n, part in enumerate(parts):
+        _bitwise(part["fwd"], whole["fwd"][n:n + 1], f"forward of batch element {n}")
+        _bitwise(part["fused"], whole["fused"][n:n + 1], f"fused forward of batch element {n}")
+        for name, a, b in zip(("grad_value", "grad_sampling_locations", "grad_attention_weights"), part["bwd"],
+                              whole["bwd"]):
+            _bitwise(a, b[n:n + 1], f"deterministic {name} of batch element {n}")
+        # atomic mode: the per-sample gradients use no atomics
+        for name, a, b in zip(("grad_sampling_locations", "grad_attention_weights"), part["bwd_atomic"][1:],
+                              whole["bwd_atomic"][1:]):
+            _bitwise(a, b[n:n + 1], f"{name} of batch element {n}")
+        for name, a, b in zip(("grad_value", "grad_reference_points", "grad_sampling_offsets",
+                               "grad_attention_logits"), part["fbwd"], whole["fbwd"]):
+            _bitwise(a, b[n:n + 1], f"deterministic fused {name} of batch element {n}")
+
+
+def test_query_split_of_one_batch_element(msda):
+    """The queries of one image split over two calls (ranks that would share
+    its value map): the outputs and per-sample gradients of the two halves
+    are bitwise those of one call, and the two grad_value halves, summed on the
+    host (the all-reduce such a split needs), match the oracle.  The split
+    point is not a multiple of the queries a warp owns."""
+    w = workloads.WORKLOADS["encoder_train"]
+    p = _slice(H.prepared(w), BATCHED, slice(0, 1))
+    cut = 11111
+    q_keys = ("sampling_locations", "attention_weights", "grad_output", "reference_points", "sampling_offsets",
+              "attention_logits")
+    halves = [_slice(p, q_keys, (slice(None), slice(0, cut))), _slice(p, q_keys, (slice(None), slice(cut, None)))]
+    whole_fwd = _run_forward(msda, w, p)
+    whole_bwd = _run_backward(msda, w, p, msda.MSDA_DETERMINISTIC)
+    gv_sum = np.zeros(p["value"].shape, np.float64)
+    for i, (h, sl) in enumerate(zip(halves, (slice(0, cut), slice(cut, None)))):
+        _bitwise(_run_forward(msda, w, h), whole_fwd[:, sl], f"forward of query half {i}")
+        gv, gl, ga = _run_backward(msda, w, h, msda.MSDA_DETERMINISTIC)
+        _bitwise(gl, whole_bwd[1][:, sl], f"grad_sampling_locations of query half {i}")
+        _bitwise(ga, whole_bwd[2][:, sl], f"grad_attention_weights of query half {i}")
+        gv_sum += gv
+    ref = _oracle_backward(p).for_gpu((gv_sum, whole_bwd[1], whole_bwd[2]))
+    H.assert_bwd(gv_sum, ref[0], "f32", "grad_value summed over the query halves")
