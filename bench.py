@@ -342,6 +342,25 @@ def run_ours(args):
     achieved = ab[dom] / (ms / 1e3) / 1e9
     traffic = profiled_traffic(name)
 
+    # ---- the SM line-rate ceilings (probes over a value-sized buffer): the
+    # forward's floor is its corner gathers at the gather rate, the backward's
+    # those plus its grad_value reductions at the reduction rate
+    line = None
+    if w.D == 32 and w.dtype == "f32":
+        gathers = w.samples * 4
+        rates = line_rates(dev, w.N * w.Len_in * w.M * w.D * 4, gathers, reps=5)
+        reds = backward_reduction_lines(w, loc_h.numpy())
+        g_rate, r_rate = rates["gather"]["lines_per_s"], rates["reduce"]["lines_per_s"]
+        ceil_us = {"fwd": gathers / g_rate * 1e6, "bwd": gathers / g_rate * 1e6 + reds / r_rate * 1e6}
+        line = {"gather_lines_per_s": g_rate, "reduce_lines_per_s": r_rate,
+                "gathers_per_launch": gathers, "backward_reductions_per_launch": reds,
+                "fwd_ceiling_us": ceil_us["fwd"], "bwd_ceiling_us": ceil_us["bwd"],
+                "frac_fwd": ceil_us["fwd"] / (fwd_ms * 1e3), "frac_bwd": ceil_us["bwd"] / (bwd_ms * 1e3),
+                "probes": rates,
+                "note": "ceiling = the launch's 128-byte line gathers at the probed gather rate (+ its grad_value "
+                        "reductions at the probed reduction rate, taken one after the other); frac = ceiling / "
+                        "the launch's CUDA-event time"}
+
     # ---- end to end from pinned host memory through the same calls
     if args.step == "fused":
         d_in = (value, ref_d, off_d, logit_d, gout)
@@ -478,7 +497,9 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "algorithmic_bytes_per_launch": ab[dom], "launch_ms": ms},
+                     "algorithmic_bytes_per_launch": ab[dom], "launch_ms": ms,
+                     "frac_of_line_ceiling": line[f"frac_{dom}"] if line else None},
+        "line_ceiling": line,
         "e2e": {"value": aggregate(pts, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
                 "pipeline": "double-buffered: upload of step i+1 and download of step i-1 on their own streams "
@@ -497,6 +518,120 @@ def run_ours(args):
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- line-rate ceilings
+PROBES = os.path.join(ROOT, "scale_deformable_attention_06_b300", "libmsda_probes.so")
+
+
+def _probes():
+    import ctypes
+    lib = ctypes.CDLL(PROBES)
+    i64, vp, u32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint32
+    lib.msda_probe_sink_bytes.restype = ctypes.c_size_t
+    lib.msda_probe_gather.argtypes = [vp, i64, i64, i64, vp, u32, vp]
+    lib.msda_probe_reduce.argtypes = [vp, i64, i64, i64, u32, vp]
+    lib.msda_probe_mixed.argtypes = [vp, i64, i64, ctypes.c_int, vp, u32, vp]
+    lib.msda_probe_accesses.argtypes = [i64]
+    lib.msda_probe_accesses.restype = i64
+    return lib
+
+
+def line_rates(dev, buf_bytes, lines, reps=10):
+    """Random 128-byte line operations per second on this GPU, measured with
+    the probes of libmsda_probes.so over a buffer of buf_bytes (the value
+    tensor's size: L2-resident for the encoder), `lines` operations per
+    launch, CUDA events, median of `reps` launches:
+      gather            four lines per warp instruction (LDG.128), uniform
+      gather_hot        the same over the first 128 KB (L1-resident)
+      reduce            red.global.add.v4.f32 into uniform lines
+      reduce_hot        the same over 128 KB (contended)
+      mixed_r           eight gathers and r reductions per quarter-warp round
+    """
+    import ctypes
+    import torch
+    lib = _probes()
+    n_lines = buf_bytes // 128
+    buf = torch.zeros(n_lines * 32, dtype=torch.float32, device=dev)
+    sink = torch.empty(lib.msda_probe_sink_bytes() // 4, dtype=torch.float32, device=dev)
+    sp = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    bp, kp = ctypes.c_void_p(buf.data_ptr()), ctypes.c_void_p(sink.data_ptr())
+
+    def timed_ms(fn):
+        for _ in range(2):
+            if fn() != 0:
+                raise RuntimeError("probe launch failed")
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i, (e0, e1) in enumerate(evs):
+            e0.record()
+            fn(i)
+            e1.record()
+        torch.cuda.synchronize(dev)
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+    hot = (128 << 10) // 128
+    done = int(lib.msda_probe_accesses(lines))          # whole rounds: at least `lines`
+    out = {"buffer_bytes": n_lines * 128, "lines_per_launch": done, "reps": reps}
+    ms = {
+        "gather": timed_ms(lambda i=0: lib.msda_probe_gather(bp, n_lines, 0, lines, kp, 17 + i, sp)),
+        "gather_hot": timed_ms(lambda i=0: lib.msda_probe_gather(bp, n_lines, hot, lines, kp, 17 + i, sp)),
+        "reduce": timed_ms(lambda i=0: lib.msda_probe_reduce(bp, n_lines, 0, lines, 17 + i, sp)),
+        "reduce_hot": timed_ms(lambda i=0: lib.msda_probe_reduce(bp, n_lines, hot, lines, 17 + i, sp)),
+    }
+    for r in (2, 4, 6, 8):
+        ms[f"mixed_{r}"] = timed_ms(lambda i=0, r=r: lib.msda_probe_mixed(bp, n_lines, lines, r, kp, 17 + i, sp))
+    for k, v in ms.items():
+        if k.startswith("mixed"):
+            r = int(k.split("_")[1])
+            out[k] = {"us": v * 1e3, "gathers": done, "reductions": done * r // 8}
+        else:
+            out[k] = {"us": v * 1e3, "lines_per_s": done / (v / 1e3)}
+    return out
+
+
+def backward_reduction_lines(w, loc):
+    """red.global.add.v4 line operations of msda_backward on workload w (head_dim
+    32, fp32: one line per corner row), as its kernel issues them: one per
+    in-map corner, except on levels with at least 32 samples per pixel
+    (Len_q * K >= 32 * H * W), where the warp's four consecutive queries of one
+    head first merge coinciding corners (one reduction per distinct pixel of
+    the group and level).  loc: sampling locations [N, Len_q, M, L, K, 2]."""
+    sh = w.spatial_shapes()
+    N, Lq, M, L, K, _ = loc.shape
+    total = 0
+    for l in range(L):
+        H, W = int(sh[l][0]), int(sh[l][1])
+        x0 = np.floor(loc[:, :, :, l, :, 0].astype(np.float64) * W - 0.5).astype(np.int64)
+        y0 = np.floor(loc[:, :, :, l, :, 1].astype(np.float64) * H - 0.5).astype(np.int64)
+        keys = []
+        for dy in (0, 1):
+            for dx in (0, 1):
+                xc, yc = x0 + dx, y0 + dy
+                keys.append(np.where((xc >= 0) & (xc < W) & (yc >= 0) & (yc < H), yc * W + xc, -1))
+        keys = np.stack(keys, -1)                                           # [N, Lq, M, K, 4]
+        if Lq * K < 32 * H * W:
+            total += int((keys >= 0).sum())
+            continue
+        G = 4
+        pad = (-Lq) % G
+        kk = np.concatenate([keys, np.full((N, pad) + keys.shape[2:], -1, np.int64)], axis=1)
+        kk = kk.reshape(N, -1, G, M, K * 4).transpose(0, 1, 3, 2, 4).reshape(N, -1, M, G * K * 4)
+        kk = np.sort(kk, axis=-1)
+        total += int(((kk[..., 1:] != kk[..., :-1]) & (kk[..., 1:] >= 0)).sum() + (kk[..., 0] >= 0).sum())
+    return total
+
+
+def run_line_rates(args):
+    """One JSON line: the probes' rates over the encoder's value-sized buffer,
+    and the encoder calls' line ceilings that follow from them."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[WORKLOAD]
+    lines = w.samples * 4
+    rates = line_rates(dev, w.N * w.Len_in * w.M * w.D * 4, lines)
+    print(json.dumps({"line_rates": True, "workload_buffer": "encoder value tensor (N=2, Len_in=22223, M=8, D=32, "
+                      "fp32)", **rates}))
 
 
 # ----------------------------------------------------------------------------- every workload
@@ -723,6 +858,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-step", action="store_true", help="time the step only (for profiler runs)")
     ap.add_argument("--sweep", action="store_true", help="per-call times on every workload (one JSON line each)")
+    ap.add_argument("--line-rates", action="store_true",
+                    help="random 128-byte line gather / reduction rates of this GPU (libmsda_probes.so)")
     ap.add_argument("--sweep-only", default="",
                     help="comma list of sweep workloads (tiny, encoder, decoder, encoder_train, large, video)")
     ap.add_argument("--step", choices=["unfused", "fused"], default="unfused",
@@ -731,7 +868,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.sweep:
+    if args.line_rates:
+        run_line_rates(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -1,4 +1,5 @@
-"""Build libmsda.so (the CUDA kernels and the C ABI) in-tree, for sm_103a.
+"""Build libmsda.so (the CUDA kernels and the C ABI) in-tree, for sm_103a, and
+libmsda_probes.so beside it (line-rate measurement kernels, used by bench.py).
 
     python scale_deformable_attention_06_b300/build.py [--force] [--verbose]
 
@@ -15,6 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmsda.so")
+PROBES_LIB = os.path.join(PKG, "libmsda_probes.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,17 +40,32 @@ def _stale():
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force=False, verbose=False, extra=()):
-    if not force and not _stale():
-        return LIB
+def _compile(out, srcs, verbose=False, extra=()):
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-fvisibility=hidden",
            "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64", "-I", INCLUDE,
-           "--expt-relaxed-constexpr", *extra, "-o", LIB + ".tmp", *sources()]
+           "--expt-relaxed-constexpr", *extra, "-o", out + ".tmp", *srcs]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)
-    os.replace(LIB + ".tmp", LIB)
+    os.replace(out + ".tmp", out)
+
+
+def build_probes(force=False):
+    """libmsda_probes.so: the line-rate measurement kernels (include/msda_probes.h)."""
+    srcs = sorted(glob.glob(os.path.join(CSRC, "probes", "*.cu")))
+    deps = srcs + [os.path.join(INCLUDE, "msda_probes.h"), os.path.abspath(__file__)]
+    if force or not os.path.exists(PROBES_LIB) or any(os.path.getmtime(p) > os.path.getmtime(PROBES_LIB)
+                                                      for p in deps):
+        _compile(PROBES_LIB, srcs, extra=("-Xcompiler", "-fvisibility=default"))
+    return PROBES_LIB
+
+
+def build(force=False, verbose=False, extra=()):
+    build_probes(force)
+    if not force and not _stale():
+        return LIB
+    _compile(LIB, sources(), verbose, extra)
     return LIB
 
 

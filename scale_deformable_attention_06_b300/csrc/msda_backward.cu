@@ -11,7 +11,8 @@
 //
 // Work decomposition.  A warp owns HW consecutive queries of one (n, head m)
 // ("head-major"), every lane 4 channels of one of them (R = D / 4 lanes per
-// query, HW = 32 / R).  Per chunk of up to RC samples:
+// query, HW = 32 / R); the warps of a block own consecutive query groups of
+// the same head.  Per chunk of up to RC samples:
 //   phase 1: one 32-byte corner record per (query, sample) into warp-private
 //            shared memory: the four corners' element offsets (clamped inside
 //            the map, see pack_record), fx, fy, A and the inside-mask; reads
@@ -100,9 +101,12 @@ struct BwdWarpSmem<HW, RC, true> {
 };
 
 // OPTS: the problem sets option bits (fused calls); without them the kernel
-// carries none of the option code.
+// carries none of the option code.  Resident blocks per SM: four in
+// deterministic mode; three in fp32 mode, which leaves the L1 cache more of
+// the SM's memory beside the blocks' shared memory (measured faster there,
+// slower in deterministic mode).
 template <typename T, int D, bool DET, bool MERGE, bool FUSED, bool OPTS>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, DET ? 4 : 3)
 msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int R = D / 4, HW = 32 / R;
     constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
@@ -114,10 +118,12 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WS &sm = smem[warp];
     const Dims &dm = a.d;
+    // query blocks fastest: the warps of a block (and blocks launched together)
+    // take consecutive queries of one head, whose samples share value rows
     const int task = blockIdx.x * kWarpsPerBlock + warp;
     if (task >= dm.N * a.qblocks * dm.M) return;       // warp-uniform
-    const int m = task % dm.M, t2 = task / dm.M;
-    const int qb = t2 % a.qblocks, n = t2 / a.qblocks;
+    const int qb = task % a.qblocks, t2 = task / a.qblocks;
+    const int m = t2 % dm.M, n = t2 / dm.M;
     const int P = dm.P;
     const int h = lane / R, ch = lane % R;
     const int q = qb * HW + h;

@@ -249,3 +249,20 @@ def test_backward_argument_checks_in_the_binding(msda):
         == (Lq, L, K)
     with pytest.raises(TypeError):
         call(value=torch.zeros(N, S, M, D, dtype=bf16))
+
+
+def test_probe_library_exports_its_header(msda):
+    """libmsda_probes.so (the line-rate measurements bench.py makes) exports
+    exactly what include/msda_probes.h declares, and nothing of the method."""
+    lib = os.path.join(os.path.dirname(msda.LIBRARY), "libmsda_probes.so")
+    text = open(os.path.join(ROOT, "include", "msda_probes.h")).read()
+    declared = set(re.findall(r"\b(msda_probe_\w+)\s*\(", text))
+    out = subprocess.run(["nm", "-D", "--defined-only", lib], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(msda_\w+)", out))
+    assert declared and exported == declared
+    probes = ctypes.CDLL(lib)
+    probes.msda_probe_accesses.argtypes = [ctypes.c_int64]
+    probes.msda_probe_accesses.restype = ctypes.c_int64
+    n = probes.msda_probe_accesses(22756352)
+    assert 22756352 <= n < 22756352 * 1.02
+    assert probes.msda_probe_accesses(0) == 0

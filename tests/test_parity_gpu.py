@@ -506,15 +506,15 @@ def test_element_offsets_near_2_31(msda, dtype):
     # unfused
     out = msda.msda_forward(value, sh, st, H.dev(loc), H.dev(attn)).float().cpu().numpy()
     H.assert_fwd(out, oracle.forward(value_s, sh_s, st_s, loc_s, attn_s), dtype, "forward near 2^31")
-    ref_s = H.backward_reference(dict(value=value_s, spatial_shapes=sh_s, level_start_index=st_s,
-                                      sampling_locations=loc_s, attention_weights=attn_s, grad_output=g))
+    bref = H.backward_reference(dict(value=value_s, spatial_shapes=sh_s, level_start_index=st_s,
+                                     sampling_locations=loc_s, attention_weights=attn_s, grad_output=g))
     for flags in (0, msda.MSDA_DETERMINISTIC):
         gv, gl, ga = msda.msda_backward(value, sh, st, H.dev(loc), H.dev(attn), gd, flags=flags)
         gv_small, gv_rest = small_level(gv)
         assert gv_rest == 0.0, f"grad_value on the outside level: {gv_rest}"
         gl, ga = gl.cpu().numpy(), ga.cpu().numpy()
         assert not gl[:, :, :, 0].any() and not ga[:, :, :, 0].any()
-        gv_r, gl_r, ga_r = ref_s.for_gpu((gv_small, gl[:, :, :, 1:], ga[:, :, :, 1:]))
+        gv_r, gl_r, ga_r = bref.for_gpu((gv_small, gl[:, :, :, 1:], ga[:, :, :, 1:]))
         H.assert_bwd(gv_small, gv_r, "f32", f"grad_value near 2^31 (flags {flags})")
         H.assert_bwd(gl[:, :, :, 1:], gl_r, "f32", f"grad_loc near 2^31 (flags {flags})")
         H.assert_bwd(ga[:, :, :, 1:], ga_r, "f32", f"grad_attn near 2^31 (flags {flags})")

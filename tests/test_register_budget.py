@@ -1,7 +1,8 @@
 """Register budgets of the hot kernels, from ptxas's own report (-Xptxas -v),
-without a GPU.  The backward runs four resident blocks (64 registers a
-thread) and measured 7-12% slower whenever a change made it spill; the fp32
-forward is compiled for five blocks (48 registers)."""
+without a GPU.  The backward runs four resident blocks in deterministic mode
+(64 registers a thread) and three in fp32 mode (85), and measured 7-12%
+slower whenever a change made it spill; the fp32 forward is compiled for five
+blocks (48 registers)."""
 import os
 import re
 import shutil
@@ -43,11 +44,20 @@ def ptxas_report(tmp_path_factory):
     return report
 
 
+def _det(name):
+    """DET template argument of a backward instantiation (the third, after T and D)."""
+    m = re.search(r"msda_backward_kernelI(?:f|13__nv_bfloat16)Li\d+ELb([01])E", name)
+    assert m, name
+    return m.group(1) == "1"
+
+
 def test_backward_kernels_do_not_spill(ptxas_report):
+    """Deterministic mode runs four resident blocks (64 registers a thread),
+    fp32 mode three (85)."""
     bwd = {k: v for k, v in ptxas_report.items() if "msda_backward_kernel" in k}
     assert len(bwd) >= 64, "every (dtype, D, det, merge, fused, opts) instantiation is reported"
-    bad = {k: v for k, v in bwd.items() if v[0] or v[1] or v[2] > 64}
-    assert not bad, f"spills or more than 64 registers: {bad}"
+    bad = {k: v for k, v in bwd.items() if v[0] or v[1] or v[2] > (64 if _det(k) else 85)}
+    assert not bad, f"spills or more registers than the block budget allows: {bad}"
 
 
 def test_fp32_forward_within_48_registers(ptxas_report):
