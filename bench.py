@@ -69,14 +69,15 @@ def aggregate(points_per_rank, world, seconds_max):
     return points_per_rank * world / seconds_max if seconds_max > 0 else 0.0
 
 
-def algorithmic_bytes(w):
+def algorithmic_bytes(w, groups=None):
     """Compulsory HBM bytes of each call on workload w: every tensor the call
     reads or writes, counted once (value re-reads and the grad_value memset
-    are not counted)."""
+    are not counted).  groups: sets of locations and weights, if the heads
+    share them in groups."""
     vb = 2 if w.dtype == "bf16" else 4
     n_val = w.N * w.Len_in * w.M * w.D
     n_out = w.N * w.Lq * w.M * w.D
-    n_smp = w.N * w.Lq * w.M * w.L * w.K
+    n_smp = w.N * w.Lq * (groups or w.M) * w.L * w.K
     fwd = n_val * vb + n_smp * 2 * 4 + n_smp * 4 + n_out * vb
     bwd = n_val * vb + n_smp * 2 * 4 + n_smp * 4 + n_out * vb + n_val * 4 + n_smp * 2 * 4 + n_smp * 4
     n_ref = w.N * w.Lq * w.L * 2
@@ -663,11 +664,17 @@ def run_sweep(args):
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
     chosen = args.sweep_only.split(",") if args.sweep_only else None
-    for name in ("tiny", "encoder", "decoder", "encoder_train", "large"):
+    for name in ("tiny", "encoder", "decoder", "encoder_train", "large", "encoder_g1"):
         if chosen is not None and name not in chosen:
             continue
-        w = workloads.WORKLOADS[name]
+        # encoder_g1: the encoder workload with one set of locations and weights
+        # shared by all 8 heads (head groups, G = 1: 256 channels a set)
+        groups = 1 if name == "encoder_g1" else None
+        w = workloads.WORKLOADS["encoder" if groups else name]
         raw = workloads.draw(w)
+        if groups:
+            for k in ("sampling_offsets", "attention_logits"):
+                raw[k] = np.ascontiguousarray(raw[k][:, :, :groups])
         sh, starts = torch.from_numpy(raw["spatial_shapes"]), raw["level_start_index"]
         vdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         if "sampling_locations" in raw:
@@ -708,7 +715,7 @@ def run_sweep(args):
                                                                 grad_attention_logits=glg, flags=acc), reps,
                                pre=lambda: gv.zero_()),
         }
-        ab = algorithmic_bytes(w)
+        ab = algorithmic_bytes(w, groups)
         ab["bwd_deterministic"] = ab["bwd"]
         # sparse queries: value traffic counted as the sectors the samples touch
         vbytes = w.N * w.Len_in * w.M * w.D * (2 if w.dtype == "bf16" else 4)
@@ -731,10 +738,19 @@ def run_sweep(args):
         _oracle_step(smp)
         el = time.perf_counter() - t0
         pts = w.N * q * w.M * w.L * w.K
-        print(json.dumps({"sweep": True, "workload": name, "dtype": w.dtype, "samples": w.samples,
-                          "value_bytes": vbytes, "value_bytes_touched": touched, "calls": calls,
-                          "oracle_fwd_bwd_points_per_s_1core": pts / el,
-                          "oracle_sample": f"{q} of {w.Lq} queries x {w.N} batches"}))
+        line = {"sweep": True, "workload": name, "dtype": w.dtype, "samples": w.samples,
+                "head_groups": groups or w.M, "value_bytes": vbytes, "value_bytes_touched": touched, "calls": calls,
+                "oracle_fwd_bwd_points_per_s_1core": pts / el,
+                "oracle_sample": f"{q} of {w.Lq} queries x {w.N} batches"}
+        if w.dtype == "bf16":
+            # the storage error itself: the forward against the oracle on the
+            # unrounded fp32 draws, on the same query sample (normwise rel)
+            import oracle
+            got = msda.msda_forward(value, sh, starts, loc, attn, output=out)[:, :q].float().cpu().numpy()
+            ref_u = oracle.forward(raw["value"], raw["spatial_shapes"], raw["level_start_index"],
+                                   loc_h.numpy()[:, :q], attn_h.numpy()[:, :q])
+            line["bf16_storage_rel_error_vs_unrounded_fp32"] = float(np.abs(got - ref_u).max() / np.abs(ref_u).max())
+        print(json.dumps(line))
     if chosen is None or "video" in chosen:
         run_sweep_volumes(timed, peak)
 
@@ -861,7 +877,8 @@ def main(argv=None):
     ap.add_argument("--line-rates", action="store_true",
                     help="random 128-byte line gather / reduction rates of this GPU (libmsda_probes.so)")
     ap.add_argument("--sweep-only", default="",
-                    help="comma list of sweep workloads (tiny, encoder, decoder, encoder_train, large, video)")
+                    help="comma list of sweep workloads (tiny, encoder, decoder, encoder_train, large, encoder_g1, "
+                         "video)")
     ap.add_argument("--step", choices=["unfused", "fused"], default="unfused",
                     help="unfused: msda_forward + msda_backward on locations and weights; fused: msda_forward_fused + "
                          "msda_backward_fused on reference points, offsets and logits")

@@ -53,9 +53,20 @@
  *   grad_sampling_locations [N][Len_q][M][L][K][2]    f32
  *   grad_attention_weights  [N][Len_q][M][L][K]       f32
  *
- * Supported: head_dim in {8, 16, 32, 64}; 1 <= n_levels <= 16;
- * 1 <= n_levels * n_points <= 256; N*Len_q*M < 2^31; (Len_in + 2*max W_l + 4)
- * * M * D < 2^31.  value/output/grad_output/grad_value must be 16-byte
+ * Head groups (msda_problem.n_groups = G, 0 for G = M): the M heads form G
+ * groups of M / G consecutive heads that share one set of locations and
+ * weights (the DAT pages' sampler: one offset field per group of channels,
+ * "un.csdn.net/yx18yrw9d9z8" §2.1-2.2).  Every per-sample tensor then has G in
+ * place of M: sampling_locations [N][Len_q][G][L][K][2], attention_weights
+ * [N][Len_q][G][L][K], sampling_offsets [N][Len_q][G][L][K][2],
+ * attention_logits [N][Len_q][G][L*K] and their gradients; head m samples with
+ * the set of group m / (M / G).  value, output and grad_value keep their
+ * layouts.
+ *
+ * Supported: (M / G) * head_dim (the channels one set samples; head_dim when
+ * G = M) a power of two from 8 to 256 (to 64 for the 3-D calls);
+ * 1 <= n_levels <= 16; 1 <= n_levels * n_points <= 256; N*Len_q*G < 2^31;
+ * (Len_in + 2*max W_l + 4) * M * D < 2^31.  value/output/grad_output/grad_value must be 16-byte
  * aligned, sampling_locations/reference_points/sampling_offsets 8-byte
  * aligned, the other f32 tensors 4-byte aligned.
  */
@@ -100,6 +111,8 @@ typedef struct msda_problem {
     int32_t n_points;   /* K, samples per level per head */
     int32_t dtype;      /* msda_dtype */
     uint32_t options;   /* MSDA_OPT_* bits, 0 for the default method */
+    int32_t n_groups;   /* G: groups of heads sharing one set of locations and
+                           weights; 0 (or n_heads) for one set per head */
 } msda_problem;
 
 /* msda_problem.options: readings of the method the pages leave open.

@@ -34,9 +34,15 @@ def bind(path):
     lib.msda_oracle_backward_fused.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, dp, dp, i64]
     lib.msda_oracle_forward3d.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, i64]
     lib.msda_oracle_backward3d.argtypes = [i64] * 7 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, i64]
+    lib.msda_oracle_forward_grouped.argtypes = [i64] * 8 + [dp, lp, lp, dp, dp, dp, i64]
+    lib.msda_oracle_forward_fused_grouped.argtypes = [i64] * 8 + [dp, lp, lp, dp, dp, dp, dp, i64]
+    lib.msda_oracle_backward_grouped.argtypes = [i64] * 8 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, i64]
+    lib.msda_oracle_backward_fused_grouped.argtypes = [i64] * 8 + [dp, lp, lp, dp, dp, dp, dp, dp, dp, dp, dp, i64]
     for f in ("msda_oracle_locations", "msda_oracle_softmax", "msda_oracle_forward",
               "msda_oracle_forward_fused", "msda_oracle_backward", "msda_oracle_backward_fused",
-              "msda_oracle_forward3d", "msda_oracle_backward3d"):
+              "msda_oracle_forward3d", "msda_oracle_backward3d", "msda_oracle_forward_grouped",
+              "msda_oracle_forward_fused_grouped", "msda_oracle_backward_grouped",
+              "msda_oracle_backward_fused_grouped"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -71,11 +77,13 @@ def _check(rc, name):
 
 
 def _dims(value, shapes, loc_like):
-    """(N, Len_in, M, D, Len_q, L, K) from value [N,S,M,D] and a [N,Lq,M,L,K,...] tensor."""
+    """(N, Len_in, M, D, Len_q, L, K, G) from value [N,S,M,D] and a per-sample tensor
+    [N,Lq,G,L,K,...]: G = M (one set of locations per head), or the number of
+    head groups that share one set each."""
     N, S, M, D = value.shape
     L = shapes.shape[0]
-    Lq, K = loc_like.shape[1], loc_like.shape[4]
-    return N, S, M, D, Lq, L, K
+    Lq, G, K = loc_like.shape[1], loc_like.shape[2], loc_like.shape[4]
+    return N, S, M, D, Lq, L, K, G
 
 
 # option bits of the forward and backward functions (msda_oracle.c header)
@@ -108,16 +116,19 @@ def softmax(logits):
 
 
 def forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, options=0):
-    """a3-a5.  Returns output [N, Len_q, M*D] in float64."""
+    """a3-a5.  Returns output [N, Len_q, M*D] in float64.  sampling_locations is
+    [N, Len_q, G, L, K, 2] with G = M, or G groups of M / G heads sharing a set
+    (attention_weights likewise); so are the per-sample arguments below."""
     lib = _load()
     v, vp = _d(value)
     sh, shp = _l(spatial_shapes)
     st, stp = _l(level_start_index)
     loc, locp = _d(sampling_locations)
     a, ap = _d(attention_weights)
-    N, S, M, D, Lq, L, K = _dims(v, sh, loc)
+    N, S, M, D, Lq, L, K, G = _dims(v, sh, loc)
     out = np.zeros((N, Lq, M * D))
-    _check(lib.msda_oracle_forward(N, S, M, D, Lq, L, K, vp, shp, stp, locp, ap, _d(out)[1], options), "forward")
+    _check(lib.msda_oracle_forward_grouped(N, S, M, G, D, Lq, L, K, vp, shp, stp, locp, ap, _d(out)[1], options),
+           "forward")
     return out
 
 
@@ -131,10 +142,10 @@ def forward_fused(value, spatial_shapes, level_start_index, reference_points, sa
     ref, refp = _d(reference_points)
     off, offp = _d(sampling_offsets)
     lg, lgp = _d(attention_logits)
-    N, S, M, D, Lq, L, K = _dims(v, sh, off)
+    N, S, M, D, Lq, L, K, G = _dims(v, sh, off)
     out = np.zeros((N, Lq, M * D))
-    _check(lib.msda_oracle_forward_fused(N, S, M, D, Lq, L, K, vp, shp, stp, refp, offp, lgp, _d(out)[1],
-                                         options), "forward_fused")
+    _check(lib.msda_oracle_forward_fused_grouped(N, S, M, G, D, Lq, L, K, vp, shp, stp, refp, offp, lgp,
+                                                 _d(out)[1], options), "forward_fused")
     return out
 
 
@@ -148,12 +159,12 @@ def backward(value, spatial_shapes, level_start_index, sampling_locations, atten
     loc, locp = _d(sampling_locations)
     a, ap = _d(attention_weights)
     g, gp = _d(grad_output)
-    N, S, M, D, Lq, L, K = _dims(v, sh, loc)
+    N, S, M, D, Lq, L, K, G = _dims(v, sh, loc)
     gv = np.zeros(v.shape)
     gl = np.zeros(loc.shape)
     ga = np.zeros(a.shape)
-    _check(lib.msda_oracle_backward(N, S, M, D, Lq, L, K, vp, shp, stp, locp, ap, gp,
-                                    _d(gv)[1], _d(gl)[1], _d(ga)[1], options), "backward")
+    _check(lib.msda_oracle_backward_grouped(N, S, M, G, D, Lq, L, K, vp, shp, stp, locp, ap, gp,
+                                            _d(gv)[1], _d(gl)[1], _d(ga)[1], options), "backward")
     return gv, gl, ga
 
 
@@ -168,13 +179,13 @@ def backward_fused(value, spatial_shapes, level_start_index, reference_points, s
     off, offp = _d(sampling_offsets)
     lg, lgp = _d(attention_logits)
     g, gp = _d(grad_output)
-    N, S, M, D, Lq, L, K = _dims(v, sh, off)
+    N, S, M, D, Lq, L, K, G = _dims(v, sh, off)
     gv = np.zeros(v.shape)
     gr = np.zeros(ref.shape)
     go = np.zeros(off.shape)
     gl = np.zeros(lg.shape)
-    _check(lib.msda_oracle_backward_fused(N, S, M, D, Lq, L, K, vp, shp, stp, refp, offp, lgp, gp,
-                                          _d(gv)[1], _d(gr)[1], _d(go)[1], _d(gl)[1], options),
+    _check(lib.msda_oracle_backward_fused_grouped(N, S, M, G, D, Lq, L, K, vp, shp, stp, refp, offp, lgp, gp,
+                                                  _d(gv)[1], _d(gr)[1], _d(go)[1], _d(gl)[1], options),
            "backward_fused")
     return gv, gr, go, gl
 

@@ -27,6 +27,13 @@
  *   reference_points   [N][Len_q][n_levels][2]
  *   sampling_offsets   [N][Len_q][n_heads][n_levels][n_points][2], in pixels of level l
  *   attention_logits   [N][Len_q][n_heads][n_levels*n_points]
+ * Grouped entry points (*_grouped): the n_heads heads form n_groups groups of
+ * n_heads / n_groups consecutive heads that share one set of locations and
+ * weights, and every per-sample tensor has n_groups in place of n_heads
+ * (sampling_locations [N][Len_q][n_groups][n_levels][n_points][2], ...); head m
+ * samples with the set of group m / (n_heads / n_groups).  n_groups = n_heads is
+ * the plain call.  (The DAT pages' sampler: one offset field per group of
+ * channels, "可变形注意力…" is silent on it.)
  *
  * Readings taken where the pages are silent or disagree:
  *   - normalised -> pixel: px = loc_x * W_l - 0.5, py = loc_y * H_l - 0.5
@@ -206,7 +213,7 @@ static void gather_sample(const double *value, int64_t Len_in, int64_t n_heads, 
 /* [MSDA-tut] §2.2 (inner sum of the MSDeformAttn formula), §3.2 steps 4-5;   */
 /* [DDETR-tut] §3.3.  `fused` selects how the corner is located.              */
 /* ------------------------------------------------------------------------- */
-static int forward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, int64_t D,
+static int forward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, int64_t n_groups, int64_t D,
                         int64_t Len_q, int64_t n_levels, int64_t n_points,
                         const double *value, const int64_t *shapes, const int64_t *starts,
                         const double *loc_or_ref, const double *offsets, const double *attn,
@@ -215,6 +222,8 @@ static int forward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, i
     int align = (options & OPT_ALIGN_CORNERS) != 0;
     if (N < 0 || Len_in < 0 || n_heads <= 0 || D <= 0 || Len_q < 0 || n_levels <= 0 || n_points <= 0)
         return -1;
+    if (n_groups <= 0 || n_heads % n_groups) return -1;
+    int64_t hpg = n_heads / n_groups;           /* heads per group */
     if (check_levels(Len_in, n_levels, shapes, starts)) return -1;
     double *sample = (double *)malloc(sizeof(double) * (size_t)D);
     if (!sample) return -1;
@@ -222,11 +231,12 @@ static int forward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, i
         for (int64_t q = 0; q < Len_q; ++q)
             for (int64_t m = 0; m < n_heads; ++m) {
                 double *o = out + ((n * Len_q + q) * n_heads + m) * D;
+                int64_t gm = m / hpg;               /* the group whose locations head m samples */
                 for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
                 for (int64_t l = 0; l < n_levels; ++l) {
                     int64_t H = shapes[2 * l], W = shapes[2 * l + 1];
                     for (int64_t k = 0; k < n_points; ++k) {
-                        int64_t s = (((n * Len_q + q) * n_heads + m) * n_levels + l) * n_points + k;
+                        int64_t s = (((n * Len_q + q) * n_groups + gm) * n_levels + l) * n_points + k;
                         corners_t c;
                         if (fused) {
                             const double *ref = loc_or_ref + ((n * Len_q + q) * n_levels + l) * 2;
@@ -250,7 +260,17 @@ int msda_oracle_forward(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, i
                         const double *sampling_locations, const double *attention_weights,
                         double *output, int64_t options)
 {
-    return forward_impl(0, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+    return forward_impl(0, N, Len_in, n_heads, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+                        level_start_index, sampling_locations, NULL, attention_weights, output, options);
+}
+
+int msda_oracle_forward_grouped(int64_t N, int64_t Len_in, int64_t n_heads, int64_t n_groups, int64_t D,
+                                int64_t Len_q, int64_t n_levels, int64_t n_points, const double *value,
+                                const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                const double *sampling_locations, const double *attention_weights,
+                                double *output, int64_t options)
+{
+    return forward_impl(0, N, Len_in, n_heads, n_groups, D, Len_q, n_levels, n_points, value, spatial_shapes,
                         level_start_index, sampling_locations, NULL, attention_weights, output, options);
 }
 
@@ -266,22 +286,34 @@ static int softmax_groups(int64_t rows, int64_t n_levels, int64_t n_points, cons
 
 /* Steps a1-a5: softmax (a2) of the raw logits, then the sampling with the
  * location taken from the reference point and the pixel offset (a1). */
+int msda_oracle_forward_fused_grouped(int64_t N, int64_t Len_in, int64_t n_heads, int64_t n_groups, int64_t D,
+                                      int64_t Len_q, int64_t n_levels, int64_t n_points, const double *value,
+                                      const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                      const double *reference_points, const double *sampling_offsets,
+                                      const double *attention_logits, double *output, int64_t options)
+{
+    if (n_groups <= 0) return -1;
+    int64_t rows = N * Len_q * n_groups, cols = n_levels * n_points;
+    if (rows < 0 || cols <= 0) return -1;
+    double *attn = (double *)malloc(sizeof(double) * (size_t)(rows * cols + 1));
+    if (!attn) return -1;
+    int rc = softmax_groups(rows, n_levels, n_points, attention_logits, attn, options);
+    if (!rc)
+        rc = forward_impl(1, N, Len_in, n_heads, n_groups, D, Len_q, n_levels, n_points, value, spatial_shapes,
+                          level_start_index, reference_points, sampling_offsets, attn, output, options);
+    free(attn);
+    return rc;
+}
+
 int msda_oracle_forward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
                               int64_t n_levels, int64_t n_points, const double *value,
                               const int64_t *spatial_shapes, const int64_t *level_start_index,
                               const double *reference_points, const double *sampling_offsets,
                               const double *attention_logits, double *output, int64_t options)
 {
-    int64_t rows = N * Len_q * n_heads, cols = n_levels * n_points;
-    if (rows < 0 || cols <= 0) return -1;
-    double *attn = (double *)malloc(sizeof(double) * (size_t)(rows * cols + 1));
-    if (!attn) return -1;
-    int rc = softmax_groups(rows, n_levels, n_points, attention_logits, attn, options);
-    if (!rc)
-        rc = forward_impl(1, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
-                          level_start_index, reference_points, sampling_offsets, attn, output, options);
-    free(attn);
-    return rc;
+    return msda_oracle_forward_fused_grouped(N, Len_in, n_heads, n_heads, D, Len_q, n_levels, n_points, value,
+                                             spatial_shapes, level_start_index, reference_points, sampling_offsets,
+                                             attention_logits, output, options);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -300,7 +332,7 @@ typedef struct {
     double *grad_value, *grad_loc, *grad_attn;
 } grads_t;
 
-static int backward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, int64_t D,
+static int backward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, int64_t n_groups, int64_t D,
                          int64_t Len_q, int64_t n_levels, int64_t n_points, const double *value,
                          const int64_t *shapes, const int64_t *starts, const double *loc_or_ref,
                          const double *offsets, const double *attn, const double *grad_out,
@@ -309,18 +341,26 @@ static int backward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, 
     int align = (options & OPT_ALIGN_CORNERS) != 0;
     if (N < 0 || Len_in < 0 || n_heads <= 0 || D <= 0 || Len_q < 0 || n_levels <= 0 || n_points <= 0)
         return -1;
+    if (n_groups <= 0 || n_heads % n_groups) return -1;
     if (check_levels(Len_in, n_levels, shapes, starts)) return -1;
+    int64_t hpg = n_heads / n_groups;           /* heads per group */
     double *v = (double *)malloc(sizeof(double) * (size_t)(4 * D));
     if (!v) return -1;
     for (int64_t i = 0; i < N * Len_in * n_heads * D; ++i) gr->grad_value[i] = 0.0;
+    /* a group's location and weight gradients sum over its heads */
+    for (int64_t i = 0; i < N * Len_q * n_groups * n_levels * n_points; ++i) {
+        gr->grad_attn[i] = 0.0;
+        gr->grad_loc[2 * i] = gr->grad_loc[2 * i + 1] = 0.0;
+    }
     for (int64_t n = 0; n < N; ++n)
         for (int64_t q = 0; q < Len_q; ++q)
             for (int64_t m = 0; m < n_heads; ++m) {
                 const double *g = grad_out + ((n * Len_q + q) * n_heads + m) * D;
+                int64_t gm = m / hpg;               /* the group whose locations head m samples */
                 for (int64_t l = 0; l < n_levels; ++l) {
                     int64_t H = shapes[2 * l], W = shapes[2 * l + 1];
                     for (int64_t k = 0; k < n_points; ++k) {
-                        int64_t s = (((n * Len_q + q) * n_heads + m) * n_levels + l) * n_points + k;
+                        int64_t s = (((n * Len_q + q) * n_groups + gm) * n_levels + l) * n_points + k;
                         corners_t c;
                         if (fused) {
                             const double *ref = loc_or_ref + ((n * Len_q + q) * n_levels + l) * 2;
@@ -343,10 +383,10 @@ static int backward_impl(int fused, int64_t N, int64_t Len_in, int64_t n_heads, 
                             gx += g[d] * dsx;
                             gy += g[d] * dsy;
                         }
-                        gr->grad_attn[s] = ga;
+                        gr->grad_attn[s] += ga;
                         /* d px / d loc_x = W (W - 1 with align_corners) */
-                        gr->grad_loc[2 * s + 0] = attn[s] * gx * (double)(align ? W - 1 : W);
-                        gr->grad_loc[2 * s + 1] = attn[s] * gy * (double)(align ? H - 1 : H);
+                        gr->grad_loc[2 * s + 0] += attn[s] * gx * (double)(align ? W - 1 : W);
+                        gr->grad_loc[2 * s + 1] += attn[s] * gy * (double)(align ? H - 1 : H);
                         for (int ci = 0; ci < 4; ++ci) {
                             if (c.row[ci] < 0) continue;
                             double *gv = gr->grad_value + ((n * Len_in + c.row[ci]) * n_heads + m) * D;
@@ -367,7 +407,20 @@ int msda_oracle_backward(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, 
                          double *grad_sampling_locations, double *grad_attention_weights, int64_t options)
 {
     grads_t gr = {grad_value, grad_sampling_locations, grad_attention_weights};
-    return backward_impl(0, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+    return backward_impl(0, N, Len_in, n_heads, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+                         level_start_index, sampling_locations, NULL, attention_weights,
+                         grad_output, &gr, options);
+}
+
+int msda_oracle_backward_grouped(int64_t N, int64_t Len_in, int64_t n_heads, int64_t n_groups, int64_t D,
+                                 int64_t Len_q, int64_t n_levels, int64_t n_points, const double *value,
+                                 const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                 const double *sampling_locations, const double *attention_weights,
+                                 const double *grad_output, double *grad_value,
+                                 double *grad_sampling_locations, double *grad_attention_weights, int64_t options)
+{
+    grads_t gr = {grad_value, grad_sampling_locations, grad_attention_weights};
+    return backward_impl(0, N, Len_in, n_heads, n_groups, D, Len_q, n_levels, n_points, value, spatial_shapes,
                          level_start_index, sampling_locations, NULL, attention_weights,
                          grad_output, &gr, options);
 }
@@ -378,15 +431,16 @@ int msda_oracle_backward(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, 
 /*                                     grad_ref_x[n,q,l] = sum_{m,k} grad_loc_x */
 /*   A = softmax(logit) over j      => grad_logit_j = A_j (gA_j - sum_i A_i gA_i) */
 /* ------------------------------------------------------------------------- */
-int msda_oracle_backward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
-                               int64_t n_levels, int64_t n_points, const double *value,
-                               const int64_t *spatial_shapes, const int64_t *level_start_index,
-                               const double *reference_points, const double *sampling_offsets,
-                               const double *attention_logits, const double *grad_output,
-                               double *grad_value, double *grad_reference_points,
-                               double *grad_sampling_offsets, double *grad_attention_logits, int64_t options)
+int msda_oracle_backward_fused_grouped(int64_t N, int64_t Len_in, int64_t n_heads, int64_t n_groups, int64_t D,
+                                       int64_t Len_q, int64_t n_levels, int64_t n_points, const double *value,
+                                       const int64_t *spatial_shapes, const int64_t *level_start_index,
+                                       const double *reference_points, const double *sampling_offsets,
+                                       const double *attention_logits, const double *grad_output,
+                                       double *grad_value, double *grad_reference_points,
+                                       double *grad_sampling_offsets, double *grad_attention_logits, int64_t options)
 {
-    int64_t rows = N * Len_q * n_heads, cols = n_levels * n_points;
+    if (n_groups <= 0) return -1;
+    int64_t rows = N * Len_q * n_groups, cols = n_levels * n_points;
     if (rows < 0 || cols <= 0) return -1;
     size_t ns = (size_t)(rows * cols + 1);
     double *attn = (double *)malloc(sizeof(double) * ns);
@@ -397,14 +451,14 @@ int msda_oracle_backward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64
     rc = softmax_groups(rows, n_levels, n_points, attention_logits, attn, options);
     if (rc) goto done;
     grads_t gr = {grad_value, gloc, gattn};
-    rc = backward_impl(1, N, Len_in, n_heads, D, Len_q, n_levels, n_points, value, spatial_shapes,
+    rc = backward_impl(1, N, Len_in, n_heads, n_groups, D, Len_q, n_levels, n_points, value, spatial_shapes,
                        level_start_index, reference_points, sampling_offsets, attn, grad_output, &gr, options);
     if (rc) goto done;
     for (int64_t i = 0; i < N * Len_q * n_levels * 2; ++i) grad_reference_points[i] = 0.0;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t q = 0; q < Len_q; ++q)
-            for (int64_t m = 0; m < n_heads; ++m) {
-                int64_t r = (n * Len_q + q) * n_heads + m;
+            for (int64_t m = 0; m < n_groups; ++m) {        /* a row: one (n, q, group) */
+                int64_t r = (n * Len_q + q) * n_groups + m;
                 for (int64_t l = 0; l < n_levels; ++l) {
                     double H = (double)spatial_shapes[2 * l], W = (double)spatial_shapes[2 * l + 1];
                     double *gref = grad_reference_points + ((n * Len_q + q) * n_levels + l) * 2;
@@ -430,6 +484,20 @@ done:
     free(gloc);
     free(gattn);
     return rc;
+}
+
+int msda_oracle_backward_fused(int64_t N, int64_t Len_in, int64_t n_heads, int64_t D, int64_t Len_q,
+                               int64_t n_levels, int64_t n_points, const double *value,
+                               const int64_t *spatial_shapes, const int64_t *level_start_index,
+                               const double *reference_points, const double *sampling_offsets,
+                               const double *attention_logits, const double *grad_output,
+                               double *grad_value, double *grad_reference_points,
+                               double *grad_sampling_offsets, double *grad_attention_logits, int64_t options)
+{
+    return msda_oracle_backward_fused_grouped(N, Len_in, n_heads, n_heads, D, Len_q, n_levels, n_points, value,
+                                              spatial_shapes, level_start_index, reference_points, sampling_offsets,
+                                              attention_logits, grad_output, grad_value, grad_reference_points,
+                                              grad_sampling_offsets, grad_attention_logits, options);
 }
 
 /* ========================================================================= */

@@ -39,7 +39,8 @@ class MSDAError(RuntimeError):
 class msda_problem(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int32), ("Len_in", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("Len_q", ctypes.c_int32), ("n_levels", ctypes.c_int32),
-                ("n_points", ctypes.c_int32), ("dtype", ctypes.c_int32), ("options", ctypes.c_uint32)]
+                ("n_points", ctypes.c_int32), ("dtype", ctypes.c_int32), ("options", ctypes.c_uint32),
+                ("n_groups", ctypes.c_int32)]
 
 
 def _load():
@@ -160,25 +161,36 @@ def _check_out(t, name, shape, dtype):
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
+def groups_of(value, per_sample):
+    """G, the sets of locations of a call: per_sample [N, Len_q, G, ...] holds one
+    set per head (G = M) or one per group of M / G heads; G must divide M."""
+    M = value.shape[2]
+    G = per_sample.shape[2] if per_sample.dim() >= 3 else 0
+    if G < 1 or M % G:
+        raise ValueError(f"the per-sample tensors have {G} sets, which does not divide n_heads {M}")
+    return G
+
+
 def _check_backward_args(value, n_levels, sampling_locations, attention_weights, grad_output, grad_value=None,
                          grad_sampling_locations=None, grad_attention_weights=None, coords=2):
     """Shapes and dtypes of a backward call, checked before anything reaches
     the library (a wrong size there would be read or written out of bounds).
-    value [N,Len_in,M,D]; sampling_locations [N,Len_q,M,L,K,coords];
-    attention_weights [N,Len_q,M,L,K]; grad_output [N,Len_q,M*D] with the
-    dtype of value; the optional outputs grad_value [N,Len_in,M,D],
-    grad_sampling_locations and grad_attention_weights (shaped like the
-    locations and weights), all float32.  Returns (Len_q, L, K)."""
+    value [N,Len_in,M,D]; sampling_locations [N,Len_q,G,L,K,coords] (G = M, or
+    G groups of M / G heads); attention_weights [N,Len_q,G,L,K]; grad_output
+    [N,Len_q,M*D] with the dtype of value; the optional outputs grad_value
+    [N,Len_in,M,D], grad_sampling_locations and grad_attention_weights (shaped
+    like the locations and weights), all float32.  Returns (Len_q, L, K)."""
     if value.dim() != 4:
         raise ValueError("value must be [N, Len_in, M, D]")
     N, S, M, D = value.shape
     if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != coords:
-        raise ValueError(f"sampling_locations must be [N, Len_q, M, L, K, {coords}]")
+        raise ValueError(f"sampling_locations must be [N, Len_q, G, L, K, {coords}]")
+    G = groups_of(value, sampling_locations)
     Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
-    if tuple(sampling_locations.shape[:5]) != (N, Lq, M, L, K):
-        raise ValueError("sampling_locations disagrees with value (N or M)")
-    if tuple(attention_weights.shape) != (N, Lq, M, L, K):
-        raise ValueError("attention_weights must be [N, Len_q, M, L, K]")
+    if tuple(sampling_locations.shape[:5]) != (N, Lq, G, L, K):
+        raise ValueError("sampling_locations disagrees with value (N)")
+    if tuple(attention_weights.shape) != (N, Lq, G, L, K):
+        raise ValueError("attention_weights must be [N, Len_q, G, L, K], like sampling_locations")
     if tuple(grad_output.shape) != (N, Lq, M * D):
         raise ValueError("grad_output must be [N, Len_q, M*D]")
     if grad_output.dtype != value.dtype:
@@ -190,12 +202,13 @@ def _check_backward_args(value, n_levels, sampling_locations, attention_weights,
             raise TypeError(f"{name} must be torch.float32, got {t.dtype}")
     _check_out(grad_value, "grad_value", (N, S, M, D), torch.float32)
     _check_out(grad_sampling_locations, "grad_sampling_locations", sampling_locations.shape, torch.float32)
-    _check_out(grad_attention_weights, "grad_attention_weights", (N, Lq, M, L, K), torch.float32)
+    _check_out(grad_attention_weights, "grad_attention_weights", (N, Lq, G, L, K), torch.float32)
     return Lq, L, K
 
-def problem(value, Len_q, n_levels, n_points, options=0):
+def problem(value, Len_q, n_levels, n_points, options=0, n_groups=0):
     N, S, M, D = value.shape
-    return msda_problem(N, S, M, D, Len_q, n_levels, n_points, _dtype_code(value), options)
+    return msda_problem(N, S, M, D, Len_q, n_levels, n_points, _dtype_code(value), options,
+                        0 if n_groups == M else n_groups)
 
 
 @_on_value_device
@@ -206,9 +219,10 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
     lv = _HostLevels(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
     if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != 2:
-        raise ValueError("sampling_locations must be [N, Len_q, M, L, K, 2]")
+        raise ValueError("sampling_locations must be [N, Len_q, G, L, K, 2]")
+    G = groups_of(value, sampling_locations)
     Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
-    if tuple(sampling_locations.shape[:5]) != (N, Lq, M, L, K) or tuple(attention_weights.shape) != (N, Lq, M, L, K):
+    if tuple(sampling_locations.shape[:5]) != (N, Lq, G, L, K) or tuple(attention_weights.shape) != (N, Lq, G, L, K):
         raise ValueError("sampling_locations / attention_weights shapes disagree with value")
     if L != lv.L:
         raise ValueError("n_levels of sampling_locations and spatial_shapes disagree")
@@ -216,7 +230,7 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
         output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
     elif tuple(output.shape) != (N, Lq, M * D) or output.dtype != value.dtype:
         raise ValueError("output must be [N, Len_q, M*D] with the dtype of value")
-    prob = problem(value, Lq, L, K, options)
+    prob = problem(value, Lq, L, K, options, G)
     _check(_lib.msda_forward(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
                              _dev(sampling_locations, "sampling_locations", torch.float32),
                              _dev(attention_weights, "attention_weights", torch.float32),
@@ -232,18 +246,21 @@ def msda_forward_fused(value, spatial_shapes, level_start_index, reference_point
     lv = _HostLevels(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
     if sampling_offsets.dim() != 6 or sampling_offsets.shape[-1] != 2:
-        raise ValueError("sampling_offsets must be [N, Len_q, M, L, K, 2]")
+        raise ValueError("sampling_offsets must be [N, Len_q, G, L, K, 2]")
+    G = groups_of(value, sampling_offsets)
     Lq, L, K = sampling_offsets.shape[1], sampling_offsets.shape[3], sampling_offsets.shape[4]
+    if tuple(sampling_offsets.shape[:5]) != (N, Lq, G, L, K):
+        raise ValueError("sampling_offsets disagrees with value (N)")
     if tuple(reference_points.shape) != (N, Lq, L, 2):
         raise ValueError("reference_points must be [N, Len_q, L, 2]")
-    if attention_logits.numel() != N * Lq * M * L * K:
-        raise ValueError("attention_logits must hold N*Len_q*M*L*K values")
+    if attention_logits.numel() != N * Lq * G * L * K:
+        raise ValueError("attention_logits must hold N*Len_q*G*L*K values")
     if L != lv.L:
         raise ValueError("n_levels of sampling_offsets and spatial_shapes disagree")
     _check_out(output, "output", (N, Lq, M * D), value.dtype)
     if output is None:
         output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
-    prob = problem(value, Lq, L, K, options)
+    prob = problem(value, Lq, L, K, options, G)
     _check(_lib.msda_forward_fused(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
                                    _dev(reference_points, "reference_points", torch.float32),
                                    _dev(sampling_offsets, "sampling_offsets", torch.float32),
@@ -273,7 +290,7 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, 
         grad_sampling_locations = torch.empty_like(sampling_locations)
     if grad_attention_weights is None:
         grad_attention_weights = torch.empty_like(attention_weights)
-    prob = problem(value, Lq, L, K, options)
+    prob = problem(value, Lq, L, K, options, sampling_locations.shape[2])
     need = int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -300,11 +317,14 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
     lv = _HostLevels(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
     if sampling_offsets.dim() != 6 or sampling_offsets.shape[-1] != 2:
-        raise ValueError("sampling_offsets must be [N, Len_q, M, L, K, 2]")
+        raise ValueError("sampling_offsets must be [N, Len_q, G, L, K, 2]")
+    G = groups_of(value, sampling_offsets)
     Lq, L, K = sampling_offsets.shape[1], sampling_offsets.shape[3], sampling_offsets.shape[4]
+    if tuple(sampling_offsets.shape[:5]) != (N, Lq, G, L, K):
+        raise ValueError("sampling_offsets disagrees with value (N)")
     if tuple(reference_points.shape) != (N, Lq, L, 2):
         raise ValueError("reference_points must be [N, Len_q, L, 2]")
-    if attention_logits.numel() != N * Lq * M * L * K or tuple(grad_output.shape) != (N, Lq, M * D):
+    if attention_logits.numel() != N * Lq * G * L * K or tuple(grad_output.shape) != (N, Lq, M * D):
         raise ValueError("attention_logits / grad_output shapes disagree with value")
     if grad_output.dtype != value.dtype:
         raise TypeError("grad_output must have the dtype of value")
@@ -323,7 +343,7 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
         grad_sampling_offsets = torch.empty_like(sampling_offsets)
     if grad_attention_logits is None:
         grad_attention_logits = torch.empty_like(attention_logits)
-    prob = problem(value, Lq, L, K, options)
+    prob = problem(value, Lq, L, K, options, G)
     need = int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -356,7 +376,7 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
             raise ValueError(f"{name} must be passed: this call allocates nothing, its outputs included")
     Lq, L, K = _check_backward_args(value, lv.L, sampling_locations, attention_weights, grad_output, grad_value,
                                     grad_sampling_locations, grad_attention_weights)
-    prob = problem(value, Lq, L, K, options)
+    prob = problem(value, Lq, L, K, options, sampling_locations.shape[2])
     _check(_lib.msda_backward_noalloc(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
                                       _dev(sampling_locations, "sampling_locations", torch.float32),
                                       _dev(attention_weights, "attention_weights", torch.float32),
@@ -387,14 +407,16 @@ def msda3d_forward(value, spatial_shapes, level_start_index, sampling_locations,
     lv = _HostVolumes(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
     if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != 3:
-        raise ValueError("sampling_locations must be [N, Len_q, M, L, K, 3]")
+        raise ValueError("sampling_locations must be [N, Len_q, G, L, K, 3]")
+    G = groups_of(value, sampling_locations)
     Lq, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
-    if tuple(attention_weights.shape) != (N, Lq, M, L, K) or L != lv.L:
+    if tuple(sampling_locations.shape[:5]) != (N, Lq, G, L, K) or tuple(attention_weights.shape) != (N, Lq, G, L, K) \
+            or L != lv.L:
         raise ValueError("attention_weights / spatial_shapes disagree with sampling_locations")
     _check_out(output, "output", (N, Lq, M * D), value.dtype)
     if output is None:
         output = torch.empty((N, Lq, M * D), dtype=value.dtype, device=value.device)
-    prob = problem(value, Lq, L, K, options)
+    prob = problem(value, Lq, L, K, options, G)
     _check(_lib.msda3d_forward(ctypes.byref(prob), _dev(value, "value"), lv.shp, lv.stp,
                                _dev(sampling_locations, "sampling_locations", torch.float32),
                                _dev(attention_weights, "attention_weights", torch.float32),
@@ -418,7 +440,7 @@ def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations
         grad_sampling_locations = torch.empty_like(sampling_locations)
     if grad_attention_weights is None:
         grad_attention_weights = torch.empty_like(attention_weights)
-    prob = problem(value, Lq, L, K, options)
+    prob = problem(value, Lq, L, K, options, sampling_locations.shape[2])
     need = int(_lib.msda_backward_workspace_size(ctypes.byref(prob), flags))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)

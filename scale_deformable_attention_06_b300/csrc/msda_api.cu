@@ -23,6 +23,24 @@ msda_status fail(msda_status s, const char *fmt, ...) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Head groups: n_groups groups of n_heads / n_groups consecutive heads share
+// one set of locations and weights (0: one set per head).  A group's heads are
+// contiguous in value and in the output, so the kernels see G "heads" of
+// D = (n_heads / G) * head_dim channels; D must be a power of two from 8 to
+// max_width.
+msda_status group_width(const msda_problem *p, int max_width, int &G, int &D) {
+    if (p->head_dim < 1) return fail(MSDA_ERR_INVALID_ARG, "head_dim %d below 1", p->head_dim);
+    G = p->n_groups ? p->n_groups : p->n_heads;
+    if (G < 1 || G > p->n_heads || p->n_heads % G)
+        return fail(MSDA_ERR_INVALID_ARG, "n_groups %d does not divide n_heads %d", p->n_groups, p->n_heads);
+    const int64_t width = (int64_t)(p->n_heads / G) * p->head_dim;
+    if (width < 8 || width > max_width || (width & (width - 1)))
+        return fail(MSDA_ERR_UNSUPPORTED, "channels a group samples with one set, (n_heads / n_groups) * head_dim "
+                    "= %lld, not a power of two from 8 to %d", (long long)width, max_width);
+    D = (int)width;
+    return MSDA_OK;
+}
+
 // Checks the sizes and the levels and fills the launch geometry.
 msda_status make_geometry(const msda_problem *p, const int64_t *shapes, const int64_t *starts,
                           msda::LaunchGeometry &g) {
@@ -35,8 +53,9 @@ msda_status make_geometry(const msda_problem *p, const int64_t *shapes, const in
         return fail(MSDA_ERR_INVALID_ARG, "unknown option bits 0x%x", p->options);
     if (p->dtype != MSDA_F32 && p->dtype != MSDA_BF16)
         return fail(MSDA_ERR_UNSUPPORTED, "dtype %d is not MSDA_F32 or MSDA_BF16", p->dtype);
-    if (p->head_dim != 8 && p->head_dim != 16 && p->head_dim != 32 && p->head_dim != 64)
-        return fail(MSDA_ERR_UNSUPPORTED, "head_dim %d not in {8, 16, 32, 64}", p->head_dim);
+    int G = 0, D = 0;
+    msda_status st = group_width(p, 256, G, D);
+    if (st != MSDA_OK) return st;
     if (p->n_levels > msda::kMaxLevels)
         return fail(MSDA_ERR_UNSUPPORTED, "n_levels %d above %d", p->n_levels, msda::kMaxLevels);
     if ((int64_t)p->n_levels * p->n_points > msda::kMaxSamples)
@@ -62,19 +81,20 @@ msda_status make_geometry(const msda_problem *p, const int64_t *shapes, const in
     const int64_t pix = (int64_t)p->n_heads * p->head_dim;
     if ((p->Len_in + 2 * maxW + 4) * pix >= (int64_t(1) << 31))
         return fail(MSDA_ERR_UNSUPPORTED, "(Len_in + 2 W + 4) * n_heads * head_dim exceeds 2^31");
-    const int64_t rows = (int64_t)p->N * p->Len_q * p->n_heads;
-    if (rows >= (int64_t(1) << 31)) return fail(MSDA_ERR_UNSUPPORTED, "N * Len_q * n_heads exceeds 2^31");
+    const int64_t rows = (int64_t)p->N * p->Len_q * G;
+    if (rows >= (int64_t(1) << 31)) return fail(MSDA_ERR_UNSUPPORTED, "N * Len_q * n_groups exceeds 2^31");
 
     std::memset(&g, 0, sizeof(g));
+    g.D = D;
     g.d.N = p->N;
     g.d.Len_in = p->Len_in;
-    g.d.M = p->n_heads;
+    g.d.M = G;
     g.d.Len_q = p->Len_q;
     g.d.L = p->n_levels;
     g.d.K = p->n_points;
     g.d.P = p->n_levels * p->n_points;
     g.d.rows = (int)rows;
-    g.d.qm = p->Len_q * p->n_heads;
+    g.d.qm = p->Len_q * G;
     g.d.pix = (int)pix;
     const bool align = (p->options & MSDA_OPT_ALIGN_CORNERS) != 0;
     g.d.per_level_softmax = (p->options & MSDA_OPT_PER_LEVEL_SOFTMAX) != 0;
@@ -109,8 +129,9 @@ msda_status make_geometry3(const msda_problem *p, const int64_t *shapes, const i
         return fail(MSDA_ERR_INVALID_ARG, "unknown option bits 0x%x", p->options);
     if (p->dtype != MSDA_F32 && p->dtype != MSDA_BF16)
         return fail(MSDA_ERR_UNSUPPORTED, "dtype %d is not MSDA_F32 or MSDA_BF16", p->dtype);
-    if (p->head_dim != 8 && p->head_dim != 16 && p->head_dim != 32 && p->head_dim != 64)
-        return fail(MSDA_ERR_UNSUPPORTED, "head_dim %d not in {8, 16, 32, 64}", p->head_dim);
+    int G = 0, D = 0;
+    msda_status st = group_width(p, 64, G, D);
+    if (st != MSDA_OK) return st;
     if (p->n_levels > msda::kMaxLevels)
         return fail(MSDA_ERR_UNSUPPORTED, "n_levels %d above %d", p->n_levels, msda::kMaxLevels);
     if ((int64_t)p->n_levels * p->n_points > msda::kMaxSamples)
@@ -139,20 +160,21 @@ msda_status make_geometry3(const msda_problem *p, const int64_t *shapes, const i
     const int64_t pix = (int64_t)p->n_heads * p->head_dim;
     if ((int64_t)p->Len_in * pix >= (int64_t(1) << 31))
         return fail(MSDA_ERR_UNSUPPORTED, "Len_in * n_heads * head_dim exceeds 2^31");
-    const int64_t rows = (int64_t)p->N * p->Len_q * p->n_heads;
-    if (rows >= (int64_t(1) << 31)) return fail(MSDA_ERR_UNSUPPORTED, "N * Len_q * n_heads exceeds 2^31");
+    const int64_t rows = (int64_t)p->N * p->Len_q * G;
+    if (rows >= (int64_t(1) << 31)) return fail(MSDA_ERR_UNSUPPORTED, "N * Len_q * n_groups exceeds 2^31");
 
     std::memset(&g3, 0, sizeof(g3));
+    g3.g.D = D;
     msda::Dims &d = g3.g.d;
     d.N = p->N;
     d.Len_in = p->Len_in;
-    d.M = p->n_heads;
+    d.M = G;
     d.Len_q = p->Len_q;
     d.L = p->n_levels;
     d.K = p->n_points;
     d.P = p->n_levels * p->n_points;
     d.rows = (int)rows;
-    d.qm = p->Len_q * p->n_heads;
+    d.qm = p->Len_q * G;
     d.pix = (int)pix;
     const bool align = (p->options & MSDA_OPT_ALIGN_CORNERS) != 0;
     g3.lv.shift = align ? 0.f : 0.5f;
@@ -194,7 +216,7 @@ msda_status noalloc_check_and_geometry(const msda_problem *problem, const int64_
 msda_status noalloc_check_pointers(const msda_problem *problem, const LaunchGeometry &g, const void *value,
                                    const float *loc, const float *attn, const void *grad_out, const float *grad_value,
                                    const float *grad_loc, const float *grad_attn) {
-    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * problem->head_dim;
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * g.D;
     if (nval > 0 && !grad_value) return fail(MSDA_ERR_INVALID_ARG, "grad_value is NULL");
     if (grad_value && !aligned(grad_value, 16)) return fail(MSDA_ERR_INVALID_ARG, "grad_value not 16-byte aligned");
     if (g.d.rows > 0) {
@@ -223,7 +245,7 @@ msda_status msda_forward(const msda_problem *problem, const void *value, const i
         return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
     if (!aligned(value, 16) || !aligned(output, 16) || !aligned(sampling_locations, 8) || !aligned(attention_weights, 4))
         return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor (value/output 16 B, locations 8 B, weights 4 B)");
-    return cuda_status(msda::launch_forward(g, problem->dtype, problem->head_dim, value, sampling_locations,
+    return cuda_status(msda::launch_forward(g, problem->dtype, g.D, value, sampling_locations,
                                             attention_weights, output, static_cast<cudaStream_t>(stream)),
                        "msda_forward launch");
 }
@@ -242,7 +264,7 @@ msda_status msda_forward_fused(const msda_problem *problem, const void *value, c
     if (!aligned(value, 16) || !aligned(output, 16) || !aligned(reference_points, 8) || !aligned(sampling_offsets, 8) ||
         !aligned(attention_logits, 4))
         return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor (value/output 16 B, points/offsets 8 B, logits 4 B)");
-    return cuda_status(msda::launch_forward_fused(g, problem->dtype, problem->head_dim, value, reference_points,
+    return cuda_status(msda::launch_forward_fused(g, problem->dtype, g.D, value, reference_points,
                                                   sampling_offsets, attention_logits, output,
                                                   static_cast<cudaStream_t>(stream)),
                        "msda_forward_fused launch");
@@ -254,7 +276,7 @@ size_t msda_backward_workspace_size(const msda_problem *problem, unsigned flags)
     std::memset(&g, 0, sizeof(g));
     g.d.N = problem->N;
     g.d.Len_in = problem->Len_in;
-    g.d.M = problem->n_heads;
+    g.d.M = problem->n_heads;         // n_heads * head_dim channels a pixel, grouped or not
     return msda::backward_workspace_bytes(g, problem->head_dim, (flags & MSDA_DETERMINISTIC) != 0);
 }
 
@@ -270,7 +292,7 @@ msda_status msda_backward(const msda_problem *problem, const void *value, const 
     if (flags & ~(MSDA_DETERMINISTIC | MSDA_ACCUMULATE_GRAD_VALUE))
         return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     const bool det = (flags & MSDA_DETERMINISTIC) != 0, acc = (flags & MSDA_ACCUMULATE_GRAD_VALUE) != 0;
-    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * problem->head_dim;
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * g.D;
     if (nval > 0 && !grad_value) return fail(MSDA_ERR_INVALID_ARG, "grad_value is NULL");
     if (grad_value && !aligned(grad_value, 16)) return fail(MSDA_ERR_INVALID_ARG, "grad_value not 16-byte aligned");
     if (g.d.rows > 0) {
@@ -281,7 +303,7 @@ msda_status msda_backward(const msda_problem *problem, const void *value, const 
             !aligned(grad_sampling_locations, 8) || !aligned(attention_weights, 4) || !aligned(grad_attention_weights, 4))
             return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor");
     }
-    const size_t need = msda::backward_workspace_bytes(g, problem->head_dim, det);
+    const size_t need = msda::backward_workspace_bytes(g, g.D, det);
     if (need > 0) {
         if (!workspace || workspace_bytes < need)
             return fail(MSDA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
@@ -289,7 +311,7 @@ msda_status msda_backward(const msda_problem *problem, const void *value, const 
     }
     if (nval == 0 && g.d.rows == 0) return MSDA_OK;
     if (g.d.rows == 0 && acc) return MSDA_OK;
-    return cuda_status(msda::launch_backward(g, problem->dtype, problem->head_dim, value, sampling_locations,
+    return cuda_status(msda::launch_backward(g, problem->dtype, g.D, value, sampling_locations,
                                              attention_weights, grad_output, grad_value, grad_sampling_locations,
                                              grad_attention_weights, det, acc, workspace,
                                              static_cast<cudaStream_t>(stream)),
@@ -309,7 +331,7 @@ msda_status msda_backward_fused(const msda_problem *problem, const void *value, 
     if (flags & ~(MSDA_DETERMINISTIC | MSDA_ACCUMULATE_GRAD_VALUE))
         return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     const bool det = (flags & MSDA_DETERMINISTIC) != 0, acc = (flags & MSDA_ACCUMULATE_GRAD_VALUE) != 0;
-    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * problem->head_dim;
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * g.D;
     if (nval > 0 && !grad_value) return fail(MSDA_ERR_INVALID_ARG, "grad_value is NULL");
     if (grad_value && !aligned(grad_value, 16)) return fail(MSDA_ERR_INVALID_ARG, "grad_value not 16-byte aligned");
     if (g.d.rows > 0) {
@@ -321,7 +343,7 @@ msda_status msda_backward_fused(const msda_problem *problem, const void *value, 
             !aligned(attention_logits, 4) || !aligned(grad_attention_logits, 4))
             return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor");
     }
-    const size_t need = msda::backward_workspace_bytes(g, problem->head_dim, det);
+    const size_t need = msda::backward_workspace_bytes(g, g.D, det);
     if (need > 0) {
         if (!workspace || workspace_bytes < need)
             return fail(MSDA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
@@ -329,7 +351,7 @@ msda_status msda_backward_fused(const msda_problem *problem, const void *value, 
     }
     if (nval == 0 && g.d.rows == 0) return MSDA_OK;
     if (g.d.rows == 0 && acc) return MSDA_OK;
-    return cuda_status(msda::launch_backward_fused(g, problem->dtype, problem->head_dim, value, reference_points,
+    return cuda_status(msda::launch_backward_fused(g, problem->dtype, g.D, value, reference_points,
                                                    sampling_offsets, attention_logits, grad_output, grad_value,
                                                    grad_reference_points, grad_sampling_offsets, grad_attention_logits,
                                                    det, acc, workspace, static_cast<cudaStream_t>(stream)),
@@ -348,7 +370,7 @@ msda_status msda3d_forward(const msda_problem *problem, const void *value, const
         return fail(MSDA_ERR_INVALID_ARG, "a tensor pointer is NULL");
     if (!aligned(value, 16) || !aligned(output, 16) || !aligned(sampling_locations, 4) || !aligned(attention_weights, 4))
         return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor (value/output 16 B, locations and weights 4 B)");
-    return cuda_status(msda::launch_forward3d(g, problem->dtype, problem->head_dim, value, sampling_locations,
+    return cuda_status(msda::launch_forward3d(g, problem->dtype, g.g.D, value, sampling_locations,
                                               attention_weights, output, static_cast<cudaStream_t>(stream)),
                        "msda3d_forward launch");
 }
@@ -365,7 +387,7 @@ msda_status msda3d_backward(const msda_problem *problem, const void *value, cons
     if (flags & ~(MSDA_DETERMINISTIC | MSDA_ACCUMULATE_GRAD_VALUE))
         return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     const bool det = (flags & MSDA_DETERMINISTIC) != 0, acc = (flags & MSDA_ACCUMULATE_GRAD_VALUE) != 0;
-    const size_t nval = (size_t)g.g.d.N * g.g.d.Len_in * g.g.d.M * problem->head_dim;
+    const size_t nval = (size_t)g.g.d.N * g.g.d.Len_in * g.g.d.M * g.g.D;
     if (nval > 0 && !grad_value) return fail(MSDA_ERR_INVALID_ARG, "grad_value is NULL");
     if (grad_value && !aligned(grad_value, 16)) return fail(MSDA_ERR_INVALID_ARG, "grad_value not 16-byte aligned");
     if (g.g.d.rows > 0) {
@@ -376,7 +398,7 @@ msda_status msda3d_backward(const msda_problem *problem, const void *value, cons
             !aligned(grad_sampling_locations, 4) || !aligned(attention_weights, 4) || !aligned(grad_attention_weights, 4))
             return fail(MSDA_ERR_INVALID_ARG, "misaligned tensor");
     }
-    const size_t need = msda::backward_workspace_bytes(g.g, problem->head_dim, det);
+    const size_t need = msda::backward_workspace_bytes(g.g, g.g.D, det);
     if (need > 0) {
         if (!workspace || workspace_bytes < need)
             return fail(MSDA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
@@ -384,7 +406,7 @@ msda_status msda3d_backward(const msda_problem *problem, const void *value, cons
     }
     if (nval == 0 && g.g.d.rows == 0) return MSDA_OK;
     if (g.g.d.rows == 0 && acc) return MSDA_OK;
-    return cuda_status(msda::launch_backward3d(g, problem->dtype, problem->head_dim, value, sampling_locations,
+    return cuda_status(msda::launch_backward3d(g, problem->dtype, g.g.D, value, sampling_locations,
                                                attention_weights, grad_output, grad_value, grad_sampling_locations,
                                                grad_attention_weights, det, acc, workspace,
                                                static_cast<cudaStream_t>(stream)),

@@ -100,15 +100,26 @@ struct BwdWarpSmem<HW, RC, true> {
     int count;
 };
 
+// Lanes of the backward for head_dim D: R lanes a query, 4 channels a vector,
+// NV vectors a lane (vector k of lane ch: channels 4 * (k * R + ch) ..), HW
+// queries a warp.
+template <int D>
+struct BwdLanes {
+    static constexpr int R = D / 4 < 32 ? D / 4 : 32;
+    static constexpr int NV = D / (4 * R);
+    static constexpr int HW = 32 / R;
+};
+
 // OPTS: the problem sets option bits (fused calls); without them the kernel
 // carries none of the option code.  Resident blocks per SM: four in
 // deterministic mode; three in fp32 mode, which leaves the L1 cache more of
 // the SM's memory beside the blocks' shared memory (measured faster there,
-// slower in deterministic mode).
+// slower in deterministic mode); three for head widths above 64 (two vectors
+// a lane need the registers).
 template <typename T, int D, bool DET, bool MERGE, bool FUSED, bool OPTS>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, DET ? 4 : 3)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, (DET && D <= 64) ? 4 : 3)
 msda_backward_kernel(const __grid_constant__ BwdArgs a) {
-    constexpr int R = D / 4, HW = 32 / R;
+    constexpr int R = BwdLanes<D>::R, HW = BwdLanes<D>::HW, NV = BwdLanes<D>::NV;
     constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
     static_assert(HW * RC == 64, "phase 1 and 3 give every lane two (query, sample) slots");
     static_assert(!MERGE || HW == 4, "the merge table holds four queries per slot");
@@ -133,8 +144,13 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     const T *vbase = static_cast<const T *>(a.value) + vhead;
     const uint64_t pol = l2_keep_policy();
 
-    float4 g = load4_stream<T>(static_cast<const T *>(a.grad_out) + (size_t)row * D + ch * 4);
-    if (!row_ok) g = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 gv[NV];                               // this lane's channels of grad_output
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        gv[k] = load4_stream<T>(static_cast<const T *>(a.grad_out) + (size_t)row * D + (k * R + ch) * 4);
+        if (!row_ok) gv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float4 &g = gv[0];
     float scale = 1.f;
     if constexpr (DET) scale = ldexpf(1.f, fixed_shift(a.bound_bits[n], dm.qm));   // this batch element's scale
 
@@ -151,7 +167,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     // pass of their own before the records, since every sample's gradient
     // needs its normalised weight
     const bool row_softmax = FUSED && !(OPTS && dm.per_level_softmax);
-    const bool seg_stats = (RC >= 16) && row_softmax && P <= RC;
+    const bool seg_stats = (RC >= 16 && RC <= 32) && row_softmax && P <= RC;
     if (row_softmax && !seg_stats) {
         row_softmax_stats<HW>(a.logits + ((size_t)(n * dm.Len_q + qb * HW) * dm.M + m) * P, (size_t)dm.M * P, P,
                           min(HW, dm.Len_q - qb * HW), lane, sm.stat);
@@ -257,17 +273,26 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 // bilinear weights; an outside corner's weight is never used (its
                 // dot product is zeroed and it is not scattered)
                 const float w[4] = {(1.f - fx) * (1.f - fy), fx * (1.f - fy), (1.f - fx) * fy, fx * fy};
-                float4 v[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) v[c] = load4_value(vbase + off[c], pol);
                 // partial <g, v_c> over this lane's channels (two packed products
-                // per corner); corners outside the map read as zero
+                // per corner and vector); corners outside the map read as zero
                 float t[4];
+                {
+                    float2 pr[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float2 pr = __fmul2_rn(make_float2(g.x, g.y), make_float2(v[c].x, v[c].y));
-                    pr = __ffma2_rn(make_float2(g.z, g.w), make_float2(v[c].z, v[c].w), pr);
-                    t[c] = in[c] ? pr.x + pr.y : 0.f;
+                    for (int k = 0; k < NV; ++k) {
+                        float4 v[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) v[c] = load4_value(vbase + off[c] + k * 4 * R, pol);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            pr[c] = k == 0 ? __fmul2_rn(make_float2(gv[k].x, gv[k].y), make_float2(v[c].x, v[c].y))
+                                           : __ffma2_rn(make_float2(gv[k].x, gv[k].y), make_float2(v[c].x, v[c].y),
+                                                        pr[c]);
+                            pr[c] = __ffma2_rn(make_float2(gv[k].z, gv[k].w), make_float2(v[c].z, v[c].w), pr[c]);
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) t[c] = in[c] ? pr[c].x + pr[c].y : 0.f;
                 }
                 // partial grad_attn, d/dpx, d/dpy
                 const float pga = w[0] * t[0] + w[1] * t[1] + w[2] * t[2] + w[3] * t[3];
@@ -287,9 +312,13 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                         for (int c = 0; c < 4; ++c) {
                             if (!in[c]) continue;
                             const float cw = A * w[c];
-                            const float2 lo = __fmul2_rn(make_float2(cw, cw), make_float2(g.x, g.y));
-                            const float2 hi = __fmul2_rn(make_float2(cw, cw), make_float2(g.z, g.w));
-                            scatter4<DET, R>(a, vhead + off[c], ch, make_float4(lo.x, lo.y, hi.x, hi.y), scale);
+#pragma unroll
+                            for (int k = 0; k < NV; ++k) {
+                                const float2 lo = __fmul2_rn(make_float2(cw, cw), make_float2(gv[k].x, gv[k].y));
+                                const float2 hi = __fmul2_rn(make_float2(cw, cw), make_float2(gv[k].z, gv[k].w));
+                                scatter4<DET, R>(a, vhead + off[c] + k * 4 * R, ch, make_float4(lo.x, lo.y, hi.x, hi.y),
+                                                 scale);
+                            }
                         }
                     } else if constexpr (MERGE) {
                         // lanes ch < 4 insert corner c = ch of their query; the valid
@@ -427,6 +456,10 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
             for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
             tot[it] = v;
         }
+        if constexpr (RC > 32) {          // one query a warp: both of a lane's slots are its samples
+            tot[0] += tot[1];
+            tot[1] = tot[0];
+        }
         if (OPTS && dm.per_level_softmax) {
             // groups are the levels.  Their K grad_A were written by several
             // lanes (and a level may straddle two record chunks), so first every
@@ -557,7 +590,7 @@ __global__ void row_bound_kernel(const float *attn, const T *grad_out, int N, in
 __global__ void fixed_to_f32_kernel(const unsigned long long *fixed, const unsigned *bound_bits, int N,
                                     int rows_per_batch, float4 *grad_value, size_t n4_per_batch, int D,
                                     int accumulate) {
-    const size_t R = (size_t)(D >> 2);
+    const size_t R = (size_t)((D >> 2) < 32 ? (D >> 2) : 32);    // lanes of a query: blocks of 4R words
     for (int n = blockIdx.y; n < N; n += gridDim.y) {
         const int shift = fixed_shift(bound_bits[n], rows_per_batch);
         const unsigned long long *fx = fixed + (size_t)n * n4_per_batch * 4;
@@ -637,6 +670,8 @@ cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const fl
                     case 16: MSDA_BOUND(float, 16); break;
                     case 32: MSDA_BOUND(float, 32); break;
                     case 64: MSDA_BOUND(float, 64); break;
+                    case 128: MSDA_BOUND(float, 128); break;
+                    case 256: MSDA_BOUND(float, 256); break;
                 }
             } else {
                 switch (D) {
@@ -644,6 +679,8 @@ cudaError_t backward_prepare(const LaunchGeometry &g, int dtype, int D, const fl
                     case 16: MSDA_BOUND(__nv_bfloat16, 16); break;
                     case 32: MSDA_BOUND(__nv_bfloat16, 32); break;
                     case 64: MSDA_BOUND(__nv_bfloat16, 64); break;
+                    case 128: MSDA_BOUND(__nv_bfloat16, 128); break;
+                    case 256: MSDA_BOUND(__nv_bfloat16, 256); break;
                 }
             }
 #undef MSDA_BOUND
@@ -679,7 +716,7 @@ struct BwdIO {
 
 template <typename T, int D, bool FUSED, bool OPTS>
 static void launch_bwd_kernel(const BwdArgs &a, bool det, unsigned blocks, cudaStream_t stream) {
-    constexpr int HW = 32 / (D / 4);
+    constexpr int HW = BwdLanes<D>::HW;
     constexpr int B = kWarpsPerBlock * 32;
     const bool merge = a.merge_mask != 0;
     if constexpr (HW == 4) {
@@ -696,7 +733,7 @@ static void launch_bwd_kernel(const BwdArgs &a, bool det, unsigned blocks, cudaS
 template <typename T, int D, bool FUSED>
 static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool det, bool accumulate, void *workspace,
                                 cudaStream_t stream) {
-    constexpr int HW = 32 / (D / 4);
+    constexpr int HW = BwdLanes<D>::HW;
     BwdArgs a{};
     a.value = io.value;
     a.loc = io.loc;
@@ -752,6 +789,8 @@ static cudaError_t dispatch_bwd(const LaunchGeometry &g, int dtype, int D, const
             case 16: return launch_bwd_t<float, 16, FUSED>(g, io, det, accumulate, workspace, stream);
             case 32: return launch_bwd_t<float, 32, FUSED>(g, io, det, accumulate, workspace, stream);
             case 64: return launch_bwd_t<float, 64, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 128: return launch_bwd_t<float, 128, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 256: return launch_bwd_t<float, 256, FUSED>(g, io, det, accumulate, workspace, stream);
         }
     } else {
         switch (D) {
@@ -759,6 +798,8 @@ static cudaError_t dispatch_bwd(const LaunchGeometry &g, int dtype, int D, const
             case 16: return launch_bwd_t<__nv_bfloat16, 16, FUSED>(g, io, det, accumulate, workspace, stream);
             case 32: return launch_bwd_t<__nv_bfloat16, 32, FUSED>(g, io, det, accumulate, workspace, stream);
             case 64: return launch_bwd_t<__nv_bfloat16, 64, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 128: return launch_bwd_t<__nv_bfloat16, 128, FUSED>(g, io, det, accumulate, workspace, stream);
+            case 256: return launch_bwd_t<__nv_bfloat16, 256, FUSED>(g, io, det, accumulate, workspace, stream);
         }
     }
     return cudaErrorInvalidValue;

@@ -44,13 +44,16 @@ struct Dims {
 };
 
 // Elements of T carried by one 16-byte load, and the lane layout that follows:
-// R lanes cover the D channels of one row, a warp covers HW = 32 / R rows.
+// R lanes cover the D channels of one row, NV 16-byte vectors a lane (vector
+// k of lane ch holds channels (k * R + ch) * V ..), a warp covers HW = 32 / R
+// rows.
 template <typename T, int D>
 struct Layout {
     static constexpr int V = 16 / (int)sizeof(T);
-    static constexpr int R = D / V;
+    static constexpr int R = D / V < 32 ? D / V : 32;
+    static constexpr int NV = D / (V * R);
     static constexpr int HW = 32 / R;
-    static_assert(D % V == 0 && R >= 1 && R <= 32 && (R & (R - 1)) == 0, "unsupported head_dim");
+    static_assert(D % V == 0 && R >= 1 && (R & (R - 1)) == 0 && NV * V * R == D, "unsupported head_dim");
 };
 
 // ---- 16-byte vectors ------------------------------------------------------

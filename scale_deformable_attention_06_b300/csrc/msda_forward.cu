@@ -9,7 +9,8 @@
 //
 // Work decomposition.  A "row" is one (n, q, m).  A warp owns HW = 32 / R
 // consecutive rows, R lanes per row, each lane holding 16 bytes of the row's
-// D channels (4 fp32 or 8 bf16).  Per chunk of samples:
+// D channels (4 fp32 or 8 bf16), NV such vectors where a row is wider than 32
+// of them (head_dim 256 fp32).  Per chunk of samples:
 //   phase 1: each lane computes the corner records (four element offsets and
 //            four weights, attention weight folded in) of one or two samples,
 //            coalesced over the warp's rows, into warp-private shared memory;
@@ -48,7 +49,7 @@ constexpr int kFwdMinBlocksF32 = 5;
 template <typename T, int D, bool FUSED, bool OPTS>
 __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     using Lay = Layout<T, D>;
-    constexpr int V = Lay::V, R = Lay::R, HW = Lay::HW;
+    constexpr int V = Lay::V, R = Lay::R, HW = Lay::HW, NV = Lay::NV;
     constexpr int JC = kRecordsPerWarp / HW;     // samples of each row per chunk
 
     __shared__ int4 s_off[kWarpsPerBlock][kRecordsPerWarp];
@@ -83,9 +84,11 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     const T *vbase = static_cast<const T *>(a.value) + ((size_t)n * dm.Len_in * dm.M + m) * D + ch * V;
     const uint64_t pol = l2_keep_policy();
 
-    float acc[V];
+    float acc[NV][V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[k][i] = 0.f;
 
     // seg_stats: the attention weight of each of this lane's two record slots
     // (slot it = record lane + 32 it, one row: HW divides 32)
@@ -198,21 +201,27 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
             if (online) {                                   // rescale to the row's new running max
                 const float sc = s_stat[warp][h].x;
 #pragma unroll
-                for (int v = 0; v < V; ++v) acc[v] *= sc;
+                for (int k = 0; k < NV; ++k)
+#pragma unroll
+                    for (int v = 0; v < V; ++v) acc[k][v] *= sc;
             }
         }
 #pragma unroll 2
         for (int j = 0; j < J; ++j) {
             const int4 o = s_off[warp][j * HW + h];
             const float4 w = s_w[warp][j * HW + h];
-            const Vec<T> v0 = load_value(vbase + o.x, pol);
-            const Vec<T> v1 = load_value(vbase + o.y, pol);
-            const Vec<T> v2 = load_value(vbase + o.z, pol);
-            const Vec<T> v3 = load_value(vbase + o.w, pol);
-            fma_row<T, V>(acc, w.x, v0);
-            fma_row<T, V>(acc, w.y, v1);
-            fma_row<T, V>(acc, w.z, v2);
-            fma_row<T, V>(acc, w.w, v3);
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {         // vector k: channels (k * R + ch) * V ..
+                const T *vb = vbase + k * R * V;
+                const Vec<T> v0 = load_value(vb + o.x, pol);
+                const Vec<T> v1 = load_value(vb + o.y, pol);
+                const Vec<T> v2 = load_value(vb + o.z, pol);
+                const Vec<T> v3 = load_value(vb + o.w, pol);
+                fma_row<T, V>(acc[k], w.x, v0);
+                fma_row<T, V>(acc[k], w.y, v1);
+                fma_row<T, V>(acc[k], w.z, v2);
+                fma_row<T, V>(acc[k], w.w, v3);
+            }
         }
         __syncwarp();
     }
@@ -220,15 +229,21 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         if (online) {                                       // divide by the row's sum
             const float inv = 1.f / s_stat[warp][h].y;
 #pragma unroll
-            for (int v = 0; v < V; ++v) acc[v] *= inv;
+            for (int k = 0; k < NV; ++k)
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[k][v] *= inv;
         }
     }
-    if (row_ok) store_row<T, V>(static_cast<T *>(a.out) + (size_t)row * D + ch * V, acc);
+    if (row_ok) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            store_row<T, V>(static_cast<T *>(a.out) + (size_t)row * D + (k * R + ch) * V, acc[k]);
+    }
 }
 
 template <typename T, int D, bool FUSED, bool OPTS>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, kFwdMinBlocksF32)
-msda_forward_kernel(const __grid_constant__ FwdArgs a) {       // fp32 value
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, D > 128 ? 3 : kFwdMinBlocksF32)
+msda_forward_kernel(const __grid_constant__ FwdArgs a) {       // fp32 value (two vectors a lane at D = 256: three blocks)
     forward_body<T, D, FUSED, OPTS>(a);
 }
 
@@ -266,6 +281,8 @@ static cudaError_t dispatch_fwd(const FwdArgs &args, int dtype, int D, cudaStrea
             case 16: return launch_fwd<float, 16, FUSED>(args, stream);
             case 32: return launch_fwd<float, 32, FUSED>(args, stream);
             case 64: return launch_fwd<float, 64, FUSED>(args, stream);
+            case 128: return launch_fwd<float, 128, FUSED>(args, stream);
+            case 256: return launch_fwd<float, 256, FUSED>(args, stream);
         }
     } else {
         switch (D) {
@@ -273,6 +290,8 @@ static cudaError_t dispatch_fwd(const FwdArgs &args, int dtype, int D, cudaStrea
             case 16: return launch_fwd<__nv_bfloat16, 16, FUSED>(args, stream);
             case 32: return launch_fwd<__nv_bfloat16, 32, FUSED>(args, stream);
             case 64: return launch_fwd<__nv_bfloat16, 64, FUSED>(args, stream);
+            case 128: return launch_fwd<__nv_bfloat16, 128, FUSED>(args, stream);
+            case 256: return launch_fwd<__nv_bfloat16, 256, FUSED>(args, stream);
         }
     }
     return cudaErrorInvalidValue;

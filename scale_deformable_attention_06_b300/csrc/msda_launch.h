@@ -11,9 +11,10 @@ namespace msda {
 // Everything the kernels need to know about the sizes and the levels; filled
 // and checked on the host by msda_api.cu.
 struct LaunchGeometry {
-    Dims d;
+    Dims d;                 // d.M: sets of locations (heads, or head groups)
     LevelTable lv;
     unsigned char level_of[kMaxSamples];
+    int D;                  // channels sampled with one set: head_dim, or heads per group * head_dim
 };
 
 cudaError_t launch_forward(const LaunchGeometry &g, int dtype, int D, const void *value, const float *loc,

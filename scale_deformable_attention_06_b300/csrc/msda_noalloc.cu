@@ -61,7 +61,7 @@ extern "C" msda_status msda_backward_noalloc(const msda_problem *problem, const 
     if (st != MSDA_OK) return st;
     if (flags & ~MSDA_ACCUMULATE_GRAD_VALUE)
         return msda::noalloc_fail(MSDA_ERR_INVALID_ARG, "msda_backward_noalloc: only MSDA_ACCUMULATE_GRAD_VALUE is accepted");
-    const size_t need = msda::backward_workspace_bytes(g, problem->head_dim, true);
+    const size_t need = msda::backward_workspace_bytes(g, g.D, true);
     if (need > kNoallocScratchBytes) {
         char msg[400];
         snprintf(msg, sizeof(msg),
@@ -74,7 +74,7 @@ extern "C" msda_status msda_backward_noalloc(const msda_problem *problem, const 
     st = msda::noalloc_check_pointers(problem, g, value, sampling_locations, attention_weights, grad_output, grad_value,
                                       grad_sampling_locations, grad_attention_weights);
     if (st != MSDA_OK) return st;
-    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * problem->head_dim;
+    const size_t nval = (size_t)g.d.N * g.d.Len_in * g.d.M * g.D;
     const bool acc = (flags & MSDA_ACCUMULATE_GRAD_VALUE) != 0;
     if (nval == 0 && g.d.rows == 0) return MSDA_OK;
     if (g.d.rows == 0 && acc) return MSDA_OK;
@@ -91,7 +91,7 @@ extern "C" msda_status msda_backward_noalloc(const msda_problem *problem, const 
     // launch_backward clears the fixed-point accumulators and the bound header
     // in the scratch before it sums into them, so the previous call's contents
     // do not leak into this one.
-    e = msda::launch_backward(g, problem->dtype, problem->head_dim, value, sampling_locations, attention_weights,
+    e = msda::launch_backward(g, problem->dtype, g.D, value, sampling_locations, attention_weights,
                               grad_output, grad_value, grad_sampling_locations, grad_attention_weights, true, acc,
                               scratch, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {

@@ -52,7 +52,7 @@ int main(void)
     cudaMemcpy(dloc, hloc, nsmp * 8, cudaMemcpyHostToDevice);
     cudaMemcpy(dA, hA, nsmp * 4, cudaMemcpyHostToDevice);
 
-    msda_problem p = {N, S, M, D, LQ, L, K, MSDA_F32, 0u};
+    msda_problem p = {N, S, M, D, LQ, L, K, MSDA_F32, 0u, 0};
     msda_status st = msda_forward(&p, dv, shapes, starts, dloc, dA, dout, NULL);
     if (st != MSDA_OK) {
         fprintf(stderr, "msda_forward: %s: %s\n", msda_status_string(st), msda_last_error());

@@ -25,6 +25,11 @@ What pins what:
   adjoint             <grad_value, dV> = <g, forward(dV)> (the forward is linear in value).
   fused_*             a9 and the fused forward: finite differences through
                       a1-a2, sum of logit gradients is 0, composition with a1/a2.
+  grouped_*           locations and weights shared by a group of heads (the DAT
+                      pages' sampler): the per-head call on the sets broadcast
+                      to every head, gradients summed over each group (forward,
+                      backward, fused forward and backward); and the plain call
+                      on value viewed as G heads of (M / G) * D channels.
   align_*             the align_corners option (px = loc * (W - 1)): torch
                       grid_sample(align_corners=True) forward and autograd in
                       float64, and exact gathers at loc = i / (W - 1).
@@ -402,6 +407,74 @@ def pin_fused_backward():
     return worst, 1e-6
 
 
+# --------------------------------------------------------------------------- grouped locations
+def _grouped_inputs(seed, G, M=4, levels=((6, 7), (3, 4)), N=2, Lq=7, K=3, D=3):
+    """Per-sample tensors with G groups of M / G heads (one set of locations,
+    weights, offsets and logits per group)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shapes = np.asarray(levels, dtype=np.int64)
+    starts = workloads.level_start_index(shapes)
+    S = int((shapes[:, 0] * shapes[:, 1]).sum())
+    L = len(levels)
+    scale = np.asarray([[w, h] for (h, w) in levels], dtype=np.float64)
+    return dict(shapes=shapes, starts=starts, value=rng.standard_normal((N, S, M, D)),
+                g=rng.standard_normal((N, Lq, M * D)), loc=rng.uniform(-0.1, 1.1, (N, Lq, G, L, K, 2)),
+                attn=rng.uniform(-0.5, 1.0, (N, Lq, G, L, K)), ref=rng.uniform(0.1, 0.9, (N, Lq, L, 2)),
+                off=rng.standard_normal((N, Lq, G, L, K, 2)) * 0.3 * scale[None, None, None, :, None, :],
+                logits=rng.standard_normal((N, Lq, G, L * K)), M=M, G=G)
+
+
+def _to_heads(x, M):
+    """Broadcast a per-group tensor [N, Lq, G, ...] to every head of its group."""
+    return np.repeat(x, M // x.shape[2], axis=2)
+
+
+def _sum_groups(x, G):
+    """Sum a per-head tensor [N, Lq, M, ...] over the heads of each group."""
+    return x.reshape(x.shape[:2] + (G, x.shape[2] // G) + x.shape[3:]).sum(axis=3)
+
+
+def pin_grouped_broadcast():
+    """A group's heads sample with the group's set: the grouped call equals the
+    per-head call on the set broadcast to every head of its group, and its
+    location, weight, offset and logit gradients are the per-head ones summed
+    over the group (the chain rule through the broadcast); grad_value and the
+    reference-point gradient are the same.  G = 1, 2 of M = 4 heads."""
+    worst = 0.0
+    for G in (1, 2):
+        f = _grouped_inputs(61 + G, G)
+        M, sh, st = f["M"], f["shapes"], f["starts"]
+        loc_h, attn_h = _to_heads(f["loc"], M), _to_heads(f["attn"], M)
+        worst = max(worst, _err(oracle.forward(f["value"], sh, st, f["loc"], f["attn"]),
+                                oracle.forward(f["value"], sh, st, loc_h, attn_h)))
+        gv, gl, ga = oracle.backward(f["value"], sh, st, f["loc"], f["attn"], f["g"])
+        hv, hl, ha = oracle.backward(f["value"], sh, st, loc_h, attn_h, f["g"])
+        worst = max(worst, _err(gv, hv), _err(gl, _sum_groups(hl, G)), _err(ga, _sum_groups(ha, G)))
+        off_h, lg_h = _to_heads(f["off"], M), _to_heads(f["logits"], M)
+        worst = max(worst, _err(oracle.forward_fused(f["value"], sh, st, f["ref"], f["off"], f["logits"]),
+                                oracle.forward_fused(f["value"], sh, st, f["ref"], off_h, lg_h)))
+        fg = oracle.backward_fused(f["value"], sh, st, f["ref"], f["off"], f["logits"], f["g"])
+        fh = oracle.backward_fused(f["value"], sh, st, f["ref"], off_h, lg_h, f["g"])
+        worst = max(worst, _err(fg[0], fh[0]), _err(fg[1], fh[1]), _err(fg[2], _sum_groups(fh[2], G)),
+                    _err(fg[3], _sum_groups(fh[3], G)))
+    return worst, 1e-12
+
+
+def pin_grouped_as_wide_heads():
+    """A group's heads are contiguous in value and in the output, so G groups of
+    M / G heads of D channels are the plain call with G heads of (M / G) * D
+    channels (the value tensor viewed as [N, Len_in, G, (M / G) * D])."""
+    f = _grouped_inputs(71, 2)
+    N, S, M, D = f["value"].shape
+    G, sh, st = f["G"], f["shapes"], f["starts"]
+    wide = f["value"].reshape(N, S, G, M // G * D)
+    worst = _err(oracle.forward(f["value"], sh, st, f["loc"], f["attn"]),
+                 oracle.forward(wide, sh, st, f["loc"], f["attn"]))
+    gv, gl, ga = oracle.backward(f["value"], sh, st, f["loc"], f["attn"], f["g"])
+    wv, wl, wa = oracle.backward(wide, sh, st, f["loc"], f["attn"], f["g"])
+    return max(worst, _err(gv, wv.reshape(gv.shape)), _err(gl, wl), _err(ga, wa)), 1e-12
+
+
 # --------------------------------------------------------------------------- options
 AL = oracle.ALIGN_CORNERS
 PL = oracle.PER_LEVEL_SOFTMAX
@@ -628,6 +701,8 @@ ALL_PINS = {
     "adjoint": pin_adjoint,
     "fused_composition": pin_fused_composition,
     "fused_backward": pin_fused_backward,
+    "grouped_broadcast": pin_grouped_broadcast,
+    "grouped_as_wide_heads": pin_grouped_as_wide_heads,
     "align_grid_sample": pin_align_grid_sample,
     "align_pixel_centres": pin_align_pixel_centres,
     "align_backward_autograd": pin_align_backward_autograd,

@@ -78,6 +78,10 @@ FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails i
     (dict(N=-1), [8, 8, 4, 4], [0, 64], 1),
     (dict(n_heads=0), [8, 8, 4, 4], [0, 64], 1),
     (dict(options=4), [8, 8, 4, 4], [0, 64], 1),
+    (dict(n_groups=3), [8, 8, 4, 4], [0, 64], 1),                   # does not divide the 2 heads
+    (dict(n_groups=-1), [8, 8, 4, 4], [0, 64], 1),
+    (dict(n_heads=3, n_groups=1), [8, 8, 4, 4], [0, 64], 2),       # 24 channels a set: not a power of two
+    (dict(n_heads=2, head_dim=256, n_groups=1), [8, 8, 4, 4], [0, 64], 2),   # 512 channels a set
 ])
 def test_host_checks_reject_before_launch(msda, kw, shapes, starts, expect):
     p = _problem(msda, **kw)

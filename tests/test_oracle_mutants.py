@@ -48,6 +48,9 @@ MUTANTS = [
     ("trilinear_z_bound", "zc >= 0 && zc < Dd)", "zc >= 0 && zc <= Dd)"),
     ("trilinear_grad_z_scale", "(double)(align ? sh[0] - 1 : sh[0])};", "(double)(align ? sh[1] - 1 : sh[1])};"),
     ("trilinear_grad_sign", "double dw = bit[a] ? 1.0 : -1.0;", "double dw = bit[a] ? -1.0 : 1.0;"),
+    ("group_index_interleaved", "int64_t gm = m / hpg;", "int64_t gm = m % n_groups;"),
+    ("grouped_grad_attn_not_summed", "gr->grad_attn[s] += ga;", "gr->grad_attn[s] = ga;"),
+    ("grouped_grad_loc_not_summed", "gr->grad_loc[2 * s + 0] += attn[s] * gx", "gr->grad_loc[2 * s + 0] = attn[s] * gx"),
 ]
 
 

@@ -612,3 +612,76 @@ def test_query_split_of_one_batch_element(msda):
         gv_sum += gv
     ref = _oracle_backward(p).for_gpu((gv_sum, whole_bwd[1], whole_bwd[2]))
     H.assert_bwd(gv_sum, ref[0], "f32", "grad_value summed over the query halves")
+
+
+# ----------------------------------------------------------------- head groups sharing one set of locations
+PER_SAMPLE = ("sampling_locations", "attention_weights", "sampling_offsets", "attention_logits")
+
+
+def _grouped(p, G):
+    """The inputs cut to G sets of locations and weights: the per-sample tensors
+    keep their first G heads' sets, shared by groups of M / G heads."""
+    return {k: (np.ascontiguousarray(v[:, :, :G]) if k in PER_SAMPLE else v) for k, v in p.items()}
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("G,K", [(1, 4), (2, 4), (4, 4), (1, 20)])
+def test_grouped_locations_all_calls(msda, dtype, G, K):
+    """8 heads of 32 channels in G groups that each share one set of locations
+    and weights (the DAT pages' sampler): the kernels sample 256 / G channels a
+    set (G = 1: two 16-byte vectors a lane in fp32).  Every call against the
+    oracle's grouped form; K = 20 gives rows of 80 samples over two record
+    chunks.  Ragged Len_q, samples partly outside the maps."""
+    levels = [(23, 31), (12, 16), (6, 8), (3, 4)]
+    w = workloads.custom(N=2, M=8, D=32, levels=levels, K=K, Len_q=53, dtype=dtype, refs="uniform",
+                         ref_range=(-0.05, 1.05), offset_sigma=0.1, seed=2000 + 10 * G + K)
+    p = _grouped(H.prepared(w), G)
+    dt = H.storage_dtype(w)
+    v, g = H.dev(p["value"], dt), H.dev(p["grad_output"], dt)
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+    loc, attn = H.dev(p["sampling_locations"]), H.dev(p["attention_weights"])
+    ref, off, lg = H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]), H.dev(p["attention_logits"])
+    out = msda.msda_forward(v, sh, st, loc, attn).float().cpu().numpy()
+    H.assert_fwd(out, oracle.forward(p["value"], sh, st, p["sampling_locations"], p["attention_weights"]), dtype,
+                 f"G={G} forward")
+    fo = msda.msda_forward_fused(v, sh, st, ref, off, lg).float().cpu().numpy()
+    H.assert_fwd(fo, oracle.forward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
+                                          p["attention_logits"]), dtype, f"G={G} fused forward")
+    ref_b, ref_fb = _oracle_backward(p), _oracle_backward_fused(p)
+    for flags in (0, msda.MSDA_DETERMINISTIC):
+        got = [t.cpu().numpy() for t in msda.msda_backward(v, sh, st, loc, attn, g, flags=flags)]
+        _check_backward(w, got, ref_b)
+        got = [t.cpu().numpy() for t in msda.msda_backward_fused(v, sh, st, ref, off, lg, g, flags=flags)]
+        _check_backward_fused(w, got, ref_fb)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,D", [(1, 128), (1, 256), (3, 128)])
+def test_wide_heads(msda, dtype, M, D):
+    """head_dim 128 and 256 without groups: one query a warp, 64 record slots a
+    row; ragged Len_q and level sizes, both backward modes."""
+    w = workloads.custom(N=2, M=M, D=D, levels=RAGGED_LEVELS, K=3, Len_q=19, dtype=dtype, refs="uniform",
+                         ref_range=(-0.05, 1.05), offset_sigma=0.2, seed=2100 + D + M)
+    p = H.prepared(w)
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), dtype, f"D={D} output")
+    fr = oracle.forward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
+                              p["sampling_offsets"], p["attention_logits"])
+    H.assert_fwd(_run_fused(msda, w, p), fr, dtype, f"D={D} fused output")
+    ref_b, ref_fb = _oracle_backward(p), _oracle_backward_fused(p)
+    for flags in (0, msda.MSDA_DETERMINISTIC):
+        _check_backward(w, _run_backward(msda, w, p, flags), ref_b)
+        _check_backward_fused(w, _run_backward_fused(msda, w, p, flags), ref_fb)
+
+
+def test_group_count_must_divide_the_heads(msda):
+    w = workloads.custom(N=1, M=6, D=8, levels=[(4, 4)], K=2, Len_q=5, refs="none", seed=3)
+    p = H.prepared(w)
+    with pytest.raises(ValueError):
+        msda.msda_forward(H.dev(p["value"]), p["spatial_shapes"], p["level_start_index"],
+                          H.dev(p["sampling_locations"][:, :, :4]), H.dev(p["attention_weights"][:, :, :4]))
+    # 6 heads of 8 channels in 3 groups: 16 channels a set, supported
+    out = msda.msda_forward(H.dev(p["value"]), p["spatial_shapes"], p["level_start_index"],
+                            H.dev(p["sampling_locations"][:, :, :3]), H.dev(p["attention_weights"][:, :, :3]))
+    ref = oracle.forward(p["value"], p["spatial_shapes"], p["level_start_index"], p["sampling_locations"][:, :, :3],
+                         p["attention_weights"][:, :, :3])
+    H.assert_fwd(out.cpu().numpy(), ref, "f32", "6 heads in 3 groups")

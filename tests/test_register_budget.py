@@ -44,31 +44,32 @@ def ptxas_report(tmp_path_factory):
     return report
 
 
-def _det(name):
-    """DET template argument of a backward instantiation (the third, after T and D)."""
-    m = re.search(r"msda_backward_kernelI(?:f|13__nv_bfloat16)Li\d+ELb([01])E", name)
+def _budget(name):
+    """Registers a backward instantiation may use: 64 (four blocks) in
+    deterministic mode up to head width 64, else 85 (three blocks)."""
+    m = re.search(r"msda_backward_kernelI(?:f|13__nv_bfloat16)Li(\d+)ELb([01])E", name)
     assert m, name
-    return m.group(1) == "1"
+    return 64 if m.group(2) == "1" and int(m.group(1)) <= 64 else 85
 
 
 def test_backward_kernels_do_not_spill(ptxas_report):
-    """Deterministic mode runs four resident blocks (64 registers a thread),
-    fp32 mode three (85)."""
+    """Deterministic mode runs four resident blocks (64 registers a thread) up
+    to head width 64, everything else three (85)."""
     bwd = {k: v for k, v in ptxas_report.items() if "msda_backward_kernel" in k}
     assert len(bwd) >= 64, "every (dtype, D, det, merge, fused, opts) instantiation is reported"
-    bad = {k: v for k, v in bwd.items() if v[0] or v[1] or v[2] > (64 if _det(k) else 85)}
+    bad = {k: v for k, v in bwd.items() if v[0] or v[1] or v[2] > _budget(k)}
     assert not bad, f"spills or more registers than the block budget allows: {bad}"
 
 
 def test_fp32_forward_within_48_registers(ptxas_report):
     fwd = {k: v for k, v in ptxas_report.items() if "msda_forward_kernelIf" in k}
-    assert len(fwd) == 16
-    bad = {k: v for k, v in fwd.items() if v[0] or v[1] or v[2] > 48}
-    assert not bad, f"spills or more than 48 registers: {bad}"
+    assert len(fwd) == 24        # six head widths x (unfused, fused, fused with options)
+    bad = {k: v for k, v in fwd.items() if v[0] or v[1] or v[2] > (85 if "Li256E" in k else 48)}
+    assert not bad, f"spills or more than 48 registers (85 at head width 256): {bad}"
 
 
 def test_bf16_forward_spills_at_most_a_word(ptxas_report):
     fwd = {k: v for k, v in ptxas_report.items() if "msda_forward_kernel_bf16" in k}
-    assert len(fwd) == 16
+    assert len(fwd) == 24
     bad = {k: v for k, v in fwd.items() if v[0] > 4 or v[1] > 4}
     assert not bad, f"spills above 4 bytes: {bad}"
