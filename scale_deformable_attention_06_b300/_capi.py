@@ -6,6 +6,7 @@ MSDAError when the library returns a non-OK status.  No step of the method
 runs in Python; there is no CPU fallback.  If libmsda.so has not been built,
 importing the package raises ImportError.
 """
+import contextlib
 import contextvars
 import ctypes
 import functools
@@ -15,6 +16,9 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libmsda.so")
+# the same kernels with every access checked against its tensor's extent
+# (include/msda_debug.h); for tests, through using_library()
+DEBUG_LIBRARY = os.path.join(_HERE, "libmsda_debug.so")
 
 MSDA_OK = 0
 MSDA_F32 = 0
@@ -43,10 +47,10 @@ class msda_problem(ctypes.Structure):
                 ("n_groups", ctypes.c_int32)]
 
 
-def _load():
-    if not os.path.exists(LIBRARY):
-        raise ImportError(f"{LIBRARY} is missing: build it with `python scale_deformable_attention_06_b300/build.py` (or __graft_entry__.build())")
-    lib = ctypes.CDLL(LIBRARY)
+def _load(path=LIBRARY):
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python scale_deformable_attention_06_b300/build.py` (or __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
     vp, i64p, fp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p
     pp = ctypes.POINTER(msda_problem)
     lib.msda_forward.argtypes = [pp, vp, i64p, i64p, fp, fp, vp, vp]
@@ -68,10 +72,26 @@ def _load():
     lib.msda_last_error.argtypes = []
     lib.msda_last_error.restype = ctypes.c_char_p
     lib.msda_version.restype = ctypes.c_int
+    if hasattr(lib, "msda_debug_violations"):
+        lib.msda_debug_violations.argtypes = [ctypes.c_int]
+        lib.msda_debug_violations.restype = ctypes.c_ulonglong
     return lib
 
 
 _lib = _load()
+
+
+@contextlib.contextmanager
+def using_library(path):
+    """Route every call of this module to another build of the library (the
+    debug build DEBUG_LIBRARY) inside the with-block; yields that ctypes
+    library."""
+    global _lib
+    saved, _lib = _lib, _load(path)
+    try:
+        yield _lib
+    finally:
+        _lib = saved
 
 
 def lib():

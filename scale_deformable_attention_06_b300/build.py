@@ -1,5 +1,6 @@
 """Build libmsda.so (the CUDA kernels and the C ABI) in-tree, for sm_103a, and
-libmsda_probes.so beside it (line-rate measurement kernels, used by bench.py).
+beside it libmsda_debug.so (the same with every kernel access checked) and
+libmsda_probes.so (line-rate measurement kernels, used by bench.py).
 
     python scale_deformable_attention_06_b300/build.py [--force] [--verbose]
 
@@ -17,6 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmsda.so")
 PROBES_LIB = os.path.join(PKG, "libmsda_probes.so")
+DEBUG_LIB = os.path.join(PKG, "libmsda_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -61,8 +63,20 @@ def build_probes(force=False):
     return PROBES_LIB
 
 
+def build_debug(force=False):
+    """libmsda_debug.so: the same sources with -DMSDA_DEBUG (every kernel access
+    checked against its tensor's extent, bad ones counted and skipped;
+    include/msda_debug.h)."""
+    deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) \
+        + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
+    if force or not os.path.exists(DEBUG_LIB) or any(os.path.getmtime(p) > os.path.getmtime(DEBUG_LIB) for p in deps):
+        _compile(DEBUG_LIB, sources(), extra=("-DMSDA_DEBUG",))
+    return DEBUG_LIB
+
+
 def build(force=False, verbose=False, extra=()):
     build_probes(force)
+    build_debug(force)
     if not force and not _stale():
         return LIB
     _compile(LIB, sources(), verbose, extra)

@@ -163,6 +163,8 @@ msda3d_forward_kernel(const __grid_constant__ Args3 a) {
     const int rowc = row_ok ? row : dm.rows - 1;
     const int n = rowc / dm.qm, m = rowc % dm.M;
     const T *vbase = static_cast<const T *>(a.value) + ((size_t)n * dm.Len_in * dm.M + m) * D + ch * V;
+    [[maybe_unused]] const T *vten = static_cast<const T *>(a.value);          // debug build: extent checks
+    [[maybe_unused]] const long long vtotal = (long long)dm.N * dm.Len_in * dm.pix;
     const uint64_t pol = l2_keep_policy();
 
     float acc[V];
@@ -193,7 +195,7 @@ msda3d_forward_kernel(const __grid_constant__ Args3 a) {
             const float wt[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
             Vec<T> v[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) v[c] = load_value(vbase + o[c], pol);
+            for (int c = 0; c < 8; ++c) v[c] = load_value(MSDA_ADDR(vten, vbase + o[c], vtotal, V), pol);
 #pragma unroll
             for (int c = 0; c < 8; ++c) fma_row<T, V>(acc, wt[c], v[c]);
         }
@@ -228,8 +230,12 @@ msda3d_backward_kernel(const __grid_constant__ Args3 a) {
     const size_t vhead = ((size_t)n * dm.Len_in * dm.M + m) * D + ch * 4;
     const T *vbase = static_cast<const T *>(a.value) + vhead;
     const uint64_t pol = l2_keep_policy();
+    [[maybe_unused]] const T *vten = static_cast<const T *>(a.value);          // debug build: extent checks
+    [[maybe_unused]] const T *gten = static_cast<const T *>(a.grad_out);
+    [[maybe_unused]] const long long vtotal = (long long)dm.N * dm.Len_in * dm.pix;
+    [[maybe_unused]] const long long gtotal = (long long)dm.N * dm.Len_q * dm.pix;
 
-    float4 g = load4_stream<T>(static_cast<const T *>(a.grad_out) + (size_t)row * D + ch * 4);
+    float4 g = load4_stream<T>(MSDA_ADDR(gten, gten + (size_t)row * D + ch * 4, gtotal, 4));
     if (!row_ok) g = make_float4(0.f, 0.f, 0.f, 0.f);
     float scale = 1.f;
     if constexpr (DET) scale = ldexpf(1.f, fixed_shift(a.bound_bits[n], dm.qm));   // this batch element's scale
@@ -267,7 +273,7 @@ msda3d_backward_kernel(const __grid_constant__ Args3 a) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 in[c] = (oc[c] & 1) != 0;
-                const float4 v = load4_value(vbase + (oc[c] & ~1), pol);
+                const float4 v = load4_value(MSDA_ADDR(vten, vbase + (oc[c] & ~1), vtotal, 4), pol);
                 float2 pr = __fmul2_rn(make_float2(g.x, g.y), make_float2(v.x, v.y));
                 pr = __ffma2_rn(make_float2(g.z, g.w), make_float2(v.z, v.w), pr);
                 t[c] = in[c] ? pr.x + pr.y : 0.f;     // outside corners read as zero
@@ -302,9 +308,12 @@ msda3d_backward_kernel(const __grid_constant__ Args3 a) {
                     const float cw = A * w[c];
                     const size_t dst = vhead + (oc[c] & ~1);
                     if constexpr (DET) {
-                        red_fixed4<R>(a.fixed, dst, ch, make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w), scale);
+                        if (MSDA_IN(a.fixed, a.fixed + (dst - 3 * (size_t)ch), vtotal, 3 * R + 1))
+                            red_fixed4<R>(a.fixed, dst, ch, make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w),
+                                          scale);
                     } else {
-                        red_add_v4(a.grad_value + dst, make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w));
+                        if (MSDA_IN(a.grad_value, a.grad_value + dst, vtotal, 4))
+                            red_add_v4(a.grad_value + dst, make_float4(cw * g.x, cw * g.y, cw * g.z, cw * g.w));
                     }
                 }
             }
@@ -346,6 +355,10 @@ static cudaError_t fwd3_t(const Args3 &a, cudaStream_t stream) {
                                   stream>>>(a);
     return cudaGetLastError();
 }
+
+#ifdef MSDA_DEBUG
+MSDA_DEBUG_COUNTER(debug_count_3d)
+#endif
 
 cudaError_t launch_forward3d(const LaunchGeometry3 &g, int dtype, int D, const void *value, const float *loc,
                              const float *attn, void *out, cudaStream_t stream) {

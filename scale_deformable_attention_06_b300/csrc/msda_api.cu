@@ -7,6 +7,9 @@
 #include <cstring>
 
 #include "../../include/msda.h"
+#ifdef MSDA_DEBUG
+#include "../../include/msda_debug.h"
+#endif
 #include "msda_launch.h"
 
 namespace {
@@ -429,3 +432,11 @@ const char *msda_last_error(void) { return g_last_error; }
 int msda_version(void) { return 100; }
 
 }  // extern "C"
+
+#ifdef MSDA_DEBUG
+extern "C" unsigned long long msda_debug_violations(int reset) {
+    cudaDeviceSynchronize();
+    return msda::debug_count_forward(reset != 0) + msda::debug_count_backward(reset != 0) +
+           msda::debug_count_3d(reset != 0);
+}
+#endif

@@ -65,10 +65,13 @@ struct BwdArgs {
 // grad_value[dst .. dst + 4) += v, lane ch of R (fp32 reduction, or fixed point)
 template <bool DET, int R>
 __device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, int ch, float4 v, float scale) {
+    [[maybe_unused]] const long long total = (long long)a.d.N * a.d.Len_in * a.d.pix;   // debug build
     if constexpr (DET) {
-        red_fixed4<R>(a.fixed, dst, ch, v, scale);
+        // words dst - 3 ch + i R, i < 4: the block's first and last word in range
+        if (MSDA_IN(a.fixed, a.fixed + (dst - 3 * (size_t)ch), total, 3 * R + 1))
+            red_fixed4<R>(a.fixed, dst, ch, v, scale);
     } else {
-        red_add_v4(a.grad_value + dst, v);
+        if (MSDA_IN(a.grad_value, a.grad_value + dst, total, 4)) red_add_v4(a.grad_value + dst, v);
     }
 }
 
@@ -143,11 +146,15 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     const size_t vhead = ((size_t)n * dm.Len_in * dm.M + m) * D + ch * 4;   // (n, pixel 0, m, lane channels)
     const T *vbase = static_cast<const T *>(a.value) + vhead;
     const uint64_t pol = l2_keep_policy();
+    [[maybe_unused]] const T *vten = static_cast<const T *>(a.value);          // debug build: extent checks
+    [[maybe_unused]] const T *gten = static_cast<const T *>(a.grad_out);
+    [[maybe_unused]] const long long vtotal = (long long)dm.N * dm.Len_in * dm.pix;
+    [[maybe_unused]] const long long gtotal = (long long)dm.N * dm.Len_q * dm.pix;
 
     float4 gv[NV];                               // this lane's channels of grad_output
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        gv[k] = load4_stream<T>(static_cast<const T *>(a.grad_out) + (size_t)row * D + (k * R + ch) * 4);
+        gv[k] = load4_stream<T>(MSDA_ADDR(gten, gten + (size_t)row * D + (k * R + ch) * 4, gtotal, 4));
         if (!row_ok) gv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     const float4 &g = gv[0];
@@ -282,7 +289,8 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                     for (int k = 0; k < NV; ++k) {
                         float4 v[4];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) v[c] = load4_value(vbase + off[c] + k * 4 * R, pol);
+                        for (int c = 0; c < 4; ++c)
+                            v[c] = load4_value(MSDA_ADDR(vten, vbase + off[c] + k * 4 * R, vtotal, 4), pol);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             pr[c] = k == 0 ? __fmul2_rn(make_float2(gv[k].x, gv[k].y), make_float2(v[c].x, v[c].y))
@@ -362,8 +370,8 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                     for (int hh = 0; hh < HW; ++hh) {
                         const int qq = qb * HW + hh;
                         gq[hh] = qq < dm.Len_q
-                                     ? load4_value<T>(static_cast<const T *>(a.grad_out) +
-                                                          ((size_t)(n * dm.Len_q + qq) * dm.M + m) * D + ch * 4,
+                                     ? load4_value<T>(MSDA_ADDR(gten, gten + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * D +
+                                                                          ch * 4, gtotal, 4),
                                                       pol)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
@@ -510,6 +518,10 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
         }
     }
 }
+
+#ifdef MSDA_DEBUG
+MSDA_DEBUG_COUNTER(debug_count_backward)
+#endif
 
 // grad_reference_points[n][q][l] = sum over heads and points of the location
 // gradient = (W_l, H_l) * sum of the offset gradients (loc = ref + off / (W, H)).

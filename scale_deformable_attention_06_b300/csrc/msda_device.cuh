@@ -15,6 +15,50 @@
 
 namespace msda {
 
+// ---- the debug build (compiled with -DMSDA_DEBUG into libmsda_debug.so) ------
+// Every value gather, grad_output load and grad_value / fixed-point reduction
+// is checked against the extent of its tensor (and the 16-byte alignment of
+// vector accesses).  A bad access is counted in the translation unit's
+// counter and skipped: a load reads the tensor's first elements instead, a
+// reduction is dropped.  Nothing traps.  Release builds compile the checks
+// away (MSDA_ADDR is the pointer itself, MSDA_IN is true).
+#ifdef MSDA_DEBUG
+static __device__ unsigned long long g_debug_violations;
+
+// p (inside or outside [base, base + total)) if its `width` elements lie in
+// the tensor and a 16-byte access there is aligned, else base.
+template <typename T>
+__device__ __forceinline__ T *debug_addr(T *base, T *p, long long total, int width) {
+    const long long i = (long long)(p - base);
+    const bool ok = i >= 0 && i + width <= total && (width * sizeof(T) < 16 || ((i * (long long)sizeof(T)) & 15) == 0);
+    if (!ok) atomicAdd(&g_debug_violations, 1ull);
+    return ok ? p : base;
+}
+template <typename T>
+__device__ __forceinline__ bool debug_in(const T *base, const T *p, long long total, int width) {
+    const long long i = (long long)(p - base);
+    const bool ok = i >= 0 && i + width <= total;
+    if (!ok) atomicAdd(&g_debug_violations, 1ull);
+    return ok;
+}
+#define MSDA_ADDR(base, p, total, width) ::msda::debug_addr((base), (p), (long long)(total), (width))
+#define MSDA_IN(base, p, total, width) ::msda::debug_in((base), (p), (long long)(total), (width))
+// the host side of a translation unit's counter: read it, and zero it if asked
+#define MSDA_DEBUG_COUNTER(fn)                                                               \
+    unsigned long long fn(bool reset) {                                                      \
+        unsigned long long v = 0;                                                            \
+        cudaMemcpyFromSymbol(&v, g_debug_violations, sizeof(v));                             \
+        if (reset) {                                                                         \
+            const unsigned long long z = 0;                                                  \
+            cudaMemcpyToSymbol(g_debug_violations, &z, sizeof(z));                           \
+        }                                                                                    \
+        return v;                                                                            \
+    }
+#else
+#define MSDA_ADDR(base, p, total, width) (p)
+#define MSDA_IN(base, p, total, width) true
+#endif
+
 constexpr int kMaxLevels = 16;
 constexpr int kMaxSamples = 256;     // n_levels * n_points per (query, head)
 constexpr int kWarpsPerBlock = 8;

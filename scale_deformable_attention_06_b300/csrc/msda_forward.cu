@@ -82,6 +82,8 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     const int n = rowc / dm.qm;
     const int m = rowc % dm.M;
     const T *vbase = static_cast<const T *>(a.value) + ((size_t)n * dm.Len_in * dm.M + m) * D + ch * V;
+    [[maybe_unused]] const T *vten = static_cast<const T *>(a.value);          // debug build: extent checks
+    [[maybe_unused]] const long long vtotal = (long long)dm.N * dm.Len_in * dm.pix;
     const uint64_t pol = l2_keep_policy();
 
     float acc[NV][V];
@@ -213,10 +215,10 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
 #pragma unroll
             for (int k = 0; k < NV; ++k) {         // vector k: channels (k * R + ch) * V ..
                 const T *vb = vbase + k * R * V;
-                const Vec<T> v0 = load_value(vb + o.x, pol);
-                const Vec<T> v1 = load_value(vb + o.y, pol);
-                const Vec<T> v2 = load_value(vb + o.z, pol);
-                const Vec<T> v3 = load_value(vb + o.w, pol);
+                const Vec<T> v0 = load_value(MSDA_ADDR(vten, vb + o.x, vtotal, V), pol);
+                const Vec<T> v1 = load_value(MSDA_ADDR(vten, vb + o.y, vtotal, V), pol);
+                const Vec<T> v2 = load_value(MSDA_ADDR(vten, vb + o.z, vtotal, V), pol);
+                const Vec<T> v3 = load_value(MSDA_ADDR(vten, vb + o.w, vtotal, V), pol);
                 fma_row<T, V>(acc[k], w.x, v0);
                 fma_row<T, V>(acc[k], w.y, v1);
                 fma_row<T, V>(acc[k], w.z, v2);
@@ -303,6 +305,10 @@ static void fill_common(FwdArgs &fa, const LaunchGeometry &g) {
     fa.opts = g.d.per_level_softmax || g.lv.shift != 0.5f;
     for (int s = 0; s < kMaxSamples; ++s) fa.level_of[s] = g.level_of[s];
 }
+
+#ifdef MSDA_DEBUG
+MSDA_DEBUG_COUNTER(debug_count_forward)
+#endif
 
 cudaError_t launch_forward(const LaunchGeometry &g, int dtype, int D, const void *value, const float *loc,
                            const float *attn, void *out, cudaStream_t stream) {

@@ -69,4 +69,12 @@ cudaError_t launch_backward3d(const LaunchGeometry3 &g, int dtype, int D, const 
                               const float *attn, const void *grad_out, float *grad_value, float *grad_loc,
                               float *grad_attn, bool det, bool accumulate, void *workspace, cudaStream_t stream);
 
+#ifdef MSDA_DEBUG
+// debug build: each kernel translation unit's count of skipped bad accesses
+// (reset: zero it after reading)
+unsigned long long debug_count_forward(bool reset);
+unsigned long long debug_count_backward(bool reset);
+unsigned long long debug_count_3d(bool reset);
+#endif
+
 }  // namespace msda

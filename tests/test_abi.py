@@ -270,3 +270,13 @@ def test_probe_library_exports_its_header(msda):
     n = probes.msda_probe_accesses(22756352)
     assert 22756352 <= n < 22756352 * 1.02
     assert probes.msda_probe_accesses(0) == 0
+
+
+def test_debug_library_exports(msda):
+    """libmsda_debug.so exports what include/msda.h declares plus the one entry
+    point of include/msda_debug.h."""
+    from scale_deformable_attention_06_b300 import _capi
+    out = subprocess.run(["nm", "-D", "--defined-only", _capi.DEBUG_LIBRARY], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT\s+(msda_\w+)", out))
+    assert exported == set(declared_symbols()) | {"msda_debug_violations"}
