@@ -147,7 +147,8 @@ def _code_only(text):
 
 def kernel_source_hash(kernel=None):
     """Hash of the code of `kernel`'s sources (of every kernel source when None)."""
-    files = KERNEL_SOURCES[kernel] if kernel else sorted(os.listdir(CSRC))
+    files = KERNEL_SOURCES[kernel] if kernel else sorted(f for f in os.listdir(CSRC)
+                                                          if os.path.isfile(os.path.join(CSRC, f)))
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
