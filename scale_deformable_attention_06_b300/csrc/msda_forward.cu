@@ -8,7 +8,8 @@
 // and A = softmax over the L*K logits of the row (the tutorial module, §3.2).
 //
 // Work decomposition.  A "row" is one (n, q, m).  A warp owns HW = 32 / R
-// consecutive rows, R lanes per row, each lane holding 16 bytes of the row's
+// consecutive rows (head-major order for fp32 rows of a 128-byte line or
+// more, query-major otherwise), R lanes per row, each lane holding 16 bytes of the row's
 // D channels (4 fp32 or 8 bf16), NV such vectors where a row is wider than 32
 // of them (head_dim 256 fp32).  Per chunk of samples:
 //   phase 1: each lane computes the corner records (four element offsets and
@@ -57,7 +58,19 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     __shared__ float2 s_stat[kWarpsPerBlock][HW];   // fused: (row max, 1 / row sum)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = (blockIdx.x * kWarpsPerBlock + warp) * HW;
+    // fp32 rows of a 128-byte line or more are taken head-major: a warp (and a
+    // block) then holds consecutive queries of one head, whose samples share
+    // value rows in L1 (encoder forward 164 -> 158 us).  Narrower rows stay
+    // query-major, so that a warp's output rows are one contiguous span (64-byte
+    // bf16 rows taken head-major measured 19% slower), and so do bf16 rows.
+    constexpr bool HEAD_MAJOR = sizeof(T) == 4 && D * (int)sizeof(T) >= 128;
+    const int row0 = (blockIdx.x * kWarpsPerBlock + warp) * HW;      // in the order above
+    // the (n, q, m) row of position vr in that order
+    auto row_of = [&](int vr) {
+        if constexpr (!HEAD_MAJOR) return vr;
+        const int q = vr % a.d.Len_q, t = vr / a.d.Len_q;
+        return (t / a.d.M * a.d.Len_q + q) * a.d.M + t % a.d.M;
+    };
     const Dims &dm = a.d;
     if (row0 >= dm.rows) return;
     const int P = dm.P;
@@ -76,9 +89,9 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
 
     // phase-2 lane role
     const int h = lane / R, ch = lane % R;
-    const int row = row0 + h;
-    const bool row_ok = row < dm.rows;
-    const int rowc = row_ok ? row : dm.rows - 1;
+    const bool row_ok = row0 + h < dm.rows;
+    const int row = HEAD_MAJOR ? (row_ok ? row_of(row0 + h) : 0) : row0 + h;
+    const int rowc = row_ok ? row : row_of(dm.rows - 1);
     const int n = rowc / dm.qm;
     const int m = rowc % dm.M;
     const T *vbase = static_cast<const T *>(a.value) + ((size_t)n * dm.Len_in * dm.M + m) * D + ch * V;
@@ -103,7 +116,7 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
             for (int it = 0; it < 2; ++it) {
                 const int i = lane + 32 * it, hh = i % HW, j = i / HW;
                 valid[it] = j < P && row0 + hh < dm.rows;
-                lg[it] = valid[it] ? __ldg(a.logits + (size_t)(row0 + hh) * P + j) : -INFINITY;
+                lg[it] = valid[it] ? __ldg(a.logits + (size_t)row_of(row0 + hh) * P + j) : -INFINITY;
             }
             float mx = fmaxf(lg[0], lg[1]);
 #pragma unroll
@@ -130,7 +143,8 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         float e_slot[2] = {0.f, 0.f};
         if constexpr (FUSED) {
             if (online) {                                   // warp-uniform
-                const int r = row0 + lane % HW;
+                const int rv = row0 + lane % HW;
+                const int r = HEAD_MAJOR ? (rv < dm.rows ? row_of(rv) : dm.rows) : rv;   // >= dm.rows: past the end
                 float lg[2];
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
@@ -156,7 +170,8 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         // ---- phase 1: corner records, record i = j * HW + hh
         for (int i = lane; i < HW * J; i += 32) {
             const int hh = i % HW, j = i / HW;
-            const int r = row0 + hh, s = s0 + j;
+            const int rv = row0 + hh, s = s0 + j;
+            const int r = HEAD_MAJOR ? (rv < dm.rows ? row_of(rv) : dm.rows) : rv;       // >= dm.rows: past the end
             int4 off = make_int4(0, 0, 0, 0);
             float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
             if (r < dm.rows) {
