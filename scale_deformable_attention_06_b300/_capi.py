@@ -235,7 +235,8 @@ def problem(value, Len_q, n_levels, n_points, options=0, n_groups=0):
 def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
                  output=None, stream=None, options=0):
     """out[N, Len_q, M*D] from value [N,Len_in,M,D] (f32|bf16), sampling_locations
-    [N,Len_q,M,L,K,2] f32 and attention_weights [N,Len_q,M,L,K] f32."""
+    [N,Len_q,G,L,K,2] f32 and attention_weights [N,Len_q,G,L,K] f32 (G = M, or the
+    number of head groups)."""
     lv = _HostLevels(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
     if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != 2:
@@ -262,7 +263,8 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
 def msda_forward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
                        attention_logits, output=None, stream=None, options=0):
     """out[N, Len_q, M*D] from reference_points [N,Len_q,L,2], sampling_offsets
-    [N,Len_q,M,L,K,2] (pixels of each level) and attention_logits [N,Len_q,M,L*K]."""
+    [N,Len_q,G,L,K,2] (pixels of each level) and attention_logits [N,Len_q,G,L*K]
+    (G = M, or the number of head groups)."""
     lv = _HostLevels(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
     if sampling_offsets.dim() != 6 or sampling_offsets.shape[-1] != 2:
@@ -332,7 +334,7 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
                         grad_sampling_offsets=None, grad_attention_logits=None, flags=0, workspace=None,
                         stream=None, options=0):
     """Gradient of msda_forward_fused.  Returns (grad_value f32 [N,Len_in,M,D],
-    grad_reference_points [N,Len_q,L,2], grad_sampling_offsets [N,Len_q,M,L,K,2],
+    grad_reference_points [N,Len_q,L,2], grad_sampling_offsets [N,Len_q,G,L,K,2],
     grad_attention_logits shaped like attention_logits)."""
     lv = _HostLevels(spatial_shapes, level_start_index)
     N, S, M, D = value.shape
