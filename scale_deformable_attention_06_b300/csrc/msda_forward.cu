@@ -56,6 +56,7 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     __shared__ int4 s_off[kWarpsPerBlock][kRecordsPerWarp];
     __shared__ float4 s_w[kWarpsPerBlock][kRecordsPerWarp];
     __shared__ float2 s_stat[kWarpsPerBlock][HW];   // fused: (row max, 1 / row sum)
+    __shared__ int s_row[kWarpsPerBlock][32];        // each lane's record-phase row (below)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // fp32 rows of a 128-byte line or more are taken head-major: a warp (and a
@@ -68,12 +69,29 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     // the (n, q, m) row of position vr in that order
     auto row_of = [&](int vr) {
         if constexpr (!HEAD_MAJOR) return vr;
-        const int q = vr % a.d.Len_q, t = vr / a.d.Len_q;
+        int q = vr % a.d.Len_q;
+        const int t = vr / a.d.Len_q;
+        if (a.d.Len_q == a.d.Len_in) q = band_query(q, a.lv, a.d.L);   // queries are the value pixels
         return (t / a.d.M * a.d.Len_q + q) * a.d.M + t % a.d.M;
     };
     const Dims &dm = a.d;
     if (row0 >= dm.rows) return;
     const int P = dm.P;
+    // a lane's row in the record and softmax phases: that of position
+    // row0 + lane % HW (HW divides 32, so every slot of the lane falls on it),
+    // dm.rows or more past the end.  Head-major, it is looked up once; with
+    // several rows a warp it is kept in shared memory between chunks (in a
+    // register it made the fused kernels spill), with one row a warp it is
+    // also the phase-2 row and stays in a register.
+    constexpr bool SROW = HEAD_MAJOR && HW > 1;
+    int r_mine = row0 + lane % HW;
+    if constexpr (HEAD_MAJOR) r_mine = r_mine < dm.rows ? row_of(r_mine) : dm.rows;
+    if constexpr (SROW) s_row[warp][lane] = r_mine;
+    auto my_row = [&]() -> int {
+        if constexpr (SROW) return s_row[warp][lane];
+        if constexpr (HEAD_MAJOR) return r_mine;
+        return row0 + lane % HW;
+    };
 
     // fused, whole-row softmax.  A row that is one record chunk (compiled in
     // where a chunk holds 16 logits) gets its statistics in the record phase
@@ -90,8 +108,11 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     // phase-2 lane role
     const int h = lane / R, ch = lane % R;
     const bool row_ok = row0 + h < dm.rows;
-    const int row = HEAD_MAJOR ? (row_ok ? row_of(row0 + h) : 0) : row0 + h;
-    const int rowc = row_ok ? row : row_of(dm.rows - 1);
+    const int row_qm = row0 + h;                    // query-major: the phase-2 row
+    // lane h holds the row of position row0 + h (one row a warp: every lane)
+    const int rowc = !HEAD_MAJOR ? (row_ok ? row_qm : dm.rows - 1)
+                     : HW == 1   ? r_mine
+                                 : __shfl_sync(0xffffffffu, r_mine, row_ok ? h : 0);
     const int n = rowc / dm.qm;
     const int m = rowc % dm.M;
     const T *vbase = static_cast<const T *>(a.value) + ((size_t)n * dm.Len_in * dm.M + m) * D + ch * V;
@@ -114,9 +135,9 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
             bool valid[2];
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
-                const int i = lane + 32 * it, hh = i % HW, j = i / HW;
-                valid[it] = j < P && row0 + hh < dm.rows;
-                lg[it] = valid[it] ? __ldg(a.logits + (size_t)row_of(row0 + hh) * P + j) : -INFINITY;
+                const int i = lane + 32 * it, j = i / HW;       // row i % HW = lane % HW
+                valid[it] = j < P && my_row() < dm.rows;
+                lg[it] = valid[it] ? __ldg(a.logits + (size_t)my_row() * P + j) : -INFINITY;
             }
             float mx = fmaxf(lg[0], lg[1]);
 #pragma unroll
@@ -143,8 +164,7 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         float e_slot[2] = {0.f, 0.f};
         if constexpr (FUSED) {
             if (online) {                                   // warp-uniform
-                const int rv = row0 + lane % HW;
-                const int r = HEAD_MAJOR ? (rv < dm.rows ? row_of(rv) : dm.rows) : rv;   // >= dm.rows: past the end
+                const int r = my_row();                         // >= dm.rows: past the end
                 float lg[2];
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
@@ -169,9 +189,8 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         }
         // ---- phase 1: corner records, record i = j * HW + hh
         for (int i = lane; i < HW * J; i += 32) {
-            const int hh = i % HW, j = i / HW;
-            const int rv = row0 + hh, s = s0 + j;
-            const int r = HEAD_MAJOR ? (rv < dm.rows ? row_of(rv) : dm.rows) : rv;       // >= dm.rows: past the end
+            const int j = i / HW, s = s0 + j;                  // row i % HW = lane % HW
+            const int r = my_row();                             // >= dm.rows: past the end
             int4 off = make_int4(0, 0, 0, 0);
             float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
             if (r < dm.rows) {
@@ -252,6 +271,9 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         }
     }
     if (row_ok) {
+        // the row again (not held through the gathers): lane h's record-phase
+        // row, written before the chunk loop's warp barriers
+        const int row = SROW ? s_row[warp][h] : HEAD_MAJOR ? r_mine : row_qm;
 #pragma unroll
         for (int k = 0; k < NV; ++k)
             store_row<T, V>(static_cast<T *>(a.out) + (size_t)row * D + (k * R + ch) * V, acc[k]);

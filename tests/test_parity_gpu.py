@@ -673,6 +673,29 @@ def test_wide_heads(msda, dtype, M, D):
         _check_backward_fused(w, _run_backward_fused(msda, w, p, flags), ref_fb)
 
 
+@pytest.mark.parametrize("M,D,K", [(3, 32, 5), (2, 64, 3), (1, 128, 4), (1, 256, 2)])
+@pytest.mark.parametrize("opt", [0, 1], ids=["row_softmax", "per_level"])
+def test_pixel_queries_band_order(msda, M, D, K, opt):
+    """One query per value pixel (Len_q == Len_in, the encoder's shape): the
+    fp32 forward takes each head's queries in bands of four rows, walked
+    column by column.  Level heights that are no multiple of four (a short
+    last band), odd widths and one-row levels; every head width the forward
+    takes head-major, unfused and fused (K = 5 at D = 32: two record chunks a
+    row, the online softmax), with and without the per-level softmax."""
+    w = workloads.custom(N=2, M=M, D=D, levels=[(7, 9), (5, 3), (1, 5), (2, 1)], K=K, offset_sigma=0.1,
+                         seed=2300 + D + opt)
+    p = H.prepared(w)
+    assert w.Lq == w.Len_in == 85
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+    if opt == 0:
+        H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), "f32", f"D={D} pixel queries")
+    fo = msda.msda_forward_fused(H.dev(p["value"]), sh, st, H.dev(p["reference_points"]),
+                                 H.dev(p["sampling_offsets"]), H.dev(p["attention_logits"]), options=opt)
+    ref = oracle.forward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
+                               p["attention_logits"], options=opt)
+    H.assert_fwd(fo.float().cpu().numpy(), ref, "f32", f"D={D} pixel queries, fused, options {opt}")
+
+
 def test_group_count_must_divide_the_heads(msda):
     w = workloads.custom(N=1, M=6, D=8, levels=[(4, 4)], K=2, Len_q=5, refs="none", seed=3)
     p = H.prepared(w)
