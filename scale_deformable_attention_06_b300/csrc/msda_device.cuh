@@ -286,30 +286,6 @@ __device__ __forceinline__ Corners make_corners(float x0f, float fx, float y0f, 
     return c;
 }
 
-// ---- query order where the queries are the value pixels ---------------------
-// In encoder self-attention Len_q == Len_in and query i sits at value pixel i
-// of the flattened levels.  The head-major forward then takes the queries of
-// one head in band order: each level cut into bands of four rows (the last
-// band of a level may be shorter), each band walked column by column.  A
-// warp's four consecutive positions are then a column of four pixels and a
-// block's 32 an 8 x 4 patch, instead of a 32 x 1 strip, so the value rows a
-// block gathers overlap more in L1 (encoder forward 158 -> 154 us).  The order
-// only decides which queries run together: it maps [0, Len_in) one to one
-// onto itself, for any query layout.  The backward keeps raster order: there
-// the extra overlap makes concurrent grad_value reductions meet on the same
-// lines, and it measured slower (405 -> 412 us).
-__device__ __forceinline__ int band_query(int p, const LevelTable &lv, int L) {
-    int l = 0;
-    while (l + 1 < L && p >= lv.start[l + 1]) ++l;
-    const int W = lv.W[l], H = lv.H[l];
-    const int i = p - lv.start[l];
-    const int band = i / (4 * W);
-    const int rem = i - band * 4 * W;
-    const int bh = min(4, H - 4 * band);            // rows of this band
-    const int x = bh == 4 ? rem >> 2 : rem / bh;    // only a level's last band is shorter
-    return lv.start[l] + (4 * band + (rem - x * bh)) * W + x;
-}
-
 // ---- 16-byte corner records -------------------------------------------------
 // One sample's four corners in 16 bytes, written once per sample and read by
 // every lane of its row:
