@@ -63,11 +63,18 @@ __device__ __forceinline__ int band_query(int p, const LevelTable &lv, int L) {
     return lv.start[l] + (4 * band + (rem - x * bh)) * W + x;
 }
 
-// Resident blocks per SM the fp32 kernels are compiled for (at most 48
-// registers a thread): faster on the fp32 gathers than the compiler's own
-// choice.  The bf16 kernels keep the compiler's choice, which measured faster
-// for them.
-constexpr int kFwdMinBlocksF32 = 5;
+// Resident blocks per SM the fp32 kernels are compiled for: six (at most 40
+// registers a thread) up to head width 64, faster on the gathers than five
+// (encoder forward 152 -> 145 us, fused 167 -> 158 us) or seven (which
+// spills: 166 us); five (48 registers) at width 128, where the fused kernel
+// with option code would spill at 40; three at 256.  The unfused bf16 kernel
+// also runs six (decoder forward 24.6 -> 22.5 us, large unchanged); the fused
+// bf16 kernel keeps the compiler's choice, six made it spill (decoder fused
+// forward 24.6 -> 27.2 us).
+constexpr int kFwdMinBlocksF32 = 6;
+template <int D>
+constexpr int fwd_min_blocks_f32() { return D > 128 ? 3 : D == 128 ? 5 : kFwdMinBlocksF32; }
+constexpr int kFwdMinBlocksBf16Unfused = 6;
 
 // The kernel body.  OPTS: the problem sets option bits (fused calls); without
 // them the kernel carries none of the option code.
@@ -305,15 +312,21 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
 }
 
 template <typename T, int D, bool FUSED, bool OPTS>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, D > 128 ? 3 : kFwdMinBlocksF32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, fwd_min_blocks_f32<D>())
 msda_forward_kernel(const __grid_constant__ FwdArgs a) {       // fp32 value (two vectors a lane at D = 256: three blocks)
     forward_body<T, D, FUSED, OPTS>(a);
 }
 
 template <typename T, int D, bool FUSED, bool OPTS>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-msda_forward_kernel_bf16(const __grid_constant__ FwdArgs a) {  // bf16 value
+msda_forward_kernel_bf16(const __grid_constant__ FwdArgs a) {  // bf16 value, fused
     forward_body<T, D, FUSED, OPTS>(a);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kFwdMinBlocksBf16Unfused)
+msda_forward_kernel_bf16_unfused(const __grid_constant__ FwdArgs a) {  // bf16 value, unfused
+    forward_body<T, D, false, false>(a);
 }
 
 template <typename T, int D, bool FUSED>
@@ -327,11 +340,13 @@ static cudaError_t launch_fwd(const FwdArgs &args, cudaStream_t stream) {
             msda_forward_kernel<T, D, FUSED, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
         else
             msda_forward_kernel<T, D, FUSED, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
-    } else {
+    } else if constexpr (FUSED) {
         if (opts)
-            msda_forward_kernel_bf16<T, D, FUSED, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+            msda_forward_kernel_bf16<T, D, true, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
         else
-            msda_forward_kernel_bf16<T, D, FUSED, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+            msda_forward_kernel_bf16<T, D, true, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    } else {
+        msda_forward_kernel_bf16_unfused<T, D><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
     }
     return cudaGetLastError();
 }
