@@ -273,7 +273,11 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
                     for (int v = 0; v < V; ++v) acc[k][v] *= sc;
             }
         }
-#pragma unroll 2
+        // samples in flight per lane: eight in the unfused kernels from head
+        // width 32 (encoder forward 145 -> 143 us, large 395 -> 389 us; four
+        // measured the same as two, eight spills at width 16), two in the fused
+        // ones (more spills there)
+#pragma unroll(FUSED || D < 32 ? 2 : 8)
         for (int j = 0; j < J; ++j) {
             const int4 o = s_off[warp][j * HW + h];
             const float4 w = s_w[warp][j * HW + h];
