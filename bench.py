@@ -9,7 +9,8 @@ One step is msda_forward followed by msda_backward (atomic mode) on the
 Deformable DETR encoder workload (N=2, M=8, D=32, four levels 100x167, 50x84,
 25x42, 13x21, Len_q = Len_in = 22223, K=4, fp32), seeded synthetic inputs.
 L2 is flushed (a 256 MB write) before every step; per-step CUDA events on the
-launching stream exclude the flush.  For N > 1 (torchrun) every rank runs its
+launching stream exclude the flush and a ~1 ms GPU spin after it that lets the
+host enqueue the whole step before its start event runs.  For N > 1 (torchrun) every rank runs its
 own batch (weak scaling, no collective on the data path); the time is the
 maximum over ranks and the value counts the points of all ranks.
 
@@ -36,6 +37,12 @@ METRIC = "MSDeformAttn sampled-points/s fwd & fwd+bwd; achieved HBM GB/s vs B300
 UNIT = "sampled-points/s"
 WORKLOAD = "encoder_train"
 FLUSH_BYTES = 256 << 20
+# Before a timed call's start event the GPU spins this many cycles (about
+# 1 ms), so that Python has enqueued the whole call by the time the event
+# runs: the interval then holds the call's device time, not the GPU waiting
+# for the host's marshalling (which exposed up to ~150 us per call on a busy
+# host, on calls of ~25 us)
+HOLD_CYCLES = 2_000_000
 NOMINAL_HBM_GBS = 8000.0      # the roofline denominator the targets are stated against (8 TB/s)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic.json")
 CSRC = os.path.join(ROOT, "scale_deformable_attention_06_b300", "csrc")
@@ -292,6 +299,7 @@ def run_ours(args):
             flush.fill_(1.0)
             if pre is not None:
                 pre()
+            torch.cuda._sleep(HOLD_CYCLES)
             e0.record(stream)
             fn()
             e1.record(stream)
@@ -480,7 +488,8 @@ def run_ours(args):
         "config": dict(workload_config(args, w, world),
                        calls=("msda_forward_fused + msda_backward_fused" if args.step == "fused" else
                               "msda_forward + msda_backward") + " (atomic grad_value)",
-                       l2="flushed before every step (256 MB write); per-step events exclude the flush"),
+                       l2="flushed before every step (256 MB write); per-step events exclude the flush and a ~1 ms GPU "
+                          "spin after it (the host enqueues the step meanwhile)"),
         "fwd": {"ms": fwd_ms, "points_per_s": pts / (fwd_ms / 1e3), "gbs": ab["fwd"] / (fwd_ms / 1e3) / 1e9,
                 "frac_of_peak": ab["fwd"] / (fwd_ms / 1e3) / 1e9 / peak,
                 "frac_of_nominal_8tbs": ab["fwd"] / (fwd_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
@@ -658,6 +667,7 @@ def run_sweep(args):
             flush.fill_(1.0)
             if pre is not None:
                 pre()
+            torch.cuda._sleep(HOLD_CYCLES)
             e0.record(stream)
             fn()
             e1.record(stream)
