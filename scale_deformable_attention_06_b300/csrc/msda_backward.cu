@@ -37,6 +37,8 @@
 // |contribution| so that no sum can overflow, then converts to fp32.  The
 // merge table's fp32 coefficient sums are formed in a fixed order (program
 // order of the samples), so they too are the same from run to run.
+#include <type_traits>
+
 #include "msda_device.cuh"
 #include "msda_launch.h"
 
@@ -76,30 +78,40 @@ __device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, int ch, f
 }
 
 constexpr unsigned kEmptyKey = 0xffffffffu;
-constexpr int kMergeSlots = 128;       // per warp; a merge chunk has at most 64 entries
+// Merge-table slots per warp; a merge chunk has at most 64 entries.  fp32
+// mode merges only the coarse levels (a quarter or less of a chunk's entries
+// distinct): 64 slots, whose smaller footprint leaves the SM more L1 (encoder
+// backward 405 -> 392 us).  Deterministic mode merges every level, up to
+// three quarters distinct on the finest: 128 slots keep its probe chains
+// short (64 measured 1-2% slower there).
+template <bool DET>
+constexpr int merge_slots() { return DET ? 128 : 64; }
 constexpr int kMergeSamples = 4;       // samples per merge chunk (4 queries x 4 x 4 corners = 64 entries)
 
-template <int HW, int RC, bool MERGE>
+// Warp-private shared memory.  The fused calls' arrays have one element in
+// the unfused kernels (never read there), and the merge table exists only
+// where it is compiled in: less shared memory a block leaves the SM more L1.
+template <int HW, int RC, bool FUSED>
 struct BwdWarpSmem {
     int4 roff[HW][RC + 1];             // corner records: element offsets of the 4 corners (padded rows)
     float4 raux[HW][RC + 1];           //   fx, fy, A, inside-mask bits
     float4 res[HW][RC + 1];            // per sample: grad_attn, A*d/dpx, A*d/dpy
-    float2 stat[HW];                   // fused: softmax max and 1 / sum of each query
-    float gdot[HW][kMaxLevels];        // fused, per-level softmax: sum_k A_k grad_A_k
-    float dotp[64];                    // fused: per (query, sample) slot, sum of A * grad_A
+    float2 stat[FUSED ? HW : 1];       // fused: softmax max and 1 / sum of each query
+    float gdot[FUSED ? HW : 1][FUSED ? kMaxLevels : 1];   // fused, per-level softmax: sum_k A_k grad_A_k
+    float dotp[FUSED ? 64 : 1];        // fused: per (query, sample) slot, sum of A * grad_A
 };
 
-template <int HW, int RC>
-struct BwdWarpSmem<HW, RC, true> {
+template <int HW, int RC, bool FUSED, int SLOTS>
+struct BwdWarpSmemMerge {
     int4 roff[HW][RC + 1];
     float4 raux[HW][RC + 1];
     float4 res[HW][RC + 1];
-    float2 stat[HW];
-    float gdot[HW][kMaxLevels];
-    float dotp[64];
-    unsigned key[kMergeSlots];         // corner pixel of the slot, kEmptyKey if free
-    float4 alpha[kMergeSlots];         // per query of the warp: summed A * w_c (HW == 4)
-    unsigned short list[kMergeSlots];  // occupied slots in order of first use
+    float2 stat[FUSED ? HW : 1];
+    float gdot[FUSED ? HW : 1][FUSED ? kMaxLevels : 1];
+    float dotp[FUSED ? 64 : 1];
+    unsigned key[SLOTS];               // corner pixel of the slot, kEmptyKey if free
+    float4 alpha[SLOTS];               // per query of the warp: summed A * w_c (HW == 4)
+    unsigned short list[SLOTS];        // occupied slots in order of first use
     int count;
 };
 
@@ -126,7 +138,8 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
     static_assert(HW * RC == 64, "phase 1 and 3 give every lane two (query, sample) slots");
     static_assert(!MERGE || HW == 4, "the merge table holds four queries per slot");
-    using WS = BwdWarpSmem<HW, RC, MERGE>;
+    constexpr int kMergeSlots = merge_slots<DET>();
+    using WS = std::conditional_t<MERGE, BwdWarpSmemMerge<HW, RC, FUSED, kMergeSlots>, BwdWarpSmem<HW, RC, FUSED>>;
     __shared__ WS smem[kWarpsPerBlock];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -339,11 +352,13 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                                 // the corner's element offset is the key (< 2^31, never kEmptyKey)
                                 const unsigned key = (unsigned)(c == 0 ? off[0] : c == 1 ? off[1] : c == 2 ? off[2] : off[3]);
                                 const float coef = A * (c == 0 ? w[0] : c == 1 ? w[1] : c == 2 ? w[2] : w[3]);
-                                // at most 64 keys per chunk in 128 slots: a free or matching
-                                // slot is always found
+                                // at most 64 keys per chunk in 64 or 128 slots: a probe of
+                                // every slot finds a free or matching one
                                 // offsets are multiples of n_heads * head_dim: hash, do not mask
-                                static_assert(kMergeSlots == 128, "the hash below yields 7 bits");
-                                unsigned slot = (key * 2654435761u) >> 25;
+                                static_assert((kMergeSlots == 64 || kMergeSlots == 128) &&
+                                                  kMergeSamples * 4 * 4 <= kMergeSlots,
+                                              "the hash below yields log2(slots) bits; a chunk's entries fit");
+                                unsigned slot = (key * 2654435761u) >> (kMergeSlots == 64 ? 26 : 25);
                                 for (int probe = 0; probe < kMergeSlots; ++probe) {
                                     const unsigned old = atomicCAS(&sm.key[slot], kEmptyKey, key);
                                     if (old == kEmptyKey) sm.list[atomicAdd(&sm.count, 1)] = (unsigned short)slot;
