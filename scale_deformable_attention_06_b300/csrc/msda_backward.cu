@@ -89,25 +89,26 @@ constexpr int merge_slots() { return DET ? 128 : 64; }
 constexpr int kMergeSamples = 4;       // samples per merge chunk (4 queries x 4 x 4 corners = 64 entries)
 
 // Warp-private shared memory.  The fused calls' arrays have one element in
-// the unfused kernels (never read there), and the merge table exists only
-// where it is compiled in: less shared memory a block leaves the SM more L1.
-template <int HW, int RC, bool FUSED>
+// the unfused kernels, the per-level softmax's in kernels without option code
+// (never read there), and the merge table exists only where it is compiled
+// in: less shared memory a block leaves the SM more L1.
+template <int HW, int RC, bool FUSED, bool OPTS>
 struct BwdWarpSmem {
     int4 roff[HW][RC + 1];             // corner records: element offsets of the 4 corners (padded rows)
     float4 raux[HW][RC + 1];           //   fx, fy, A, inside-mask bits
     float4 res[HW][RC + 1];            // per sample: grad_attn, A*d/dpx, A*d/dpy
     float2 stat[FUSED ? HW : 1];       // fused: softmax max and 1 / sum of each query
-    float gdot[FUSED ? HW : 1][FUSED ? kMaxLevels : 1];   // fused, per-level softmax: sum_k A_k grad_A_k
+    float gdot[FUSED && OPTS ? HW : 1][FUSED && OPTS ? kMaxLevels : 1];   // per-level softmax: sum_k A_k grad_A_k
     float dotp[FUSED ? 64 : 1];        // fused: per (query, sample) slot, sum of A * grad_A
 };
 
-template <int HW, int RC, bool FUSED, int SLOTS>
+template <int HW, int RC, bool FUSED, bool OPTS, int SLOTS>
 struct BwdWarpSmemMerge {
     int4 roff[HW][RC + 1];
     float4 raux[HW][RC + 1];
     float4 res[HW][RC + 1];
     float2 stat[FUSED ? HW : 1];
-    float gdot[FUSED ? HW : 1][FUSED ? kMaxLevels : 1];
+    float gdot[FUSED && OPTS ? HW : 1][FUSED && OPTS ? kMaxLevels : 1];
     float dotp[FUSED ? 64 : 1];
     unsigned key[SLOTS];               // corner pixel of the slot, kEmptyKey if free
     float4 alpha[SLOTS];               // per query of the warp: summed A * w_c (HW == 4)
@@ -139,7 +140,8 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     static_assert(HW * RC == 64, "phase 1 and 3 give every lane two (query, sample) slots");
     static_assert(!MERGE || HW == 4, "the merge table holds four queries per slot");
     constexpr int kMergeSlots = merge_slots<DET>();
-    using WS = std::conditional_t<MERGE, BwdWarpSmemMerge<HW, RC, FUSED, kMergeSlots>, BwdWarpSmem<HW, RC, FUSED>>;
+    using WS = std::conditional_t<MERGE, BwdWarpSmemMerge<HW, RC, FUSED, OPTS, kMergeSlots>,
+                                  BwdWarpSmem<HW, RC, FUSED, OPTS>>;
     __shared__ WS smem[kWarpsPerBlock];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
