@@ -77,12 +77,15 @@ constexpr int fwd_min_blocks_f32() { return D > 128 ? 3 : D == 128 ? 5 : kFwdMin
 constexpr int kFwdMinBlocksBf16Unfused = 6;
 
 // The kernel body.  OPTS: the problem sets option bits (fused calls); without
-// them the kernel carries none of the option code.
-template <typename T, int D, bool FUSED, bool OPTS>
+// them the kernel carries none of the option code.  SEG: a fused call with
+// the whole-row softmax whose rows are one record chunk each (the host checks
+// L * K <= JC): the kernel carries only that softmax path, no online one.
+template <typename T, int D, bool FUSED, bool OPTS, bool SEG>
 __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     using Lay = Layout<T, D>;
     constexpr int V = Lay::V, R = Lay::R, HW = Lay::HW, NV = Lay::NV;
     constexpr int JC = kRecordsPerWarp / HW;     // samples of each row per chunk
+    static_assert(!SEG || (FUSED && JC >= 16), "one-chunk rows: fused calls where a chunk holds 16 logits");
 
     __shared__ int4 s_off[kWarpsPerBlock][kRecordsPerWarp];
     __shared__ float4 s_w[kWarpsPerBlock][kRecordsPerWarp];
@@ -124,16 +127,17 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         return row0 + lane % HW;
     };
 
-    // fused, whole-row softmax.  A row that is one record chunk (compiled in
-    // where a chunk holds 16 logits) gets its statistics in the record phase
-    // and normalised weights.  A row of several chunks is summed online: each
+    // fused, whole-row softmax.  A row that is one record chunk (the SEG
+    // kernels) gets its statistics in the record phase and normalised
+    // weights.  A row of several chunks (the other fused kernels) is summed
+    // online: each
     // chunk's record phase updates the row's running max and sum and keeps the
     // weights relative to that max, the gather phase first rescales the
     // accumulator by exp(old max - new max), and the output is divided by the
     // sum at the end, so no pass over the logits precedes the gathers.
     const bool row_softmax = FUSED && !(OPTS && a.d.per_level_softmax);
-    const bool seg_stats = (JC >= 16) && row_softmax && P <= JC;
-    const bool online = row_softmax && !seg_stats;
+    constexpr bool seg_stats = SEG;
+    const bool online = !SEG && row_softmax;
     float run_max = -INFINITY, run_sum = 0.f;      // online: of row lane % HW (phase-1 role)
 
     // phase-2 lane role
@@ -276,7 +280,7 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
         // samples in flight per lane: eight in the unfused kernels from head
         // width 32 (encoder forward 145 -> 143 us, large 395 -> 389 us; four
         // measured the same as two, eight spills at width 16), two in the fused
-        // ones (more spills there)
+        // ones (four or eight spill there, also in the one-chunk kernels)
 #pragma unroll(FUSED || D < 32 ? 2 : 8)
         for (int j = 0; j < J; ++j) {
             const int4 o = s_off[warp][j * HW + h];
@@ -315,42 +319,57 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     }
 }
 
-template <typename T, int D, bool FUSED, bool OPTS>
+template <typename T, int D, bool FUSED, bool OPTS, bool SEG>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, fwd_min_blocks_f32<D>())
 msda_forward_kernel(const __grid_constant__ FwdArgs a) {       // fp32 value (two vectors a lane at D = 256: three blocks)
-    forward_body<T, D, FUSED, OPTS>(a);
+    forward_body<T, D, FUSED, OPTS, SEG>(a);
 }
 
-template <typename T, int D, bool FUSED, bool OPTS>
+template <typename T, int D, bool FUSED, bool OPTS, bool SEG>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 msda_forward_kernel_bf16(const __grid_constant__ FwdArgs a) {  // bf16 value, fused
-    forward_body<T, D, FUSED, OPTS>(a);
+    forward_body<T, D, FUSED, OPTS, SEG>(a);
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kFwdMinBlocksBf16Unfused)
 msda_forward_kernel_bf16_unfused(const __grid_constant__ FwdArgs a) {  // bf16 value, unfused
-    forward_body<T, D, false, false>(a);
+    forward_body<T, D, false, false, false>(a);
+}
+
+template <typename T, int D, bool OPTS, bool SEG>
+static void launch_fwd_fused(const FwdArgs &args, unsigned blocks, cudaStream_t stream) {
+    if constexpr (sizeof(T) == 4)
+        msda_forward_kernel<T, D, true, OPTS, SEG><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    else
+        msda_forward_kernel_bf16<T, D, true, OPTS, SEG><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
 }
 
 template <typename T, int D, bool FUSED>
 static cudaError_t launch_fwd(const FwdArgs &args, cudaStream_t stream) {
     constexpr int HW = Layout<T, D>::HW;
+    constexpr int JC = kRecordsPerWarp / HW;
     const long long warps = ((long long)args.d.rows + HW - 1) / HW;
-    const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const bool opts = FUSED && args.opts;
-    if constexpr (sizeof(T) == 4) {
-        if (opts)
-            msda_forward_kernel<T, D, FUSED, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+    const unsigned blocks = (unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    if constexpr (!FUSED) {
+        if constexpr (sizeof(T) == 4)
+            msda_forward_kernel<T, D, false, false, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
         else
-            msda_forward_kernel<T, D, FUSED, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
-    } else if constexpr (FUSED) {
-        if (opts)
-            msda_forward_kernel_bf16<T, D, true, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
-        else
-            msda_forward_kernel_bf16<T, D, true, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+            msda_forward_kernel_bf16_unfused<T, D><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
     } else {
-        msda_forward_kernel_bf16_unfused<T, D><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+        const bool opts = args.opts != 0;
+        // rows of one record chunk under the whole-row softmax: the one-chunk kernels
+        bool seg = false;
+        if constexpr (JC >= 16) seg = !(opts && args.d.per_level_softmax) && args.d.P <= JC;
+        if constexpr (JC >= 16) {
+            if (seg) {
+                if (opts) launch_fwd_fused<T, D, true, true>(args, blocks, stream);
+                else launch_fwd_fused<T, D, false, true>(args, blocks, stream);
+                return cudaGetLastError();
+            }
+        }
+        if (opts) launch_fwd_fused<T, D, true, false>(args, blocks, stream);
+        else launch_fwd_fused<T, D, false, false>(args, blocks, stream);
     }
     return cudaGetLastError();
 }

@@ -674,14 +674,16 @@ def test_wide_heads(msda, dtype, M, D):
 
 
 @pytest.mark.parametrize("M,D,K", [(3, 32, 5), (2, 64, 3), (1, 128, 4), (1, 256, 2)])
-@pytest.mark.parametrize("opt", [0, 1], ids=["row_softmax", "per_level"])
+@pytest.mark.parametrize("opt", [0, 1, 2], ids=["row_softmax", "per_level", "align"])
 def test_pixel_queries_band_order(msda, M, D, K, opt):
     """One query per value pixel (Len_q == Len_in, the encoder's shape): the
     fp32 forward takes each head's queries in bands of four rows, walked
     column by column.  Level heights that are no multiple of four (a short
     last band), odd widths and one-row levels; every head width the forward
-    takes head-major, unfused and fused (K = 5 at D = 32: two record chunks a
-    row, the online softmax), with and without the per-level softmax."""
+    takes head-major, unfused and fused: K = 5 at D = 32 is two record chunks
+    a row (the online softmax), the other widths one (the one-chunk kernels);
+    the per-level softmax, and align_corners (option code in the one-chunk
+    kernels)."""
     w = workloads.custom(N=2, M=M, D=D, levels=[(7, 9), (5, 3), (1, 5), (2, 1)], K=K, offset_sigma=0.1,
                          seed=2300 + D + opt)
     p = H.prepared(w)
