@@ -77,6 +77,12 @@ __device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, int ch, f
     }
 }
 
+// Warps a backward block: four.  Smaller blocks balance the SMs better
+// (finer blocks to place) and keep fewer concurrent reductions on shared
+// lines: encoder backward 392 -> 383 us, large 1.60 -> 1.55 ms, decoder
+// 57 -> 51 us, deterministic mode 4-5% faster, against eight.
+constexpr int kBwdWarpsPerBlock = 4;
+
 constexpr unsigned kEmptyKey = 0xffffffffu;
 // Merge-table slots per warp; a merge chunk has at most 64 entries.  fp32
 // mode merges only the coarse levels (a quarter or less of a chunk's entries
@@ -127,13 +133,12 @@ struct BwdLanes {
 };
 
 // OPTS: the problem sets option bits (fused calls); without them the kernel
-// carries none of the option code.  Resident blocks per SM: four in
-// deterministic mode; three in fp32 mode, which leaves the L1 cache more of
-// the SM's memory beside the blocks' shared memory (measured faster there,
-// slower in deterministic mode); three for head widths above 64 (two vectors
-// a lane need the registers).
+// carries none of the option code.  Launch bounds: eight blocks of four warps
+// per SM in deterministic mode up to head width 64 (64 registers), six
+// otherwise (85; fp32 mode uses about 62, so eight fit there too, and head
+// widths above 64 need the registers for two vectors a lane).
 template <typename T, int D, bool DET, bool MERGE, bool FUSED, bool OPTS>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, (DET && D <= 64) ? 4 : 3)
+__global__ void __launch_bounds__(kBwdWarpsPerBlock * 32, (DET && D <= 64) ? 8 : 6)
 msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int R = BwdLanes<D>::R, HW = BwdLanes<D>::HW, NV = BwdLanes<D>::NV;
     constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
@@ -142,14 +147,14 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int kMergeSlots = merge_slots<DET>();
     using WS = std::conditional_t<MERGE, BwdWarpSmemMerge<HW, RC, FUSED, OPTS, kMergeSlots>,
                                   BwdWarpSmem<HW, RC, FUSED, OPTS>>;
-    __shared__ WS smem[kWarpsPerBlock];
+    __shared__ WS smem[kBwdWarpsPerBlock];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WS &sm = smem[warp];
     const Dims &dm = a.d;
     // query blocks fastest: the warps of a block (and blocks launched together)
     // take consecutive queries of one head, whose samples share value rows
-    const int task = blockIdx.x * kWarpsPerBlock + warp;
+    const int task = blockIdx.x * kBwdWarpsPerBlock + warp;
     if (task >= dm.N * a.qblocks * dm.M) return;       // warp-uniform
     const int qb = task % a.qblocks, t2 = task / a.qblocks;
     const int m = t2 % dm.M, n = t2 / dm.M;
@@ -746,7 +751,7 @@ struct BwdIO {
 template <typename T, int D, bool FUSED, bool OPTS>
 static void launch_bwd_kernel(const BwdArgs &a, bool det, unsigned blocks, cudaStream_t stream) {
     constexpr int HW = BwdLanes<D>::HW;
-    constexpr int B = kWarpsPerBlock * 32;
+    constexpr int B = kBwdWarpsPerBlock * 32;
     const bool merge = a.merge_mask != 0;
     if constexpr (HW == 4) {
         if (det && merge) msda_backward_kernel<T, D, true, true, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
@@ -793,7 +798,7 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
     a.bound_bits = bound;
     if (g.d.rows > 0) {
         const long long tasks = (long long)g.d.N * a.qblocks * g.d.M;
-        const unsigned blocks = (unsigned)((tasks + kWarpsPerBlock - 1) / kWarpsPerBlock);
+        const unsigned blocks = (unsigned)((tasks + kBwdWarpsPerBlock - 1) / kBwdWarpsPerBlock);
         if (FUSED && (g.d.per_level_softmax || g.lv.shift != 0.5f))
             launch_bwd_kernel<T, D, FUSED, true>(a, det, blocks, stream);
         else

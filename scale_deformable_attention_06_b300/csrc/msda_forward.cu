@@ -72,9 +72,14 @@ __device__ __forceinline__ int band_query(int p, const LevelTable &lv, int L) {
 // bf16 kernel keeps the compiler's choice, six made it spill (decoder fused
 // forward 24.6 -> 27.2 us).
 constexpr int kFwdMinBlocksF32 = 6;
+// Warps a forward block: eight for fp32 values, whose band-ordered blocks
+// then cover an 8 x 4 patch (four warps measured slower: encoder 143 ->
+// 150 us); four for bf16 (large forward 391 -> 387 us, fused 440 -> 432 us).
+template <typename T>
+constexpr int fwd_warps() { return sizeof(T) == 4 ? kWarpsPerBlock : 4; }
 template <int D>
 constexpr int fwd_min_blocks_f32() { return D > 128 ? 3 : D == 128 ? 5 : kFwdMinBlocksF32; }
-constexpr int kFwdMinBlocksBf16Unfused = 6;
+constexpr int kFwdMinBlocksBf16Unfused = 12;     // of four warps: 40 registers
 
 // The kernel body.  OPTS: the problem sets option bits (fused calls); without
 // them the kernel carries none of the option code.  SEG: a fused call with
@@ -87,10 +92,11 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     constexpr int JC = kRecordsPerWarp / HW;     // samples of each row per chunk
     static_assert(!SEG || (FUSED && JC >= 16), "one-chunk rows: fused calls where a chunk holds 16 logits");
 
-    __shared__ int4 s_off[kWarpsPerBlock][kRecordsPerWarp];
-    __shared__ float4 s_w[kWarpsPerBlock][kRecordsPerWarp];
-    __shared__ float2 s_stat[kWarpsPerBlock][HW];   // fused: (row max, 1 / row sum)
-    __shared__ int s_row[kWarpsPerBlock][32];        // each lane's record-phase row (below)
+    constexpr int WB = fwd_warps<T>();           // warps a block
+    __shared__ int4 s_off[WB][kRecordsPerWarp];
+    __shared__ float4 s_w[WB][kRecordsPerWarp];
+    __shared__ float2 s_stat[WB][HW];               // fused: (row max, 1 / row sum)
+    __shared__ int s_row[WB][32];                    // each lane's record-phase row (below)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // fp32 rows of a 128-byte line or more are taken head-major: a warp (and a
@@ -99,7 +105,7 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
     // query-major, so that a warp's output rows are one contiguous span (64-byte
     // bf16 rows taken head-major measured 19% slower), and so do bf16 rows.
     constexpr bool HEAD_MAJOR = sizeof(T) == 4 && D * (int)sizeof(T) >= 128;
-    const int row0 = (blockIdx.x * kWarpsPerBlock + warp) * HW;      // in the order above
+    const int row0 = (blockIdx.x * WB + warp) * HW;                  // in the order above
     // the (n, q, m) row of position vr in that order
     auto row_of = [&](int vr) {
         if constexpr (!HEAD_MAJOR) return vr;
@@ -320,19 +326,19 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
 }
 
 template <typename T, int D, bool FUSED, bool OPTS, bool SEG>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, fwd_min_blocks_f32<D>())
+__global__ void __launch_bounds__(fwd_warps<T>() * 32, fwd_min_blocks_f32<D>())
 msda_forward_kernel(const __grid_constant__ FwdArgs a) {       // fp32 value (two vectors a lane at D = 256: three blocks)
     forward_body<T, D, FUSED, OPTS, SEG>(a);
 }
 
 template <typename T, int D, bool FUSED, bool OPTS, bool SEG>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(fwd_warps<T>() * 32)
 msda_forward_kernel_bf16(const __grid_constant__ FwdArgs a) {  // bf16 value, fused
     forward_body<T, D, FUSED, OPTS, SEG>(a);
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, kFwdMinBlocksBf16Unfused)
+__global__ void __launch_bounds__(fwd_warps<T>() * 32, kFwdMinBlocksBf16Unfused)
 msda_forward_kernel_bf16_unfused(const __grid_constant__ FwdArgs a) {  // bf16 value, unfused
     forward_body<T, D, false, false, false>(a);
 }
@@ -340,9 +346,9 @@ msda_forward_kernel_bf16_unfused(const __grid_constant__ FwdArgs a) {  // bf16 v
 template <typename T, int D, bool OPTS, bool SEG>
 static void launch_fwd_fused(const FwdArgs &args, unsigned blocks, cudaStream_t stream) {
     if constexpr (sizeof(T) == 4)
-        msda_forward_kernel<T, D, true, OPTS, SEG><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+        msda_forward_kernel<T, D, true, OPTS, SEG><<<blocks, fwd_warps<T>() * 32, 0, stream>>>(args);
     else
-        msda_forward_kernel_bf16<T, D, true, OPTS, SEG><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+        msda_forward_kernel_bf16<T, D, true, OPTS, SEG><<<blocks, fwd_warps<T>() * 32, 0, stream>>>(args);
 }
 
 template <typename T, int D, bool FUSED>
@@ -350,12 +356,13 @@ static cudaError_t launch_fwd(const FwdArgs &args, cudaStream_t stream) {
     constexpr int HW = Layout<T, D>::HW;
     constexpr int JC = kRecordsPerWarp / HW;
     const long long warps = ((long long)args.d.rows + HW - 1) / HW;
-    const unsigned blocks = (unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    constexpr int WB = fwd_warps<T>();
+    const unsigned blocks = (unsigned)((warps + WB - 1) / WB);
     if constexpr (!FUSED) {
         if constexpr (sizeof(T) == 4)
-            msda_forward_kernel<T, D, false, false, false><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+            msda_forward_kernel<T, D, false, false, false><<<blocks, WB * 32, 0, stream>>>(args);
         else
-            msda_forward_kernel_bf16_unfused<T, D><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(args);
+            msda_forward_kernel_bf16_unfused<T, D><<<blocks, WB * 32, 0, stream>>>(args);
     } else {
         const bool opts = args.opts != 0;
         // rows of one record chunk under the whole-row softmax: the one-chunk kernels
