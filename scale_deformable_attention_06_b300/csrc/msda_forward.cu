@@ -283,11 +283,13 @@ __device__ __forceinline__ void forward_body(const FwdArgs &a) {
                     for (int v = 0; v < V; ++v) acc[k][v] *= sc;
             }
         }
-        // samples in flight per lane: eight in the unfused kernels from head
-        // width 32 (encoder forward 145 -> 143 us, large 395 -> 389 us; four
-        // measured the same as two, eight spills at width 16), two in the fused
-        // ones (four or eight spill there, also in the one-chunk kernels)
-#pragma unroll(FUSED || D < 32 ? 2 : 8)
+        // samples in flight per lane: eight from head width 32 in the unfused
+        // kernels (encoder forward 145 -> 143 us, large 395 -> 389 us; four
+        // measured the same as two, eight spills at width 16) and in the fused
+        // bf16 ones up to width 128 (no register cap there: large fused forward
+        // 432 -> 414 us), two in the fused fp32 ones and at width 256 (four or
+        // eight spill there)
+#pragma unroll((FUSED && (sizeof(T) == 4 || D > 128)) || D < 32 ? 2 : 8)
         for (int j = 0; j < J; ++j) {
             const int4 o = s_off[warp][j * HW + h];
             const float4 w = s_w[warp][j * HW + h];
