@@ -48,9 +48,12 @@ struct FwdArgs {
 // block's 32 an 8 x 4 patch, instead of a 32 x 1 strip, so the value rows a
 // block gathers overlap more in L1 (encoder forward 158 -> 152 us).  The order
 // only decides which queries run together: it maps [0, Len_in) one to one
-// onto itself, for any query layout.  The backward keeps raster order: there
-// the extra overlap makes concurrent grad_value reductions meet on the same
-// lines, and it measured slower (405 -> 412 us).
+// onto itself, for any query layout.  It relies on the levels tiling
+// [0, Len_in) exactly (start[l] the running sum of H * W, the sum Len_in,
+// every side at least 1), which the host checks before any launch.  The
+// backward keeps raster order: there the extra overlap makes concurrent
+// grad_value reductions meet on the same lines, and it measured slower
+// (405 -> 412 us; 391 -> 399 us with its lean shared memory).
 __device__ __forceinline__ int band_query(int p, const LevelTable &lv, int L) {
     int l = 0;
     while (l + 1 < L && p >= lv.start[l + 1]) ++l;
