@@ -106,6 +106,26 @@ def workload_config(args, w, world):
             "parallelism": f"dp{world} (independent batches per rank)"}
 
 
+def location_inputs(raw, sh):
+    """(sampling_locations float32, reference_points, sampling_offsets) of a
+    draw, as torch CPU tensors (input preparation, outside every timed region).
+    Drawn references and offsets give the locations ref + off / (W, H) in
+    float64; locations drawn directly (the tiny workload) give a reference at
+    each row's first sample and pixel offsets to the others."""
+    import torch
+    if "sampling_locations" in raw:
+        loc_h = torch.from_numpy(raw["sampling_locations"]).contiguous()
+        ref_h = loc_h[:, :, 0, :, 0, :].clone().contiguous()
+        whf = sh[:, [1, 0]].float()
+        off_h = ((loc_h - ref_h[:, :, None, :, None, :]) * whf[None, None, None, :, None, :]).contiguous()
+        return loc_h, ref_h, off_h
+    ref_h = torch.from_numpy(raw["reference_points"])
+    off_h = torch.from_numpy(raw["sampling_offsets"])
+    wh = sh[:, [1, 0]].to(torch.float64)
+    loc_h = (ref_h.double()[:, :, None, :, None, :] + off_h.double() / wh[None, None, None, :, None, :]).float()
+    return loc_h.contiguous(), ref_h, off_h
+
+
 def touched_value_bytes(w, loc):
     """Byte accounting for workloads whose queries are sparse: the bytes of
     the distinct 32-byte sectors of value that the in-map corners of all
@@ -243,10 +263,7 @@ def run_ours(args):
     # input preparation (outside every timed region): the unfused inputs are
     # the location step and the softmax of the raw draws, in float64 on the host
     sh = torch.from_numpy(raw["spatial_shapes"])
-    wh = sh[:, [1, 0]].to(torch.float64)
-    ref = torch.from_numpy(raw["reference_points"]).double()
-    off = torch.from_numpy(raw["sampling_offsets"]).double()
-    loc_h = (ref[:, :, None, :, None, :] + off / wh[None, None, None, :, None, :]).float().contiguous()
+    loc_h, ref_h, off_h = location_inputs(raw, sh)
     attn_h = torch.softmax(torch.from_numpy(raw["attention_logits"]).double(), -1).float() \
         .reshape(loc_h.shape[:-1]).contiguous()
     vdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -255,8 +272,7 @@ def run_ours(args):
     starts = raw["level_start_index"]
 
     value, loc, attn, gout = (t.to(dev) for t in (value_h, loc_h, attn_h, gout_h))
-    ref_d = torch.from_numpy(raw["reference_points"]).to(dev)
-    off_d = torch.from_numpy(raw["sampling_offsets"]).to(dev)
+    ref_d, off_d = ref_h.contiguous().to(dev), off_h.contiguous().to(dev)
     logit_d = torch.from_numpy(raw["attention_logits"]).to(dev)
     out = torch.empty((w.N, w.Lq, w.M * w.D), dtype=vdt, device=dev)
     gv = torch.empty(value.shape, dtype=torch.float32, device=dev)
@@ -292,11 +308,13 @@ def run_ours(args):
             fwd()
             bwd()
 
-    def timed(fn, iters, pre=None):
-        """Sum of per-call device times (ms) with an L2 flush before each call."""
+    def timed(fn, iters, pre=None, warm=False):
+        """Per-call device times (ms) with an L2 flush before each call, unless
+        warm (then the call's inputs are left in L2 by the call before)."""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
         for e0, e1 in evs:
-            flush.fill_(1.0)
+            if not warm:
+                flush.fill_(1.0)
             if pre is not None:
                 pre()
             torch.cuda._sleep(HOLD_CYCLES)
@@ -342,6 +360,9 @@ def run_ours(args):
     fwd_ms = statistics.mean(timed(fwd, reps))
     fused_ms = statistics.mean(timed(fused, reps))
     bwd_ms = statistics.mean(timed(lambda: bwd(msda.MSDA_ACCUMULATE_GRAD_VALUE), reps, pre=lambda: gv.zero_()))
+    fwd_warm_ms = statistics.mean(timed(fwd, reps, warm=True))
+    bwd_warm_ms = statistics.mean(timed(lambda: bwd(msda.MSDA_ACCUMULATE_GRAD_VALUE), reps, pre=lambda: gv.zero_(),
+                                        warm=True))
     det_ms = statistics.mean(timed(lambda: bwd(msda.MSDA_DETERMINISTIC), max(5, reps // 4)))
     fused_bwd_ms = statistics.mean(timed(lambda: fused_bwd(msda.MSDA_ACCUMULATE_GRAD_VALUE), reps,
                                          pre=lambda: gv.zero_()))
@@ -493,12 +514,12 @@ def run_ours(args):
         "fwd": {"ms": fwd_ms, "points_per_s": pts / (fwd_ms / 1e3), "gbs": ab["fwd"] / (fwd_ms / 1e3) / 1e9,
                 "frac_of_peak": ab["fwd"] / (fwd_ms / 1e3) / 1e9 / peak,
                 "frac_of_nominal_8tbs": ab["fwd"] / (fwd_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-                "algorithmic_bytes": ab["fwd"]},
+                "algorithmic_bytes": ab["fwd"], "warm_l2_ms": fwd_warm_ms},
         "bwd": {"ms": bwd_ms, "points_per_s": pts / (bwd_ms / 1e3), "gbs": ab["bwd"] / (bwd_ms / 1e3) / 1e9,
                 "frac_of_peak": ab["bwd"] / (bwd_ms / 1e3) / 1e9 / peak,
                 "frac_of_nominal_8tbs": ab["bwd"] / (bwd_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                 "algorithmic_bytes": ab["bwd"],
-                "deterministic_ms": det_ms},
+                "deterministic_ms": det_ms, "warm_l2_ms": bwd_warm_ms},
         "fused_fwd": {"ms": fused_ms, "points_per_s": pts / (fused_ms / 1e3),
                       "gbs": ab["fused_fwd"] / (fused_ms / 1e3) / 1e9},
         "fused_bwd": {"ms": fused_bwd_ms, "points_per_s": pts / (fused_bwd_ms / 1e3),
@@ -659,12 +680,15 @@ def run_sweep(args):
     stream = torch.cuda.current_stream(dev)
     peak, _ = measured_peak()
 
-    def timed(fn, iters, pre=None):
+    def timed(fn, iters, pre=None, warm=False):
+        """Median device time (ms); L2 flushed before each call unless warm
+        (then the call's inputs are left in L2 by the call before)."""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
         for _ in range(3):
             fn()
         for e0, e1 in evs:
-            flush.fill_(1.0)
+            if not warm:
+                flush.fill_(1.0)
             if pre is not None:
                 pre()
             torch.cuda._sleep(HOLD_CYCLES)
@@ -688,17 +712,7 @@ def run_sweep(args):
                 raw[k] = np.ascontiguousarray(raw[k][:, :, :groups])
         sh, starts = torch.from_numpy(raw["spatial_shapes"]), raw["level_start_index"]
         vdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-        if "sampling_locations" in raw:
-            loc_h = torch.from_numpy(raw["sampling_locations"])
-            # a reference point at the first sample's location and offsets to the others, in pixels
-            ref_h = loc_h[:, :, 0, :, 0, :].clone().contiguous()
-            whf = sh[:, [1, 0]].float()
-            off_h = ((loc_h - ref_h[:, :, None, :, None, :]) * whf[None, None, None, :, None, :]).contiguous()
-        else:
-            ref_h = torch.from_numpy(raw["reference_points"])
-            off_h = torch.from_numpy(raw["sampling_offsets"])
-            wh = sh[:, [1, 0]].to(torch.float64)
-            loc_h = (ref_h.double()[:, :, None, :, None, :] + off_h.double() / wh[None, None, None, :, None, :]).float()
+        loc_h, ref_h, off_h = location_inputs(raw, sh)
         lg_h = torch.from_numpy(raw["attention_logits"])
         attn_h = torch.softmax(lg_h.double(), -1).float().reshape(loc_h.shape[:-1]).contiguous()
         value = torch.from_numpy(raw["value"]).to(vdt).to(dev)
@@ -726,6 +740,12 @@ def run_sweep(args):
                                                                 grad_attention_logits=glg, flags=acc), reps,
                                pre=lambda: gv.zero_()),
         }
+        # the same calls with L2 warm (no flush between them): reported beside
+        # the flushed times, which are the ones the rates use
+        warm = {"fwd": timed(lambda: msda.msda_forward(value, sh, starts, loc, attn, output=out), reps, warm=True),
+                "bwd": timed(lambda: msda.msda_backward(value, sh, starts, loc, attn, gout, grad_value=gv,
+                                                        grad_sampling_locations=gl, grad_attention_weights=ga,
+                                                        flags=acc), reps, pre=lambda: gv.zero_(), warm=True)}
         ab = algorithmic_bytes(w, groups)
         ab["bwd_deterministic"] = ab["bwd"]
         # sparse queries: value traffic counted as the sectors the samples touch
@@ -737,6 +757,8 @@ def run_sweep(args):
             calls[k] = {"us": ms * 1e3, "points_per_s": w.samples / (ms / 1e3), "gbs": gbs,
                         "frac_of_measured_hbm_peak": gbs / peak, "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
                         "algorithmic_bytes": ab[k]}
+            if k in warm:
+                calls[k]["warm_l2_us"] = warm[k] * 1e3
             if touched is not None:
                 tb = ab[k] - vbytes + touched
                 calls[k].update({"algorithmic_bytes_touched_value": tb,
@@ -827,6 +849,18 @@ def _oracle_step(s):
     oracle.backward(s["value"], s["sh"], s["st"], s["loc"], s["attn"], s["g"])
 
 
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo), or None."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def cpu_baseline(w, raw, loc, attn, value, gout, budget_s=12.0):
     """The fp64 oracle, as it stands, single-threaded on this host: forward +
     backward on the whole workload, repeated until about `budget_s` seconds."""
@@ -840,7 +874,7 @@ def cpu_baseline(w, raw, loc, attn, value, gout, budget_s=12.0):
             break
     return {"value": w.samples * reps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"whole {w.name} workload (all {w.N * w.Lq} queries), forward + backward, {reps} repetitions, "
-                      f"{el:.1f} s", "host_cores_available": os.cpu_count()}
+                      f"{el:.1f} s", "host_cores_available": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args):
@@ -850,7 +884,11 @@ def run_reference(args):
     import oracle
     w = workloads.WORKLOADS[args.workload]
     raw = workloads.draw(w)
-    loc = oracle.locations(raw["spatial_shapes"], raw["reference_points"], raw["sampling_offsets"]).astype(np.float32)
+    if "sampling_locations" in raw:        # locations drawn directly (the tiny workload)
+        loc = raw["sampling_locations"].astype(np.float32)
+    else:
+        loc = oracle.locations(raw["spatial_shapes"], raw["reference_points"],
+                               raw["sampling_offsets"]).astype(np.float32)
     attn = oracle.softmax(raw["attention_logits"]).astype(np.float32).reshape(loc.shape[:-1])
     # one step = forward + backward of a bounded query sample (all batches)
     q_per_step = max(1, w.Lq // 16)

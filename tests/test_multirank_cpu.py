@@ -102,3 +102,24 @@ def test_reference_arm_line():
     args = types.SimpleNamespace(workload=bench.WORKLOAD, step="unfused")
     expect = bench.workload_config(args, bench.workloads.WORKLOADS[bench.WORKLOAD], 1)
     assert {k: line["config"][k] for k in expect} == expect
+
+
+@pytest.mark.parametrize("name", ["tiny", "encoder"])
+def test_location_inputs_of_both_kinds_of_draw(name):
+    """The bench's input preparation: drawn references and offsets give
+    ref + off / (W, H); directly drawn locations (tiny) give a reference and
+    pixel offsets that rebuild them."""
+    import numpy as np
+    import torch
+    import workloads
+    w = workloads.WORKLOADS[name]
+    raw = workloads.draw(w)
+    sh = torch.from_numpy(raw["spatial_shapes"])
+    loc, ref, off = bench.location_inputs(raw, sh)
+    assert loc.dtype == torch.float32 and tuple(loc.shape) == (w.N, w.Lq, w.M, w.L, w.K, 2)
+    assert tuple(ref.shape) == (w.N, w.Lq, w.L, 2) and tuple(off.shape) == tuple(loc.shape)
+    wh = sh[:, [1, 0]].double()
+    rebuilt = ref.double()[:, :, None, :, None, :] + off.double() / wh[None, None, None, :, None, :]
+    assert np.allclose(rebuilt.numpy(), loc.double().numpy(), rtol=0, atol=1e-6)
+    if "sampling_locations" in raw:
+        assert np.array_equal(loc.numpy(), raw["sampling_locations"])
