@@ -768,13 +768,27 @@ def run_sweep(args):
         smp = _oracle_sample(w, raw, loc_h.numpy(), attn_h.numpy(), value.float().cpu().numpy(),
                              gout.float().cpu().numpy(), 0, q)
         t0 = time.perf_counter()
-        _oracle_step(smp)
+        ref_out, ref_gv, _, ref_ga = _oracle_step(smp)
         el = time.perf_counter() - t0
         pts = w.N * q * w.M * w.L * w.K
+        # the library on the same sample and the same (storage-rounded) inputs:
+        # a forward and a backward call on the sample's queries alone
+        lq, aq, gq = (t[:, :q].contiguous() for t in (loc, attn, gout))
+        got_out = msda.msda_forward(value, sh, starts, lq, aq).float().cpu().numpy()
+        got_gv, _, got_ga = msda.msda_backward(value, sh, starts, lq, aq, gq)
+
+        def rel(a, b):
+            return float(np.abs(a - b).max() / max(float(np.abs(b).max()), 1e-30))
         line = {"sweep": True, "workload": name, "dtype": w.dtype, "samples": w.samples,
                 "head_groups": groups or w.M, "value_bytes": vbytes, "value_bytes_touched": touched, "calls": calls,
                 "oracle_fwd_bwd_points_per_s_1core": pts / el,
-                "oracle_sample": f"{q} of {w.Lq} queries x {w.N} batches"}
+                "oracle_sample": f"{q} of {w.Lq} queries x {w.N} batches",
+                "rel_error_vs_oracle": {
+                    "output": rel(got_out, ref_out), "grad_value": rel(got_gv.cpu().numpy(), ref_gv),
+                    "grad_attention_weights": rel(got_ga.cpu().numpy(), ref_ga),
+                    "norm": "max |lib - oracle| / max |oracle| on the oracle's query sample, same inputs "
+                            "(grad_sampling_locations is compared in the tests, which handle its one-sided "
+                            "derivative at cell edges)"}}
         if w.dtype == "bf16":
             # the storage error itself: the forward against the oracle on the
             # unrounded fp32 draws, on the same query sample (normwise rel)
@@ -825,13 +839,24 @@ def run_sweep_volumes(timed, peak):
     q = 64
     lv = raw["sampling_locations"][:, :q].astype(np.float64)
     t0 = time.perf_counter()
-    oracle.forward3d(raw["value"].astype(np.float64), sh, st, lv, attn_h.numpy()[:, :q].astype(np.float64))
-    oracle.backward3d(raw["value"].astype(np.float64), sh, st, lv, attn_h.numpy()[:, :q].astype(np.float64),
-                      raw["grad_output"][:, :q].astype(np.float64))
+    ref_out = oracle.forward3d(raw["value"].astype(np.float64), sh, st, lv, attn_h.numpy()[:, :q].astype(np.float64))
+    ref_gv, _, ref_ga = oracle.backward3d(raw["value"].astype(np.float64), sh, st, lv,
+                                          attn_h.numpy()[:, :q].astype(np.float64),
+                                          raw["grad_output"][:, :q].astype(np.float64))
     el = time.perf_counter() - t0
+    # the library on the same sample (same inputs)
+    lq, aq, gq = (t[:, :q].contiguous() for t in (loc, attn, gout))
+    got_out = msda.msda3d_forward(value, sh, st, lq, aq).cpu().numpy()
+    got_gv, _, got_ga = msda.msda3d_backward(value, sh, st, lq, aq, gq)
+
+    def rel(a, b):
+        return float(np.abs(a - b).max() / max(float(np.abs(b).max()), 1e-30))
     print(json.dumps({"sweep": True, "workload": "video (3-D, trilinear)", "dtype": "f32", "samples": samples,
                       "calls": calls, "oracle_fwd_bwd_points_per_s_1core": N * q * M * L * K / el,
-                      "oracle_sample": f"{q} of {Lq} queries"}))
+                      "oracle_sample": f"{q} of {Lq} queries",
+                      "rel_error_vs_oracle": {"output": rel(got_out, ref_out),
+                                              "grad_value": rel(got_gv.cpu().numpy(), ref_gv),
+                                              "grad_attention_weights": rel(got_ga.cpu().numpy(), ref_ga)}}))
 
 
 # ----------------------------------------------------------------------------- oracle timings
@@ -844,9 +869,10 @@ def _oracle_sample(w, raw, loc, attn, value, gout, q0, q1):
 
 
 def _oracle_step(s):
+    """Forward and backward of the oracle on a sample: (out, grad_value, grad_loc, grad_attn)."""
     import oracle
-    oracle.forward(s["value"], s["sh"], s["st"], s["loc"], s["attn"])
-    oracle.backward(s["value"], s["sh"], s["st"], s["loc"], s["attn"], s["g"])
+    out = oracle.forward(s["value"], s["sh"], s["st"], s["loc"], s["attn"])
+    return (out,) + tuple(oracle.backward(s["value"], s["sh"], s["st"], s["loc"], s["attn"], s["g"]))
 
 
 def cpu_model():
