@@ -698,6 +698,21 @@ def test_pixel_queries_band_order(msda, M, D, K, opt):
     H.assert_fwd(fo.float().cpu().numpy(), ref, "f32", f"D={D} pixel queries, fused, options {opt}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_band_order_with_any_queries(msda, dtype):
+    """Len_q == Len_in with queries that are not the value pixels (reference
+    points drawn at random): the fp32 forward still takes them in band order,
+    which only permutes the rows; unfused and fused against the oracle."""
+    w = workloads.custom(N=2, M=2, D=32, levels=[(6, 5), (3, 7), (2, 2)], K=4, dtype=dtype, refs="uniform",
+                         ref_range=(-0.05, 1.05), offset_sigma=0.2, seed=2400)
+    p = H.prepared(w)
+    assert w.Lq == w.Len_in
+    H.assert_fwd(_run_forward(msda, w, p), _oracle_forward(p), dtype, "random queries, band order")
+    ref = oracle.forward_fused(p["value"], p["spatial_shapes"], p["level_start_index"], p["reference_points"],
+                               p["sampling_offsets"], p["attention_logits"])
+    H.assert_fwd(_run_fused(msda, w, p), ref, dtype, "random queries, band order, fused")
+
+
 def test_group_count_must_divide_the_heads(msda):
     w = workloads.custom(N=1, M=6, D=8, levels=[(4, 4)], K=2, Len_q=5, refs="none", seed=3)
     p = H.prepared(w)
