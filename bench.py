@@ -887,6 +887,69 @@ def cpu_model():
     return None
 
 
+_WORKER_INPUTS = {}
+
+
+def _oracle_inputs(name):
+    """The oracle's float64 inputs of a whole workload (storage-rounded value
+    and grad_output, as the GPU sees them), drawn from the workload's seed."""
+    import torch
+    w = workloads.WORKLOADS[name]
+    raw = workloads.draw(w)
+    sh = torch.from_numpy(raw["spatial_shapes"])
+    loc_h, _, _ = location_inputs(raw, sh)
+    attn_h = torch.softmax(torch.from_numpy(raw["attention_logits"]).double(), -1).float().reshape(loc_h.shape[:-1])
+    vdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    value = torch.from_numpy(raw["value"]).to(vdt).float().numpy()
+    gout = torch.from_numpy(raw["grad_output"]).to(vdt).float().numpy()
+    return w, raw, loc_h.numpy(), attn_h.numpy(), value, gout
+
+
+def _worker_prepare(name):
+    """Pool worker: draw and keep the workload's oracle inputs (untimed)."""
+    if name not in _WORKER_INPUTS:
+        _WORKER_INPUTS[name] = _oracle_inputs(name)
+    w, raw, loc, attn, value, gout = _WORKER_INPUTS[name]
+    _oracle_step(_oracle_sample(w, raw, loc, attn, value, gout, 0, 1))     # loads the oracle library
+    return os.getpid()
+
+
+def _worker_range(task):
+    """Pool worker: the oracle's forward + backward on queries [q0, q1) of all batches."""
+    name, q0, q1 = task
+    w, raw, loc, attn, value, gout = _WORKER_INPUTS[name]
+    _oracle_step(_oracle_sample(w, raw, loc, attn, value, gout, q0, q1))
+    return q1 - q0
+
+
+def run_cpu_all_cores(args):
+    """The fp64 oracle, as it stands, on every host core: the workload's queries
+    split over one process per core (a spawn-started pool that never touches
+    the GPU), forward + backward of the whole workload timed by wall clock.
+    Prints one JSON line."""
+    import multiprocessing as mp
+    w = workloads.WORKLOADS[args.workload]
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pids = set(pool.map(_worker_prepare, [args.workload] * (4 * cores)))
+        if len(pids) < cores:          # every worker prepared before the clock starts
+            pool.map(_worker_prepare, [args.workload] * (16 * cores))
+        chunk = max(1, -(-w.Lq // (4 * cores)))
+        tasks = [(args.workload, q0, min(w.Lq, q0 + chunk)) for q0 in range(0, w.Lq, chunk)]
+        times = []
+        for _ in range(3):             # the median of three passes over the whole workload
+            t0 = time.perf_counter()
+            done = sum(pool.map(_worker_range, tasks, chunksize=1))
+            times.append(time.perf_counter() - t0)
+            assert done == w.Lq
+    el = statistics.median(times)
+    print(json.dumps({"cpu_baseline_all_cores": {
+        "value": w.samples / el, "unit": UNIT, "cores": cores, "kind": "oracle", "seconds": el,
+        "sample": f"whole {args.workload} workload, forward + backward, its {w.Lq} queries (x{w.N} batches) in "
+                  f"{len(tasks)} ranges over {cores} processes; median of 3 passes", "cpu_model": cpu_model()}}))
+
+
 def cpu_baseline(w, raw, loc, attn, value, gout, budget_s=12.0):
     """The fp64 oracle, as it stands, single-threaded on this host: forward +
     backward on the whole workload, repeated until about `budget_s` seconds."""
@@ -954,13 +1017,17 @@ def main(argv=None):
     ap.add_argument("--sweep-only", default="",
                     help="comma list of sweep workloads (tiny, encoder, decoder, encoder_train, large, encoder_g1, "
                          "video)")
+    ap.add_argument("--cpu-all-cores", action="store_true",
+                    help="the oracle on every host core (one process each), the whole workload once; no GPU")
     ap.add_argument("--step", choices=["unfused", "fused"], default="unfused",
                     help="unfused: msda_forward + msda_backward on locations and weights; fused: msda_forward_fused + "
                          "msda_backward_fused on reference points, offsets and logits")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.line_rates:
+    if args.cpu_all_cores:
+        run_cpu_all_cores(args)
+    elif args.line_rates:
         run_line_rates(args)
     elif args.sweep:
         run_sweep(args)

@@ -123,3 +123,11 @@ def test_location_inputs_of_both_kinds_of_draw(name):
     assert np.allclose(rebuilt.numpy(), loc.double().numpy(), rtol=0, atol=1e-6)
     if "sampling_locations" in raw:
         assert np.array_equal(loc.numpy(), raw["sampling_locations"])
+
+
+def test_oracle_on_all_cores_line(capsys):
+    """bench.py --cpu-all-cores: the oracle over every host core, one JSON line."""
+    import json
+    bench.main(["--cpu-all-cores", "--workload", "tiny"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])["cpu_baseline_all_cores"]
+    assert line["kind"] == "oracle" and line["cores"] >= 1 and line["value"] > 0 and line["unit"] == bench.UNIT
