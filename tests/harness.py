@@ -208,3 +208,25 @@ def assert_bwd(gpu, ref, dtype, what):
     tol = BF16_REL if dtype == "bf16" else BWD_F32_REL
     assert rel <= tol, f"{what}: rel {rel:.3e} > {tol} (abs {ab:.3e})"
     return ab, rel
+
+
+RANDOM_PROBLEMS = 64
+
+
+def random_problem(i):
+    """Seeded random problem i of the randomized parity tests: (workload, options).
+    Head width 8-256, 1-8 heads, 1-5 levels of 1-12 x 1-12 pixels, 1-8 points,
+    Len_q either every pixel (pixel-centre references) or 1-69 random queries,
+    either dtype, any option combination."""
+    r = np.random.default_rng(5000 + i)
+    D = int(r.choice([8, 16, 32, 64, 128, 256]))
+    M = int(r.choice([m for m in (1, 2, 3, 4, 8) if m * D <= 1024]))
+    L = int(r.integers(1, 6))
+    K = int(r.integers(1, 9))
+    levels = [(int(r.integers(1, 13)), int(r.integers(1, 13))) for _ in range(L)]
+    pixel_queries = bool(r.integers(0, 2))
+    w = workloads.custom(N=int(r.integers(1, 4)), M=M, D=D, levels=levels, K=K,
+                         Len_q=-1 if pixel_queries else int(r.integers(1, 70)),
+                         dtype=str(r.choice(["f32", "bf16"])), refs="pixel_centres" if pixel_queries else "uniform",
+                         ref_range=(-0.05, 1.05), offset_sigma=float(r.choice([0.05, 0.2])), seed=6000 + i)
+    return w, int(r.integers(0, 4))

@@ -4,8 +4,9 @@ its tensor's extent and alignment; a bad access is counted and skipped, never
 trapped.  These cases run the shapes most likely to expose an index mistake
 (ragged query counts and level sizes, 1 x 1 and 2 x 1 levels, samples outside
 the maps, every head width, the merge table, both options, head groups, the
-3-D calls, the built-in-scratch backward) through it, and check that nothing
-was skipped and that the results still match the oracle."""
+3-D calls, the built-in-scratch backward, and the randomized parity tests'
+problems) through it, and check that nothing was skipped and that the results
+still match the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -33,6 +34,9 @@ def _cases():
                                       ref_range=(-0.05, 1.05), offset_sigma=0.2, seed=3300), 3, None
     yield "groups", workloads.custom(N=2, M=8, D=32, levels=[(23, 31), (6, 8), (3, 4)], K=4, Len_q=53,
                                      refs="uniform", offset_sigma=0.1, seed=3400), 0, 1
+    for i in range(H.RANDOM_PROBLEMS):        # the randomized parity tests' problems
+        w, opt = H.random_problem(i)
+        yield f"random-{i}", w, opt, None
 
 
 @pytest.fixture(scope="module")

@@ -713,6 +713,34 @@ def test_band_order_with_any_queries(msda, dtype):
     H.assert_fwd(_run_fused(msda, w, p), ref, dtype, "random queries, band order, fused")
 
 
+@pytest.mark.parametrize("i", range(H.RANDOM_PROBLEMS))
+def test_random_problems_all_calls(msda, i):
+    """Seeded random problems: head width 8-256, 1-8 heads, 1-5 levels of
+    1-12 x 1-12 pixels, 1-8 points, Len_q either every pixel (band order in
+    the fp32 forward) or 1-69 random queries, either dtype, every option
+    combination; every call against the oracle, both backward modes."""
+    w, opt = H.random_problem(i)
+    p = H.prepared(w)
+    dt = H.storage_dtype(w)
+    v, g = H.dev(p["value"], dt), H.dev(p["grad_output"], dt)
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+    loc, attn = H.dev(p["sampling_locations"]), H.dev(p["attention_weights"])
+    ref, off, lg = H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]), H.dev(p["attention_logits"])
+    what = f"case {i}: N={w.N} M={w.M} D={w.D} levels={w.levels} K={w.K} Lq={w.Lq} {w.dtype} options={opt}"
+    out = msda.msda_forward(v, sh, st, loc, attn, options=opt).float().cpu().numpy()
+    H.assert_fwd(out, oracle.forward(p["value"], sh, st, p["sampling_locations"], p["attention_weights"],
+                                     options=opt), w.dtype, what + " forward")
+    fo = msda.msda_forward_fused(v, sh, st, ref, off, lg, options=opt).float().cpu().numpy()
+    H.assert_fwd(fo, oracle.forward_fused(p["value"], sh, st, p["reference_points"], p["sampling_offsets"],
+                                          p["attention_logits"], options=opt), w.dtype, what + " fused forward")
+    ref_b, ref_fb = _oracle_backward(p, opt), _oracle_backward_fused(p, opt)
+    for flags in (0, msda.MSDA_DETERMINISTIC):
+        got = msda.msda_backward(v, sh, st, loc, attn, g, flags=flags, options=opt)
+        _check_backward(w, [t.cpu().numpy() for t in got], ref_b)
+        got = msda.msda_backward_fused(v, sh, st, ref, off, lg, g, flags=flags, options=opt)
+        _check_backward_fused(w, [t.cpu().numpy() for t in got], ref_fb)
+
+
 def test_group_count_must_divide_the_heads(msda):
     w = workloads.custom(N=1, M=6, D=8, levels=[(4, 4)], K=2, Len_q=5, refs="none", seed=3)
     p = H.prepared(w)
