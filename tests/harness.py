@@ -214,10 +214,11 @@ RANDOM_PROBLEMS = 64
 
 
 def random_problem(i):
-    """Seeded random problem i of the randomized parity tests: (workload, options).
+    """Seeded random problem i of the randomized parity tests: (workload,
+    options, head groups G).
     Head width 8-256, 1-8 heads, 1-5 levels of 1-12 x 1-12 pixels, 1-8 points,
     Len_q either every pixel (pixel-centre references) or 1-69 random queries,
-    either dtype, any option combination."""
+    either dtype, any option combination, any head grouping the kernels take."""
     r = np.random.default_rng(5000 + i)
     D = int(r.choice([8, 16, 32, 64, 128, 256]))
     M = int(r.choice([m for m in (1, 2, 3, 4, 8) if m * D <= 1024]))
@@ -229,4 +230,19 @@ def random_problem(i):
                          Len_q=-1 if pixel_queries else int(r.integers(1, 70)),
                          dtype=str(r.choice(["f32", "bf16"])), refs="pixel_centres" if pixel_queries else "uniform",
                          ref_range=(-0.05, 1.05), offset_sigma=float(r.choice([0.05, 0.2])), seed=6000 + i)
-    return w, int(r.integers(0, 4))
+    opt = int(r.integers(0, 4))
+    # head groups: G sets shared by M / G heads each, where the group width
+    # (M / G) * D is a power of two the kernels take (G = M half the time)
+    widths = {8, 16, 32, 64, 128, 256}
+    Gs = [g for g in range(1, M + 1) if M % g == 0 and (M // g) * D in widths]
+    G = M if r.integers(0, 2) == 0 else int(r.choice(Gs))
+    return w, opt, G
+
+
+PER_SAMPLE = ("sampling_locations", "attention_weights", "sampling_offsets", "attention_logits")
+
+
+def grouped(p, G):
+    """The inputs cut to G sets of locations and weights: the per-sample tensors
+    keep their first G heads' sets, shared by groups of M / G heads."""
+    return {k: (np.ascontiguousarray(v[:, :, :G]) if k in PER_SAMPLE else v) for k, v in p.items()}

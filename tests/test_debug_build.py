@@ -35,8 +35,8 @@ def _cases():
     yield "groups", workloads.custom(N=2, M=8, D=32, levels=[(23, 31), (6, 8), (3, 4)], K=4, Len_q=53,
                                      refs="uniform", offset_sigma=0.1, seed=3400), 0, 1
     for i in range(H.RANDOM_PROBLEMS):        # the randomized parity tests' problems
-        w, opt = H.random_problem(i)
-        yield f"random-{i}", w, opt, None
+        w, opt, G = H.random_problem(i)
+        yield f"random-{i}", w, opt, G if G < w.M else None
 
 
 @pytest.fixture(scope="module")

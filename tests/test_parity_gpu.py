@@ -715,18 +715,19 @@ def test_band_order_with_any_queries(msda, dtype):
 
 @pytest.mark.parametrize("i", range(H.RANDOM_PROBLEMS))
 def test_random_problems_all_calls(msda, i):
-    """Seeded random problems: head width 8-256, 1-8 heads, 1-5 levels of
-    1-12 x 1-12 pixels, 1-8 points, Len_q either every pixel (band order in
-    the fp32 forward) or 1-69 random queries, either dtype, every option
-    combination; every call against the oracle, both backward modes."""
-    w, opt = H.random_problem(i)
-    p = H.prepared(w)
+    """Seeded random problems: head width 8-256, 1-8 heads in any supported
+    grouping, 1-5 levels of 1-12 x 1-12 pixels, 1-8 points, Len_q either every
+    pixel (band order in the fp32 forward) or 1-69 random queries, either dtype,
+    every option combination; every call against the oracle, both backward
+    modes."""
+    w, opt, G = H.random_problem(i)
+    p = H.grouped(H.prepared(w), G)
     dt = H.storage_dtype(w)
     v, g = H.dev(p["value"], dt), H.dev(p["grad_output"], dt)
     sh, st = p["spatial_shapes"], p["level_start_index"]
     loc, attn = H.dev(p["sampling_locations"]), H.dev(p["attention_weights"])
     ref, off, lg = H.dev(p["reference_points"]), H.dev(p["sampling_offsets"]), H.dev(p["attention_logits"])
-    what = f"case {i}: N={w.N} M={w.M} D={w.D} levels={w.levels} K={w.K} Lq={w.Lq} {w.dtype} options={opt}"
+    what = f"case {i}: N={w.N} M={w.M} G={G} D={w.D} levels={w.levels} K={w.K} Lq={w.Lq} {w.dtype} options={opt}"
     out = msda.msda_forward(v, sh, st, loc, attn, options=opt).float().cpu().numpy()
     H.assert_fwd(out, oracle.forward(p["value"], sh, st, p["sampling_locations"], p["attention_weights"],
                                      options=opt), w.dtype, what + " forward")
