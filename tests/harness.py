@@ -246,3 +246,41 @@ def grouped(p, G):
     """The inputs cut to G sets of locations and weights: the per-sample tensors
     keep their first G heads' sets, shared by groups of M / G heads."""
     return {k: (np.ascontiguousarray(v[:, :, :G]) if k in PER_SAMPLE else v) for k, v in p.items()}
+
+
+RANDOM_VOLUMES = 24
+
+
+def random_volume_problem(i):
+    """Seeded random 3-D problem i: (raw draws, value, grad_output, attention
+    weights, dtype, options).  Head width 8-64, 1-4 heads, 1-4 levels of 1-6
+    frames x 1-6 rows x 1-6 columns, 1-6 points, 1-60 queries, locations over
+    [-0.15, 1.15]^3, either dtype, align_corners or not."""
+    r = np.random.default_rng(7000 + i)
+    D = int(r.choice([8, 16, 32, 64]))
+    M, L, K = int(r.integers(1, 5)), int(r.integers(1, 5)), int(r.integers(1, 7))
+    levels = [tuple(int(x) for x in r.integers(1, 7, size=3)) for _ in range(L)]
+    N, Lq = int(r.integers(1, 4)), int(r.integers(1, 61))
+    dtype, opt = str(r.choice(["f32", "bf16"])), int(r.choice([0, 2]))
+    raw = workloads.draw_volumes(N, M, D, levels, K, Lq, dtype=dtype, loc_range=(-0.15, 1.15), seed=7500 + i)
+    attn = oracle.softmax(raw["attention_logits"]).astype(np.float32).reshape(N, Lq, M, L, K)
+    value, g = raw["value"], raw["grad_output"]
+    if dtype == "bf16":
+        value, g = bf16_round(value), bf16_round(g)
+    return raw, value, g, attn, dtype, opt
+
+
+def check_3d_calls(msda, case, what):
+    """msda3d_forward and msda3d_backward (both modes) of a 3-D case against the oracle."""
+    raw, value, g, attn, dtype, opt = case
+    sh, st, loc = raw["spatial_shapes"], raw["level_start_index"], raw["sampling_locations"]
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    v, gd, locd, ad = dev(value, dt), dev(g, dt), dev(loc), dev(attn)
+    out = msda.msda3d_forward(v, sh, st, locd, ad, options=opt).float().cpu().numpy()
+    assert_fwd(out, oracle.forward3d(value, sh, st, loc, attn, options=opt), dtype, what + " forward")
+    ref = backward3d_reference(dict(value=value, spatial_shapes=sh, level_start_index=st, sampling_locations=loc,
+                                    attention_weights=attn, grad_output=g), opt)
+    for flags in (0, msda.MSDA_DETERMINISTIC):
+        got = [t.cpu().numpy() for t in msda.msda3d_backward(v, sh, st, locd, ad, gd, flags=flags, options=opt)]
+        for nm, a, b in zip(("grad_value", "grad_loc", "grad_attn"), got, ref.for_gpu(got)):
+            assert_bwd(a, b, "f32", f"{what} {nm} flags {flags}")

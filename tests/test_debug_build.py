@@ -111,3 +111,13 @@ def test_debug_build_3d_and_noalloc(debug_msda):
         H.assert_bwd(a, b, "f32", f"built-in scratch {nm}")
     torch.cuda.synchronize()
     assert lib.msda_debug_violations(1) == 0, "the debug build skipped accesses"
+
+
+def test_debug_build_3d_random_problems(debug_msda):
+    """The randomized 3-D parity tests' problems through the debug build."""
+    msda, lib = debug_msda
+    lib.msda_debug_violations(1)
+    for i in range(H.RANDOM_VOLUMES):
+        H.check_3d_calls(msda, H.random_volume_problem(i), f"3-D case {i}")
+    torch.cuda.synchronize()
+    assert lib.msda_debug_violations(1) == 0, "the debug build skipped accesses"

@@ -442,6 +442,14 @@ def test_3d_forward_backward(msda, dtype, D, opt):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), "deterministic 3-D backward is not bitwise stable"
 
 
+@pytest.mark.parametrize("i", range(H.RANDOM_VOLUMES))
+def test_3d_random_problems(msda, i):
+    """Seeded random 3-D problems (head width 8-64, 1-4 heads, 1-4 levels of
+    up to 6 x 6 x 6 voxels, 1-6 points, 1-60 queries, either dtype, with and
+    without align_corners): both 3-D calls, both modes, against the oracle."""
+    H.check_3d_calls(msda, H.random_volume_problem(i), f"3-D case {i}")
+
+
 def test_3d_one_slice_is_2d(msda):
     """One-slice volumes sampled on their centre plane give the 2-D call's result."""
     w = workloads.custom(N=1, M=2, D=32, levels=[(6, 7), (3, 4)], K=3, Len_q=19, refs="none", seed=1450)
