@@ -564,6 +564,7 @@ def _probes():
     lib.msda_probe_gather.argtypes = [vp, i64, i64, i64, vp, u32, vp]
     lib.msda_probe_reduce.argtypes = [vp, i64, i64, i64, u32, vp]
     lib.msda_probe_mixed.argtypes = [vp, i64, i64, ctypes.c_int, vp, u32, vp]
+    lib.msda_probe_bulk_reduce.argtypes = [vp, i64, i64, u32, vp]
     lib.msda_probe_accesses.argtypes = [i64]
     lib.msda_probe_accesses.restype = i64
     return lib
@@ -578,6 +579,8 @@ def line_rates(dev, buf_bytes, lines, reps=10):
       gather_hot        the same over the first 128 KB (L1-resident)
       reduce            red.global.add.v4.f32 into uniform lines
       reduce_hot        the same over 128 KB (contended)
+      bulk_reduce       the same reductions through the TMA unit (a 128-byte
+                        cp.reduce.async.bulk per line, staged in shared memory)
       mixed_r           eight gathers and r reductions per quarter-warp round
     """
     import ctypes
@@ -609,6 +612,7 @@ def line_rates(dev, buf_bytes, lines, reps=10):
         "gather_hot": timed_ms(lambda i=0: lib.msda_probe_gather(bp, n_lines, hot, lines, kp, 17 + i, sp)),
         "reduce": timed_ms(lambda i=0: lib.msda_probe_reduce(bp, n_lines, 0, lines, 17 + i, sp)),
         "reduce_hot": timed_ms(lambda i=0: lib.msda_probe_reduce(bp, n_lines, hot, lines, 17 + i, sp)),
+        "bulk_reduce": timed_ms(lambda i=0: lib.msda_probe_bulk_reduce(bp, n_lines, lines, 17 + i, sp)),
     }
     for r in (2, 4, 6, 8):
         ms[f"mixed_{r}"] = timed_ms(lambda i=0, r=r: lib.msda_probe_mixed(bp, n_lines, lines, r, kp, 17 + i, sp))

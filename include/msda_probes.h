@@ -23,6 +23,11 @@
  *                       msda_probe_sink_bytes())
  *   msda_probe_reduce   red.global.add.v4.f32 of 1.0 into each line (the
  *                       buffer must hold floats; its contents change)
+ *   msda_probe_bulk_reduce  the same reductions through the TMA unit: each
+ *                       quarter-warp stages its line's 128 bytes of 1.0 in
+ *                       shared memory and issues one cp.reduce.async.bulk
+ *                       .add.f32 of them into the line (the buffer must hold
+ *                       floats; its contents change)
  *   msda_probe_mixed    per eight gathers, `reds_per_8` (0..8) reductions into
  *                       other lines (from a second stream): the backward's mix;
  *                       msda_probe_accesses(lines) gathers, that times
@@ -43,6 +48,7 @@ int64_t msda_probe_accesses(int64_t lines);
 int msda_probe_gather(const void *buf, int64_t n_lines, int64_t hot_lines, int64_t lines, void *sink, uint32_t seed,
                       void *stream);
 int msda_probe_reduce(void *buf, int64_t n_lines, int64_t hot_lines, int64_t lines, uint32_t seed, void *stream);
+int msda_probe_bulk_reduce(void *buf, int64_t n_lines, int64_t lines, uint32_t seed, void *stream);
 int msda_probe_mixed(void *buf, int64_t n_lines, int64_t lines, int reds_per_8, void *sink, uint32_t seed,
                      void *stream);
 

@@ -117,6 +117,46 @@ __global__ void __launch_bounds__(kThreads) mixed_kernel(float4 *buf, uint32_t n
     sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = make_float4(acc, 0.f, 0.f, 0.f);
 }
 
+// Bulk (TMA) reductions: each quarter-warp stages its line in one of kSlots
+// 128-byte shared-memory slots (its eight lanes write 16 bytes each), fences
+// the writes to the async proxy, and its first lane issues one
+// cp.reduce.async.bulk .add.f32 of the 128 bytes into the line, so a warp
+// step covers four lines as the reductions above do.  A slot is written again
+// only after the bulk group that read it has finished reading (wait_group.read
+// on the issuing lane, which owns the groups), and every lane's groups are
+// complete before the kernel returns.
+constexpr int kSlots = 8;
+
+__global__ void __launch_bounds__(kThreads) bulk_reduce_kernel(float4 *buf, uint32_t n, long long rounds,
+                                                               uint32_t seed) {
+    __shared__ __align__(128) float4 stage[kThreads / 8][kSlots][8];     // [quarter][slot][lane]
+    const int sub = threadIdx.x & 7, qw = threadIdx.x >> 3;
+    const uint32_t quarter = (blockIdx.x * blockDim.x + threadIdx.x) >> 3;
+    uint32_t x = mix32(seed ^ mix32(quarter));
+    const float4 one = make_float4(1.f, 1.f, 1.f, 1.f);
+    for (long long r = 0; r < rounds; ++r) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int slot = u % kSlots;
+            x = lcg(x);
+            const uint32_t line = pick(x, n);
+            if (sub == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kSlots - 1) : "memory");
+            __syncwarp();
+            stage[qw][slot][sub] = one;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (sub == 0) {
+                const uint32_t sa = (uint32_t)__cvta_generic_to_shared(&stage[qw][slot][0]);
+                asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], 128;"
+                             ::"l"(buf + (size_t)line * 8), "r"(sa) : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+        }
+    }
+    if (sub == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+}
+
 // accesses per launch: rounds * kUnroll * quarter-warps
 long long rounds_for(int64_t lines) {
     const long long q = (long long)kBlocks * kThreads / 8;
@@ -141,6 +181,13 @@ int msda_probe_gather(const void *buf, int64_t n_lines, int64_t hot_lines, int64
     const uint32_t n = (uint32_t)(hot_lines > 0 && hot_lines < n_lines ? hot_lines : n_lines);
     gather_kernel<<<kBlocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const float4 *>(buf), n, rounds_for(lines), static_cast<float4 *>(sink), seed);
+    return (int)cudaGetLastError();
+}
+
+int msda_probe_bulk_reduce(void *buf, int64_t n_lines, int64_t lines, uint32_t seed, void *stream) {
+    if (!buf || !lines_ok(n_lines, lines) || (reinterpret_cast<uintptr_t>(buf) & 15)) return (int)cudaErrorInvalidValue;
+    bulk_reduce_kernel<<<kBlocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<float4 *>(buf), (uint32_t)n_lines, rounds_for(lines), seed);
     return (int)cudaGetLastError();
 }
 
