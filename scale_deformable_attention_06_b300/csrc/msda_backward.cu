@@ -24,12 +24,14 @@
 //            3 * log2(R); then the grad_value contributions A * w_c * g;
 //   phase 3: the chunk's per-sample gradients, written contiguously.
 // grad_value contributions go out as one vector reduction (red.global.add.v4
-// .f32) per corner and lane, or, on densely sampled levels of a D = 32
-// problem, through a per-warp merge table: the HW queries of a warp are
-// neighbours, so on a coarse level their corners often coincide; the table
-// sums, per distinct corner pixel, one coefficient per query, and one
-// reduction per distinct pixel carries sum_h alpha_h * g_h.  Either way every
-// contribution is added exactly once.
+// .f32) per corner and lane, or through a per-warp merge table: on densely
+// sampled levels of a D = 32 problem the HW = 4 queries of a warp are
+// neighbours, so on a coarse level their corners often coincide; where a warp
+// holds one query of 128 or 256 channels, that query's own samples coincide
+// often enough on every level, and a merged entry saves a whole row of
+// reductions.  The table sums, per distinct corner pixel, one coefficient per
+// query, and one reduction per distinct pixel carries sum_h alpha_h * g_h.
+// Either way every contribution is added exactly once.
 //
 // Deterministic mode replaces the fp32 reductions by 64-bit integer ones in
 // fixed point (integer addition is associative, so the order in which the
@@ -117,7 +119,7 @@ struct BwdWarpSmemMerge {
     float gdot[FUSED && OPTS ? HW : 1][FUSED && OPTS ? kMaxLevels : 1];
     float dotp[FUSED ? 64 : 1];
     unsigned key[SLOTS];               // corner pixel of the slot, kEmptyKey if free
-    float4 alpha[SLOTS];               // per query of the warp: summed A * w_c (HW == 4)
+    std::conditional_t<HW == 4, float4, float> alpha[SLOTS];   // per query of the warp: summed A * w_c
     unsigned short list[SLOTS];        // occupied slots in order of first use
     int count;
 };
@@ -143,7 +145,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int R = BwdLanes<D>::R, HW = BwdLanes<D>::HW, NV = BwdLanes<D>::NV;
     constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
     static_assert(HW * RC == 64, "phase 1 and 3 give every lane two (query, sample) slots");
-    static_assert(!MERGE || HW == 4, "the merge table holds four queries per slot");
+    static_assert(!MERGE || HW == 4 || HW == 1, "the merge table holds four queries or one per slot");
     constexpr int kMergeSlots = merge_slots<DET>();
     using WS = std::conditional_t<MERGE, BwdWarpSmemMerge<HW, RC, FUSED, OPTS, kMergeSlots>,
                                   BwdWarpSmem<HW, RC, FUSED, OPTS>>;
@@ -184,7 +186,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     if constexpr (MERGE) {
         for (int i = lane; i < kMergeSlots; i += 32) {
             sm.key[i] = kEmptyKey;
-            sm.alpha[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            sm.alpha[i] = {};
         }
         if (lane == 0) sm.count = 0;
         __syncwarp();
@@ -385,36 +387,50 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 if (merge) {
                     // one reduction per distinct corner pixel and lane: sum_h alpha_h * g_h
                     const int U = sm.count;
-                    // this lane's channels of grad_output of each of the warp's queries,
-                    // reloaded here rather than held in registers through the sample loop
-                    float4 gq[HW];
+                    if constexpr (HW == 4) {
+                        // this lane's channels of grad_output of each of the warp's queries,
+                        // reloaded here rather than held in registers through the sample loop
+                        float4 gq[HW];
 #pragma unroll
-                    for (int hh = 0; hh < HW; ++hh) {
-                        const int qq = qb * HW + hh;
-                        gq[hh] = qq < dm.Len_q
-                                     ? load4_value<T>(MSDA_ADDR(gten, gten + ((size_t)(n * dm.Len_q + qq) * dm.M + m) * D +
-                                                                          ch * 4, gtotal, 4),
-                                                      pol)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    for (int u0 = 0; u0 < U; u0 += HW) {
-                        const int ui = u0 + h;
-                        if (ui < U) {
+                        for (int hh = 0; hh < HW; ++hh) {
+                            const int qq = qb * HW + hh;
+                            gq[hh] = qq < dm.Len_q
+                                         ? load4_value<T>(MSDA_ADDR(gten, gten + ((size_t)(n * dm.Len_q + qq) * dm.M + m) *
+                                                                              D + ch * 4, gtotal, 4),
+                                                          pol)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        for (int u0 = 0; u0 < U; u0 += HW) {
+                            const int ui = u0 + h;
+                            if (ui < U) {
+                                const int slot = sm.list[ui];
+                                const float4 al = sm.alpha[slot];
+                                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                                acc = ffma4(al.x, gq[0], acc);
+                                acc = ffma4(al.y, gq[1], acc);
+                                acc = ffma4(al.z, gq[2], acc);
+                                acc = ffma4(al.w, gq[3], acc);
+                                scatter4<DET, R>(a, vhead + sm.key[slot], ch, acc, scale);
+                            }
+                        }
+                    } else {
+                        // one query a warp: every lane takes every distinct pixel, its
+                        // NV vectors of the query's grad_output already in registers
+                        for (int ui = 0; ui < U; ++ui) {
                             const int slot = sm.list[ui];
-                            const float4 al = sm.alpha[slot];
-                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                            acc = ffma4(al.x, gq[0], acc);
-                            acc = ffma4(al.y, gq[1], acc);
-                            acc = ffma4(al.z, gq[2], acc);
-                            acc = ffma4(al.w, gq[3], acc);
-                            scatter4<DET, R>(a, vhead + sm.key[slot], ch, acc, scale);
+                            const float al = sm.alpha[slot];
+                            const size_t base = vhead + sm.key[slot];
+#pragma unroll
+                            for (int k = 0; k < NV; ++k)
+                                scatter4<DET, R>(a, base + k * 4 * R, ch, ffma4(al, gv[k], make_float4(0.f, 0.f, 0.f, 0.f)),
+                                                 scale);
                         }
                     }
                     __syncwarp();
                     for (int ui = lane; ui < U; ui += 32) {
                         const int slot = sm.list[ui];
                         sm.key[slot] = kEmptyKey;
-                        sm.alpha[slot] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        sm.alpha[slot] = {};
                     }
                     if (lane == 0) sm.count = 0;
                     __syncwarp();
@@ -753,7 +769,7 @@ static void launch_bwd_kernel(const BwdArgs &a, bool det, unsigned blocks, cudaS
     constexpr int HW = BwdLanes<D>::HW;
     constexpr int B = kBwdWarpsPerBlock * 32;
     const bool merge = a.merge_mask != 0;
-    if constexpr (HW == 4) {
+    if constexpr (HW == 4 || HW == 1) {
         if (det && merge) msda_backward_kernel<T, D, true, true, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
         else if (det) msda_backward_kernel<T, D, true, false, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
         else if (merge) msda_backward_kernel<T, D, false, true, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
@@ -785,7 +801,10 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
     a.qblocks = (g.d.Len_q + HW - 1) / HW;
     // deterministic mode: a fixed-point reduction is four 64-bit atomics per
     // lane and corner, so merging pays on every level
-    a.merge_mask = HW == 4 ? (det ? (1u << g.d.L) - 1u : merge_levels(g)) : 0u;
+    // four queries a warp: the coarse levels (every level in deterministic mode);
+    // one query a warp (128 channels or more): every level, a merged entry
+    // saving at least a whole row of reductions
+    a.merge_mask = HW == 4 ? (det ? (1u << g.d.L) - 1u : merge_levels(g)) : HW == 1 ? (1u << g.d.L) - 1u : 0u;
     // fused: a row's weights are softmax outputs, summing to 1 (n_levels with
     // the per-level softmax)
     const float row_sum = g.d.per_level_softmax ? (float)g.d.L : 1.f;
