@@ -703,12 +703,12 @@ def run_sweep(args):
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
     chosen = args.sweep_only.split(",") if args.sweep_only else None
-    for name in ("tiny", "encoder", "decoder", "encoder_train", "large", "encoder_g1"):
+    for name in ("tiny", "encoder", "decoder", "encoder_train", "large", "encoder_g1", "encoder_g2", "encoder_g4"):
         if chosen is not None and name not in chosen:
             continue
-        # encoder_g1: the encoder workload with one set of locations and weights
-        # shared by all 8 heads (head groups, G = 1: 256 channels a set)
-        groups = 1 if name == "encoder_g1" else None
+        # encoder_gG: the encoder workload with G sets of locations and weights,
+        # each shared by 8 / G heads (head groups: 256, 128 or 64 channels a set)
+        groups = int(name[len("encoder_g"):]) if name.startswith("encoder_g") else None
         w = workloads.WORKLOADS["encoder" if groups else name]
         raw = workloads.draw(w)
         if groups:
@@ -1019,7 +1019,8 @@ def main(argv=None):
     ap.add_argument("--line-rates", action="store_true",
                     help="random 128-byte line gather / reduction rates of this GPU (libmsda_probes.so)")
     ap.add_argument("--sweep-only", default="",
-                    help="comma list of sweep workloads (tiny, encoder, decoder, encoder_train, large, encoder_g1, "
+                    help="comma list of sweep workloads (tiny, encoder, decoder, encoder_train, large, encoder_g1, encoder_g2, "
+                         "encoder_g4, "
                          "video)")
     ap.add_argument("--cpu-all-cores", action="store_true",
                     help="the oracle on every host core (one process each), the whole workload once; no GPU")

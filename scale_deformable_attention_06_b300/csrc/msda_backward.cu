@@ -25,11 +25,11 @@
 //   phase 3: the chunk's per-sample gradients, written contiguously.
 // grad_value contributions go out as one vector reduction (red.global.add.v4
 // .f32) per corner and lane, or through a per-warp merge table: on densely
-// sampled levels of a D = 32 problem the HW = 4 queries of a warp are
-// neighbours, so on a coarse level their corners often coincide; where a warp
-// holds one query of 128 or 256 channels, that query's own samples coincide
-// often enough on every level, and a merged entry saves a whole row of
-// reductions.  The table sums, per distinct corner pixel, one coefficient per
+// sampled levels of problems of 32 or 64 channels a set the HW = 4 or 2
+// queries of a warp are neighbours, so on a coarse level their corners often
+// coincide; where a warp holds one query of 128 or 256 channels, that query's
+// own samples coincide often enough on every level, and a merged entry saves
+// a whole row of reductions.  The table sums, per distinct corner pixel, one coefficient per
 // query, and one reduction per distinct pixel carries sum_h alpha_h * g_h.
 // Either way every contribution is added exactly once.
 //
@@ -119,7 +119,7 @@ struct BwdWarpSmemMerge {
     float gdot[FUSED && OPTS ? HW : 1][FUSED && OPTS ? kMaxLevels : 1];
     float dotp[FUSED ? 64 : 1];
     unsigned key[SLOTS];               // corner pixel of the slot, kEmptyKey if free
-    std::conditional_t<HW == 4, float4, float> alpha[SLOTS];   // per query of the warp: summed A * w_c
+    std::conditional_t<HW == 4, float4, std::conditional_t<HW == 2, float2, float>> alpha[SLOTS];   // per query of the warp: summed A * w_c
     unsigned short list[SLOTS];        // occupied slots in order of first use
     int count;
 };
@@ -145,7 +145,8 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int R = BwdLanes<D>::R, HW = BwdLanes<D>::HW, NV = BwdLanes<D>::NV;
     constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
     static_assert(HW * RC == 64, "phase 1 and 3 give every lane two (query, sample) slots");
-    static_assert(!MERGE || HW == 4 || HW == 1, "the merge table holds four queries or one per slot");
+    static_assert(!MERGE || HW == 4 || HW == 2 || HW == 1, "the merge table holds four, two or one queries a slot");
+    static_assert(!MERGE || HW == 1 || NV == 1, "several queries a warp: one vector a lane");
     constexpr int kMergeSlots = merge_slots<DET>();
     using WS = std::conditional_t<MERGE, BwdWarpSmemMerge<HW, RC, FUSED, OPTS, kMergeSlots>,
                                   BwdWarpSmem<HW, RC, FUSED, OPTS>>;
@@ -387,7 +388,7 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                 if (merge) {
                     // one reduction per distinct corner pixel and lane: sum_h alpha_h * g_h
                     const int U = sm.count;
-                    if constexpr (HW == 4) {
+                    if constexpr (HW > 1) {
                         // this lane's channels of grad_output of each of the warp's queries,
                         // reloaded here rather than held in registers through the sample loop
                         float4 gq[HW];
@@ -404,12 +405,11 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                             const int ui = u0 + h;
                             if (ui < U) {
                                 const int slot = sm.list[ui];
-                                const float4 al = sm.alpha[slot];
+                                const auto al = sm.alpha[slot];
+                                const float *alq = reinterpret_cast<const float *>(&al);
                                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                                acc = ffma4(al.x, gq[0], acc);
-                                acc = ffma4(al.y, gq[1], acc);
-                                acc = ffma4(al.z, gq[2], acc);
-                                acc = ffma4(al.w, gq[3], acc);
+#pragma unroll
+                                for (int hh = 0; hh < HW; ++hh) acc = ffma4(alq[hh], gq[hh], acc);
                                 scatter4<DET, R>(a, vhead + sm.key[slot], ch, acc, scale);
                             }
                         }
@@ -769,7 +769,7 @@ static void launch_bwd_kernel(const BwdArgs &a, bool det, unsigned blocks, cudaS
     constexpr int HW = BwdLanes<D>::HW;
     constexpr int B = kBwdWarpsPerBlock * 32;
     const bool merge = a.merge_mask != 0;
-    if constexpr (HW == 4 || HW == 1) {
+    if constexpr (HW == 4 || HW == 2 || HW == 1) {
         if (det && merge) msda_backward_kernel<T, D, true, true, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
         else if (det) msda_backward_kernel<T, D, true, false, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
         else if (merge) msda_backward_kernel<T, D, false, true, FUSED, OPTS><<<blocks, B, 0, stream>>>(a);
@@ -801,10 +801,13 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
     a.qblocks = (g.d.Len_q + HW - 1) / HW;
     // deterministic mode: a fixed-point reduction is four 64-bit atomics per
     // lane and corner, so merging pays on every level
-    // four queries a warp: the coarse levels (every level in deterministic mode);
-    // one query a warp (128 channels or more): every level, a merged entry
-    // saving at least a whole row of reductions
-    a.merge_mask = HW == 4 ? (det ? (1u << g.d.L) - 1u : merge_levels(g)) : HW == 1 ? (1u << g.d.L) - 1u : 0u;
+    // four or two queries a warp: the coarse levels (every level in
+    // deterministic mode; at two queries every level measured slower in fp32
+    // mode: 444 against 383 us on the encoder with 64 channels a set); one
+    // query a warp (128 channels or more): every level, a merged entry saving
+    // at least a whole row of reductions
+    const unsigned all_levels = (1u << g.d.L) - 1u;
+    a.merge_mask = HW == 1 ? all_levels : (HW == 4 || HW == 2) ? (det ? all_levels : merge_levels(g)) : 0u;
     // fused: a row's weights are softmax outputs, summing to 1 (n_levels with
     // the per-level softmax)
     const float row_sum = g.d.per_level_softmax ? (float)g.d.L : 1.f;
