@@ -136,11 +136,16 @@ struct BwdLanes {
 
 // OPTS: the problem sets option bits (fused calls); without them the kernel
 // carries none of the option code.  Launch bounds: eight blocks of four warps
-// per SM in deterministic mode up to head width 64 (64 registers), six
-// otherwise (85; fp32 mode uses about 62, so eight fit there too, and head
-// widths above 64 need the registers for two vectors a lane).
+// per SM up to head width 64 in deterministic mode and in the fused calls
+// (64 registers; fused kernels at 66-67 fell to seven blocks: large fused
+// backward 1.73 -> 1.70 ms, decoder 64 -> 62 us with the cap), except the
+// fp32 fused kernels with the merge table, and six otherwise (85: these use
+// 62-64, so eight fit, and the cap made them slower: encoder fused backward
+// 429 -> 436 us, unfused 383 -> 403 us; head widths above 64 need the
+// registers for two vectors a lane).
 template <typename T, int D, bool DET, bool MERGE, bool FUSED, bool OPTS>
-__global__ void __launch_bounds__(kBwdWarpsPerBlock * 32, (DET && D <= 64) ? 8 : 6)
+__global__ void __launch_bounds__(kBwdWarpsPerBlock * 32,
+                                  (D <= 64 && (DET || (FUSED && (sizeof(T) == 2 || !MERGE)))) ? 8 : 6)
 msda_backward_kernel(const __grid_constant__ BwdArgs a) {
     constexpr int R = BwdLanes<D>::R, HW = BwdLanes<D>::HW, NV = BwdLanes<D>::NV;
     constexpr int RC = kRecordsPerWarp / HW;      // samples per record chunk
@@ -406,10 +411,13 @@ msda_backward_kernel(const __grid_constant__ BwdArgs a) {
                             if (ui < U) {
                                 const int slot = sm.list[ui];
                                 const auto al = sm.alpha[slot];
-                                const float *alq = reinterpret_cast<const float *>(&al);
                                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                                for (int hh = 0; hh < HW; ++hh) acc = ffma4(alq[hh], gq[hh], acc);
+                                acc = ffma4(al.x, gq[0], acc);
+                                acc = ffma4(al.y, gq[1], acc);
+                                if constexpr (HW == 4) {
+                                    acc = ffma4(al.z, gq[2], acc);
+                                    acc = ffma4(al.w, gq[3], acc);
+                                }
                                 scatter4<DET, R>(a, vhead + sm.key[slot], ch, acc, scale);
                             }
                         }
@@ -801,13 +809,15 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
     a.qblocks = (g.d.Len_q + HW - 1) / HW;
     // deterministic mode: a fixed-point reduction is four 64-bit atomics per
     // lane and corner, so merging pays on every level
-    // four or two queries a warp: the coarse levels (every level in
-    // deterministic mode; at two queries every level measured slower in fp32
-    // mode: 444 against 383 us on the encoder with 64 channels a set); one
-    // query a warp (128 channels or more): every level, a merged entry saving
-    // at least a whole row of reductions
+    // Levels merged: every level in deterministic mode (a fixed-point reduction
+    // costs four); in fp32 mode the coarse levels, and every level where a
+    // warp holds one query of 256 channels, whose merged entry saves two 512-byte
+    // rows of reductions.  Measured on the encoder with G sets: 64 channels
+    // every level 444 against 383 us coarse; 128 channels 409 against 385 us;
+    // 256 channels 373 against 389 us.
     const unsigned all_levels = (1u << g.d.L) - 1u;
-    a.merge_mask = HW == 1 ? all_levels : (HW == 4 || HW == 2) ? (det ? all_levels : merge_levels(g)) : 0u;
+    constexpr bool kMergeable = HW == 4 || HW == 2 || HW == 1;
+    a.merge_mask = !kMergeable ? 0u : (det || (HW == 1 && BwdLanes<D>::NV == 2)) ? all_levels : merge_levels(g);
     // fused: a row's weights are softmax outputs, summing to 1 (n_levels with
     // the per-level softmax)
     const float row_sum = g.d.per_level_softmax ? (float)g.d.L : 1.f;
