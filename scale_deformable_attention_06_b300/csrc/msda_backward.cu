@@ -10,9 +10,9 @@
 // 解析" §2.3 (continuous, so the gradient reaches the offset branch).
 //
 // Work decomposition.  A warp owns HW consecutive queries of one (n, head m)
-// ("head-major"), every lane 4 channels of one of them (R = D / 4 lanes per
-// query, HW = 32 / R); the warps of a block own consecutive query groups of
-// the same head.  Per chunk of up to RC samples:
+// ("head-major"), every lane NV vectors of 4 channels of one of them
+// (R = min(D / 4, 32) lanes per query, HW = 32 / R); the warps of a block own
+// consecutive query groups of the same head.  Per chunk of up to RC samples:
 //   phase 1: one 32-byte corner record per (query, sample) into warp-private
 //            shared memory: the four corners' element offsets (clamped inside
 //            the map, see pack_record), fx, fy, A and the inside-mask; reads
@@ -28,8 +28,8 @@
 // sampled levels of problems of 32 or 64 channels a set the HW = 4 or 2
 // queries of a warp are neighbours, so on a coarse level their corners often
 // coincide; where a warp holds one query of 128 or 256 channels, that query's
-// own samples coincide often enough on every level, and a merged entry saves
-// a whole row of reductions.  The table sums, per distinct corner pixel, one coefficient per
+// own samples coincide too, and a merged entry saves a whole row of
+// reductions.  The table sums, per distinct corner pixel, one coefficient per
 // query, and one reduction per distinct pixel carries sum_h alpha_h * g_h.
 // Either way every contribution is added exactly once.
 //
@@ -86,12 +86,13 @@ __device__ __forceinline__ void scatter4(const BwdArgs &a, size_t dst, int ch, f
 constexpr int kBwdWarpsPerBlock = 4;
 
 constexpr unsigned kEmptyKey = 0xffffffffu;
-// Merge-table slots per warp; a merge chunk has at most 64 entries.  fp32
-// mode merges only the coarse levels (a quarter or less of a chunk's entries
-// distinct): 64 slots, whose smaller footprint leaves the SM more L1 (encoder
-// backward 405 -> 392 us).  Deterministic mode merges every level, up to
-// three quarters distinct on the finest: 128 slots keep its probe chains
-// short (64 measured 1-2% slower there).
+// Merge-table slots per warp; a merge chunk has at most 64 entries (16 with
+// one query a warp).  fp32 mode merges the coarse levels (a quarter or less
+// of a chunk's entries distinct), every level only with one query a warp:
+// 64 slots, whose smaller footprint leaves the SM more L1 (encoder backward
+// 405 -> 392 us).  Deterministic mode merges every level, up to three
+// quarters distinct on the finest: 128 slots keep its probe chains short (64
+// measured 1-2% slower there).
 template <bool DET>
 constexpr int merge_slots() { return DET ? 128 : 64; }
 constexpr int kMergeSamples = 4;       // samples per merge chunk (4 queries x 4 x 4 corners = 64 entries)
