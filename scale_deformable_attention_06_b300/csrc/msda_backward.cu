@@ -589,6 +589,38 @@ __global__ void ref_grad_kernel(const float *grad_off, float *grad_ref, int nql,
     }
 }
 
+// The same sums for small problems where n_heads * n_levels divides 32: one
+// thread per (n, q, m, l) in memory order reads its K offset gradients (K * 8
+// contiguous bytes, so a warp reads whole rows), and an xor tree over the
+// lanes of the heads (lane bits log2(L) and up, a fixed order) sums the
+// heads; the thread of head 0 writes.  M times the threads of the kernel
+// above: decoder fused backward 61.6 -> 57.5 us; on the encoder and larger
+// problems the kernel above is as fast or faster (428.6 against 430.5 us).
+__global__ void ref_grad_kernel_rows(const float *grad_off, float *grad_ref, int nqml, int M, int L, int K,
+                                     LevelTable lv) {
+    const int lane = threadIdx.x & 31;
+    for (int t0 = blockIdx.x * blockDim.x; t0 < nqml; t0 += gridDim.x * blockDim.x) {
+        const int t = t0 + (threadIdx.x & ~31) + lane;                 // whole warps in range together
+        const bool ok = t < nqml;
+        const int l = t % L, m = (t / L) % M, nq = t / (L * M);
+        float sx = 0.f, sy = 0.f;
+        if (ok) {
+            const float2 *g = reinterpret_cast<const float2 *>(grad_off) + (size_t)t * K;   // ((nq*M + m)*L + l)*K
+            for (int k = 0; k < K; ++k) {
+                const float2 v = g[k];
+                sx += v.x;
+                sy += v.y;
+            }
+        }
+        for (int o = L; o < L * M; o <<= 1) {           // the heads' lanes: bits log2(L) .. log2(L*M)-1
+            sx += __shfl_xor_sync(0xffffffffu, sx, o);
+            sy += __shfl_xor_sync(0xffffffffu, sy, o);
+        }
+        if (ok && m == 0)
+            reinterpret_cast<float2 *>(grad_ref)[(size_t)nq * L + l] = make_float2(sx * lv.Wf[l], sy * lv.Hf[l]);
+    }
+}
+
 // ---- helpers of the backward -----------------------------------------------
 __global__ void zero_f32_kernel(float4 *p, size_t n4) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
@@ -838,8 +870,15 @@ static cudaError_t launch_bwd_t(const LaunchGeometry &g, const BwdIO &io, bool d
             launch_bwd_kernel<T, D, FUSED, false>(a, det, blocks, stream);
         if (FUSED) {
             const int nql = g.d.N * g.d.Len_q * g.d.L;
-            ref_grad_kernel<<<grid_for(nql, 256), 256, 0, stream>>>(io.grad_loc, io.grad_ref, nql, g.d.M, g.d.L,
-                                                                   g.d.K, g.lv);
+            const int ML = g.d.M * g.d.L;
+            if (32 % ML == 0 && nql < (1 << 16)) {      // small problems whose heads x levels tile a warp
+                const int nqml = nql * g.d.M;
+                ref_grad_kernel_rows<<<grid_for(nqml, 256), 256, 0, stream>>>(io.grad_loc, io.grad_ref, nqml, g.d.M,
+                                                                            g.d.L, g.d.K, g.lv);
+            } else {
+                ref_grad_kernel<<<grid_for(nql, 256), 256, 0, stream>>>(io.grad_loc, io.grad_ref, nql, g.d.M, g.d.L,
+                                                                       g.d.K, g.lv);
+            }
         }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
