@@ -71,8 +71,9 @@ __device__ __forceinline__ int band_query(int p, const LevelTable &lv, int L) {
 // (encoder forward 152 -> 145 us, fused 167 -> 158 us) or seven (which
 // spills: 166 us); five (48 registers) at width 128, where the fused kernel
 // with option code would spill at 40; three at 256.  The unfused bf16 kernel
-// also runs six (decoder forward 24.6 -> 22.5 us, large unchanged); the fused
-// bf16 kernel keeps the compiler's choice, six made it spill (decoder fused
+// is held to the same 40 registers (twelve of its four-warp blocks; decoder
+// forward 24.6 -> 22.5 us, large unchanged); the fused bf16 kernel keeps the
+// compiler's choice, the 40-register bound made it spill (decoder fused
 // forward 24.6 -> 27.2 us).
 constexpr int kFwdMinBlocksF32 = 6;
 // Warps a forward block: eight for fp32 values, whose band-ordered blocks
