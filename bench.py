@@ -197,6 +197,22 @@ def profiled_traffic(kernel):
     return k.get("dram_bytes_per_launch")
 
 
+def step_kernels(step, ms):
+    """(kernel, ms a launch, key of its algorithmic bytes) of the step's two
+    calls: the fused calls' kernels under the fused step.  `ms` maps the keys
+    fwd, bwd, fused_fwd and fused_bwd to CUDA-event times."""
+    if step == "fused":
+        return {"fwd": ("msda_forward_kernel_fused", ms["fused_fwd"], "fused_fwd"),
+                "bwd": ("msda_backward_kernel_fused", ms["fused_bwd"], "fused_bwd")}
+    return {"fwd": ("msda_forward_kernel", ms["fwd"], "fwd"), "bwd": ("msda_backward_kernel", ms["bwd"], "bwd")}
+
+
+def roofline_traffic(kernel, workload):
+    """DRAM bytes a launch for the roofline: the committed counts are of the
+    encoder training workload's launches, so None for any other workload."""
+    return profiled_traffic(kernel) if workload == WORKLOAD else None
+
+
 def measured_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -367,17 +383,11 @@ def run_ours(args):
     fused_bwd_ms = statistics.mean(timed(lambda: fused_bwd(msda.MSDA_ACCUMULATE_GRAD_VALUE), reps,
                                          pre=lambda: gv.zero_()))
     peak, peak_src = measured_peak()
-    # the step's own kernels: the fused calls' under --step fused
-    if args.step == "fused":
-        kern = {"fwd": ("msda_forward_kernel_fused", fused_ms, "fused_fwd"),
-                "bwd": ("msda_backward_kernel_fused", fused_bwd_ms, "fused_bwd")}
-    else:
-        kern = {"fwd": ("msda_forward_kernel", fwd_ms, "fwd"), "bwd": ("msda_backward_kernel", bwd_ms, "bwd")}
+    kern = step_kernels(args.step, {"fwd": fwd_ms, "bwd": bwd_ms, "fused_fwd": fused_ms, "fused_bwd": fused_bwd_ms})
     dom = max(kern, key=lambda k: kern[k][1])
     name, ms, ab_key = kern[dom]
     achieved = ab[ab_key] / (ms / 1e3) / 1e9
-    # the committed DRAM counts are of the encoder training workload's launches
-    traffic = profiled_traffic(name) if args.workload == WORKLOAD else None
+    traffic = roofline_traffic(name, args.workload)
 
     # ---- the SM line-rate ceilings (probes over a value-sized buffer): the
     # forward's floor is its corner gathers at the gather rate, the backward's

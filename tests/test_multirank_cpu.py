@@ -63,6 +63,26 @@ def test_algorithmic_bytes_of_the_encoder_step():
     assert ab["bwd"] == pytest.approx(273.1e6, rel=2e-3)
 
 
+def test_roofline_follows_the_steps_own_kernels():
+    """The roofline names the kernels of the step that was timed, with bytes of
+    the same calls, and takes DRAM counts only on the workload they were
+    captured on."""
+    import workloads
+    ms = {"fwd": 0.14, "bwd": 0.38, "fused_fwd": 0.15, "fused_bwd": 0.43}
+    ab = bench.algorithmic_bytes(workloads.WORKLOADS["encoder_train"])
+    for step, names in (("forward + backward", ("msda_forward_kernel", "msda_backward_kernel")),
+                        ("fused", ("msda_forward_kernel_fused", "msda_backward_kernel_fused"))):
+        kern = bench.step_kernels(step, ms)
+        assert (kern["fwd"][0], kern["bwd"][0]) == names
+        for call, (name, t, key) in kern.items():
+            assert key in ab and t == ms[key]
+    assert bench.step_kernels("fused", ms)["bwd"][2] == "fused_bwd"
+    assert ab["fused_bwd"] > ab["bwd"]          # the fused backward also reads the reference points
+    for name in ("msda_backward_kernel", "msda_backward_kernel_fused"):
+        assert bench.roofline_traffic(name, "large") is None
+        assert bench.roofline_traffic(name, bench.WORKLOAD) == bench.profiled_traffic(name)
+
+
 def test_touched_value_bytes():
     """Byte accounting of sparse queries: whole 32-byte sectors of the rows
     the in-map corners reach, each counted once."""
