@@ -32,6 +32,18 @@ def test_header_declares_the_three_calls():
         assert name in syms
 
 
+def test_autograd_functions_refuse_host_tensors(msda):
+    """Each autograd Function is a torch.autograd.Function over the library's
+    calls: with host tensors its forward fails in the binding, before any C
+    call, like the calls it wraps."""
+    import torch
+    for fn in (msda.MSDeformAttnFunction, msda.MSDeformAttnFusedFunction, msda.MSDeformAttn3DFunction):
+        assert issubclass(fn, torch.autograd.Function)
+    v = torch.zeros(1, 4, 1, 8)
+    with pytest.raises((ValueError, TypeError)):
+        msda.MSDeformAttnFunction.apply(v, [[2, 2]], [0], torch.zeros(1, 1, 1, 1, 1, 2), torch.zeros(1, 1, 1, 1, 1))
+
+
 def test_library_exports_every_declared_symbol(msda):
     out = subprocess.run(["nm", "-D", "--defined-only", msda.LIBRARY], capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\bT\s+(msda_\w+)", out))
