@@ -11,8 +11,9 @@ Argument marshalling only: both directions run in libmsda.so.
 spatial_shapes and level_start_index take no gradient.  grad_value comes out
 of the library in fp32 and is handed to autograd in the dtype of value (bf16
 values get a bf16 gradient, as autograd requires).  `flags` is passed to the
-backward call (MSDA_DETERMINISTIC for run-to-run identical gradients);
-`options` to both calls.
+backward call (MSDA_DETERMINISTIC for run-to-run identical gradients) less
+MSDA_ACCUMULATE_GRAD_VALUE: autograd sums gradients into .grad itself;
+`options` goes to both calls.
 """
 import torch
 
@@ -21,6 +22,10 @@ from . import _capi
 
 def _grad_out(grad_output, value):
     return grad_output.to(value.dtype).contiguous()
+
+
+def _backward_flags(flags):
+    return flags & ~_capi.MSDA_ACCUMULATE_GRAD_VALUE
 
 
 class MSDeformAttnFunction(torch.autograd.Function):
@@ -36,7 +41,7 @@ class MSDeformAttnFunction(torch.autograd.Function):
                                  options=options)
         ctx.save_for_backward(value, sampling_locations, attention_weights)
         ctx.levels = (spatial_shapes, level_start_index)
-        ctx.flags, ctx.options = flags, options
+        ctx.flags, ctx.options = _backward_flags(flags), options
         return out
 
     @staticmethod
@@ -61,7 +66,7 @@ class MSDeformAttnFusedFunction(torch.autograd.Function):
                                        attention_logits, options=options)
         ctx.save_for_backward(value, reference_points, sampling_offsets, attention_logits)
         ctx.levels = (spatial_shapes, level_start_index)
-        ctx.flags, ctx.options = flags, options
+        ctx.flags, ctx.options = _backward_flags(flags), options
         return out
 
     @staticmethod
@@ -86,7 +91,7 @@ class MSDeformAttn3DFunction(torch.autograd.Function):
                                    options=options)
         ctx.save_for_backward(value, sampling_locations, attention_weights)
         ctx.levels = (spatial_shapes, level_start_index)
-        ctx.flags, ctx.options = flags, options
+        ctx.flags, ctx.options = _backward_flags(flags), options
         return out
 
     @staticmethod

@@ -225,6 +225,18 @@ def _check_backward_args(value, n_levels, sampling_locations, attention_weights,
     _check_out(grad_attention_weights, "grad_attention_weights", (N, Lq, G, L, K), torch.float32)
     return Lq, L, K
 
+def _grad_value_out(value, grad_value, flags):
+    """The grad_value the backward writes: the caller's, else a new one.  With
+    MSDA_ACCUMULATE_GRAD_VALUE the library adds into it, so a new (unwritten)
+    tensor would give garbage: the caller must pass the one to add into."""
+    if grad_value is not None:
+        return grad_value
+    if flags & MSDA_ACCUMULATE_GRAD_VALUE:
+        raise ValueError("MSDA_ACCUMULATE_GRAD_VALUE adds into the caller's grad_value: pass grad_value")
+    N, S, M, D = value.shape
+    return torch.empty((N, S, M, D), dtype=torch.float32, device=value.device)
+
+
 def problem(value, Len_q, n_levels, n_points, options=0, n_groups=0):
     N, S, M, D = value.shape
     return msda_problem(N, S, M, D, Len_q, n_levels, n_points, _dtype_code(value), options,
@@ -306,8 +318,7 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations, 
     Lq, L, K = _check_backward_args(value, lv.L, sampling_locations, attention_weights, grad_output, grad_value,
                                     grad_sampling_locations, grad_attention_weights)
     dev = value.device
-    if grad_value is None:
-        grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)
+    grad_value = _grad_value_out(value, grad_value, flags)
     if grad_sampling_locations is None:
         grad_sampling_locations = torch.empty_like(sampling_locations)
     if grad_attention_weights is None:
@@ -357,8 +368,7 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
     _check_out(grad_sampling_offsets, "grad_sampling_offsets", sampling_offsets.shape, torch.float32)
     _check_out(grad_attention_logits, "grad_attention_logits", attention_logits.shape, torch.float32)
     dev = value.device
-    if grad_value is None:
-        grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)
+    grad_value = _grad_value_out(value, grad_value, flags)
     if grad_reference_points is None:
         grad_reference_points = torch.empty_like(reference_points)
     if grad_sampling_offsets is None:
@@ -456,8 +466,7 @@ def msda3d_backward(value, spatial_shapes, level_start_index, sampling_locations
     Lq, L, K = _check_backward_args(value, lv.L, sampling_locations, attention_weights, grad_output, grad_value,
                                     grad_sampling_locations, grad_attention_weights, coords=3)
     dev = value.device
-    if grad_value is None:
-        grad_value = torch.empty((N, S, M, D), dtype=torch.float32, device=dev)
+    grad_value = _grad_value_out(value, grad_value, flags)
     if grad_sampling_locations is None:
         grad_sampling_locations = torch.empty_like(sampling_locations)
     if grad_attention_weights is None:

@@ -44,6 +44,23 @@ def test_autograd_functions_refuse_host_tensors(msda):
         msda.MSDeformAttnFunction.apply(v, [[2, 2]], [0], torch.zeros(1, 1, 1, 1, 1, 2), torch.zeros(1, 1, 1, 1, 1))
 
 
+def test_accumulate_needs_a_grad_value(msda):
+    """MSDA_ACCUMULATE_GRAD_VALUE adds into grad_value: without the caller's
+    tensor the backward bindings refuse before allocating or calling (a fresh
+    tensor would be unwritten memory).  Shapes only, so CPU tensors stand in."""
+    import torch
+    from scale_deformable_attention_06_b300 import _capi
+    v = torch.zeros((2, 5, 3, 8), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="pass grad_value"):
+        _capi._grad_value_out(v, None, msda.MSDA_ACCUMULATE_GRAD_VALUE | msda.MSDA_DETERMINISTIC)
+    fresh = _capi._grad_value_out(v, None, msda.MSDA_DETERMINISTIC)
+    assert fresh.shape == v.shape and fresh.dtype == torch.float32
+    mine = torch.ones((2, 5, 3, 8))
+    assert _capi._grad_value_out(v, mine, msda.MSDA_ACCUMULATE_GRAD_VALUE) is mine
+    src = open(_capi.__file__).read()
+    assert src.count("= _grad_value_out(value, grad_value, flags)") == 3     # msda_backward, _fused, msda3d_
+
+
 def test_library_exports_every_declared_symbol(msda):
     out = subprocess.run(["nm", "-D", "--defined-only", msda.LIBRARY], capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\bT\s+(msda_\w+)", out))

@@ -99,3 +99,19 @@ def test_3d_function_equals_the_direct_calls(msda):
     gv, gl, ga = msda.msda3d_backward(value.detach(), sh, st, loc.detach(), attn.detach(), g,
                                       flags=msda.MSDA_DETERMINISTIC, options=opt)
     assert torch.equal(value.grad, gv.to(dt)) and torch.equal(loc.grad, gl) and torch.equal(attn.grad, ga)
+
+
+def test_accumulate_flag(msda):
+    """The bindings refuse MSDA_ACCUMULATE_GRAD_VALUE without a grad_value to
+    add into; the Functions drop it (autograd sums into .grad itself)."""
+    w = _workload("f32")
+    p = H.prepared(w)
+    sh, st = p["spatial_shapes"], p["level_start_index"]
+    value, loc, attn, g = (H.dev(p[k]) for k in ("value", "sampling_locations", "attention_weights", "grad_output"))
+    with pytest.raises(ValueError, match="pass grad_value"):
+        msda.msda_backward(value, sh, st, loc, attn, g, flags=msda.MSDA_ACCUMULATE_GRAD_VALUE)
+    leaf = value.clone().requires_grad_()
+    flags = msda.MSDA_DETERMINISTIC | msda.MSDA_ACCUMULATE_GRAD_VALUE
+    msda.MSDeformAttnFunction.apply(leaf, sh, st, loc, attn, flags).backward(g)
+    gv, _, _ = msda.msda_backward(value, sh, st, loc, attn, g, flags=msda.MSDA_DETERMINISTIC)
+    assert torch.equal(leaf.grad, gv)
