@@ -156,6 +156,7 @@ def touched_value_bytes(w, loc):
 # and the headers it includes).
 KERNEL_SOURCES = {
     "msda_forward_kernel": ("msda_forward.cu", "msda_device.cuh", "msda_launch.h"),
+    "msda_forward_kernel_fused": ("msda_forward.cu", "msda_device.cuh", "msda_launch.h"),
     "msda_backward_kernel": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
     "msda_backward_kernel_fused": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
     "ref_grad_kernel": ("msda_backward.cu", "msda_device.cuh", "msda_launch.h"),
